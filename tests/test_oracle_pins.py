@@ -1,0 +1,362 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test checks the oracle against something fixed independently of its own
+code: a value the pages print (tests/golden/page_facts.txt), the OCP E4M3
+table, a library routine on a special case (torch float64 matmul, gelu, silu;
+torch's float8/bfloat16 casts), a closed form, an invariant (swap-AB, split-K)
+or brute force on tiny inputs.  They are chosen so that a dropped term, a
+wrong sign, a wrong index or a transposed operand in the oracle fails at
+least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from epilogue_tcgen05_tmem_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _facts():
+    out = {}
+    with open(os.path.join(GOLDEN, "page_facts.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, *v = line.split()
+                out[k] = v
+    return out
+
+
+def _torch_decode(p, arr):
+    """Decode input codes with torch's own casts (independent of the oracle)."""
+    t = torch.from_numpy(np.ascontiguousarray(arr))
+    if p.dtype == "bf16":
+        return t.view(torch.bfloat16).to(torch.float64)
+    if p.dtype == "e4m3":
+        return t.view(torch.float8_e4m3fn).to(torch.float64)
+    return t.to(torch.float64)
+
+
+def _bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(torch.bfloat16).to(torch.float64)
+
+
+# ------------------------------------------------------------------ codecs --
+
+def test_e4m3_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c) for c in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+    assert np.array_equal(np.signbit(ref[ok]), np.signbit(got[ok]))
+
+
+def test_e4m3_ocp_table():
+    with open(os.path.join(GOLDEN, "e4m3_ocp.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for code, val in rows:
+        got = oracle.e4m3_to_double(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+def test_bf16_decode_all_patterns_match_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits[::7]])
+    r = ref[::7]
+    assert np.array_equal(np.isnan(r), np.isnan(got))
+    ok = ~np.isnan(r)
+    assert np.array_equal(r[ok], got[ok])
+
+
+def test_bf16_rne_matches_torch_on_float32_values():
+    # Values exact in float32: torch's float32 -> bf16 cast is round to
+    # nearest even in one step, so it must agree with the oracle exactly.
+    rng = np.random.default_rng(1)
+    u = rng.integers(0, 2**32, 20000, dtype=np.uint64).astype(np.uint32)
+    u = u[(u & 0x7F800000) != 0x7F800000]              # finite only
+    ties = (u & 0xFFFF0000) | 0x8000                   # exact half-way cases
+    vals = np.concatenate([u, ties]).view(np.float32)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.bf16_from_double(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(ref, got)
+
+
+def test_bf16_rne_direct_from_double():
+    # Cases where rounding through float32 first would give another answer.
+    assert oracle.bf16_from_double(1 + 2**-8) == 0x3F80              # tie -> even
+    assert oracle.bf16_from_double(1 + 3 * 2**-8) == 0x3F82          # tie -> even (up)
+    assert oracle.bf16_from_double(1 + 2**-8 + 2**-30) == 0x3F81     # just above a tie
+    assert oracle.bf16_from_double(-(1 + 2**-8 + 2**-30)) == 0xBF81
+    assert oracle.bf16_from_double(1 + 2**-8 - 2**-40) == 0x3F80
+    assert oracle.bf16_from_double(3.0e38) == 0x7F62
+    assert oracle.bf16_from_double(3.4e38) == 0x7F80                 # past max -> inf
+    assert oracle.bf16_from_double(2**-133) == 0x0001                # smallest subnormal
+    assert oracle.bf16_from_double(2**-134) == 0x0000                # tie -> even (zero)
+    assert oracle.bf16_from_double(-0.0) == 0x8000
+    assert oracle.bf16_from_double(float("nan")) & 0x7FC0 == 0x7FC0
+
+
+# ------------------------------------------------------------- activations --
+
+def test_activations_match_torch():
+    x = torch.linspace(-12, 12, 4801, dtype=torch.float64)
+    F = torch.nn.functional
+    refs = {"gelu_erf": F.gelu(x), "gelu_tanh": F.gelu(x, approximate="tanh"),
+            "silu": F.silu(x), "relu": F.relu(x), "none": x}
+    for name, ref in refs.items():
+        got = torch.tensor([oracle.act(name, float(v)) for v in x], dtype=torch.float64)
+        # 1 + tanh(..) cancels for large negative x: bound the absolute error
+        # by a few float64 ulps of |x| there
+        tol = 1e-13 * ref.abs() + 1e-15 * (1 + x.abs())
+        assert torch.all((got - ref).abs() <= tol), name
+
+
+def test_activation_closed_forms():
+    for a in ("relu", "gelu_erf", "gelu_tanh", "silu"):
+        assert oracle.act(a, 0.0) == 0.0
+    assert oracle.act("relu", -3.0) == 0.0 and oracle.act("relu", 3.0) == 3.0
+    assert abs(oracle.act("gelu_erf", 10.0) - 10.0) < 1e-20
+    assert abs(oracle.act("gelu_erf", -10.0)) < 1e-20
+    assert abs(oracle.act("gelu_erf", 1.0) - 0.5 * (1 + math.erf(1 / math.sqrt(2)))) < 1e-15
+    for v in (0.3, 1.7, 5.0):      # SiLU(v) - SiLU(-v) = v ; GELU(v) - GELU(-v) = v
+        assert abs(oracle.act("silu", v) - oracle.act("silu", -v) - v) < 1e-14
+        assert abs(oracle.act("gelu_erf", v) - oracle.act("gelu_erf", -v) - v) < 1e-14
+        assert abs(oracle.act("gelu_tanh", v) - oracle.act("gelu_tanh", -v) - v) < 1e-14
+
+
+def test_gelu_tanh_constant_printed_on_page():
+    c0, c1 = (float(v) for v in _facts()["gelu_tanh_constants"])
+    assert abs(c0 - math.sqrt(2 / math.pi)) < 1e-8
+    # the oracle uses sqrt(2/pi) and 0.044715: check one point by the formula
+    v = 1.3
+    ref = 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + c1 * v ** 3)))
+    assert abs(oracle.act("gelu_tanh", v) - ref) < 1e-15
+
+
+# ----------------------------------------------------------- contraction --
+
+def _small(dtype, scale, M=5, N=7, K=256, **kw):
+    return inputs.make_problem(M, N, K, dtype, scale, seed=3, **kw)
+
+
+@pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel"),
+                                         ("int8", "token_channel"), ("e4m3", "block")])
+def test_accumulator_matches_torch_matmul(dtype, scale):
+    p = _small(dtype, scale, M=9, N=130, K=384)
+    _, acc, acc64 = oracle.linear(p, want_acc=True)
+    a, w = _torch_decode(p, p.A), _torch_decode(p, p.W)
+    if scale == "block":
+        sa = torch.from_numpy(p.s_a).double()
+        sw = torch.from_numpy(p.s_w).double()
+        ref = torch.zeros(p.M, p.N, dtype=torch.float64)
+        for kb in range(p.K // 128):
+            part = a[:, kb * 128:(kb + 1) * 128] @ w[:, kb * 128:(kb + 1) * 128].T
+            scale_mn = sa[:, kb][:, None] * sw[torch.arange(p.N) // 128, kb][None, :]
+            ref += scale_mn * part
+    else:
+        ref = a @ w.T
+    err = (torch.from_numpy(acc) - ref).abs().max().item()
+    assert err <= 1e-12 * max(ref.abs().max().item(), 1e-30)
+    if dtype == "int8":
+        exact = p.A.astype(np.int64) @ p.W.astype(np.int64).T
+        assert np.array_equal(acc64, exact)
+
+
+def test_transposed_operand_would_fail():
+    # W[n][k] = n + 1 and A[m][k] = m + 1 give acc = K (m+1)(n+1); with
+    # M != N != K an A.W or A^T.W reading gives other values or shapes.
+    M, N, K = 3, 5, 8
+    p = _small("bf16", "none", M, N, K)
+    p.A = inputs.to_bf16_bits(np.repeat(np.arange(1, M + 1, dtype=np.float64)[:, None], K, 1))
+    p.W = inputs.to_bf16_bits(np.repeat(np.arange(1, N + 1, dtype=np.float64)[:, None], K, 1))
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    ref = K * np.outer(np.arange(1, M + 1), np.arange(1, N + 1))
+    assert np.array_equal(acc, ref)
+
+
+def test_identity_weight():
+    K = 64
+    p = _small("bf16", "none", 4, K, K)
+    eye = inputs.to_bf16_bits(np.eye(K))
+    p.W = eye
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    assert np.array_equal(acc, _torch_decode(p, p.A).numpy())
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "int8"])
+def test_all_ones_token_channel_closed_form(dtype):
+    M, N, K = 4, 6, 96
+    p = _small(dtype, "token_channel", M, N, K)
+    one = {"e4m3": 0x38, "int8": 1}[dtype]
+    p.A = np.full((M, K), one, dtype=p.A.dtype)
+    p.W = np.full((N, K), one, dtype=p.W.dtype)
+    p.s_a = (2.0 ** -np.arange(M)).astype(np.float32)
+    p.s_w = (2.0 ** np.arange(N) / 64).astype(np.float32)
+    Y, acc, _ = oracle.linear(p, want_acc=True)
+    assert np.all(acc == K)
+    expect = K * np.outer(p.s_a.astype(np.float64), p.s_w.astype(np.float64))
+    assert np.array_equal(_bf16(Y).numpy(), expect)   # powers of two: exact in bf16
+
+
+def test_block_scale_indexing_closed_form():
+    # codes all 1.0; s_a[m][kb] = 2^-m, s_w[nb][kb] = (kb+1) 2^nb
+    M, N, K = 3, 384, 512
+    KB, NB = K // 128, N // 128
+    p = _small("e4m3", "block", M, N, K)
+    p.A = np.full((M, K), 0x38, np.uint8)
+    p.W = np.full((N, K), 0x38, np.uint8)
+    p.s_a = np.repeat((2.0 ** -np.arange(M))[:, None], KB, 1).astype(np.float32)
+    p.s_w = (np.arange(1, KB + 1)[None, :] * (2.0 ** np.arange(NB))[:, None]).astype(np.float32)
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    nb = np.arange(N) // 128
+    expect = 128.0 * (2.0 ** (nb[None, :] - np.arange(M)[:, None])) * (KB * (KB + 1) / 2)
+    assert np.array_equal(acc, expect)
+
+
+def test_int8_worst_case_fits_int32():
+    M, N, K = 2, 3, 12288
+    p = _small("int8", "token_channel", M, N, K)
+    p.A = np.full((M, K), 127, np.int8)
+    p.W = np.full((N, K), -127, np.int8)
+    _, acc, acc64 = oracle.linear(p, want_acc=True)
+    assert np.all(acc64 == -(127 ** 2) * K)
+    assert 127 ** 2 * K < 2 ** 31
+
+
+# ---------------------------------------------------------------- epilogue --
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu_erf", "gelu_tanh", "silu"])
+@pytest.mark.parametrize("pre", [False, True])
+def test_epilogue_with_zero_accumulator(act, pre):
+    """A = 0 reduces the layer to act(bias[n]) + R[m][n] (or act(bias + R)):
+    checks bias indexing by n, residual by (m, n), the order flag and the
+    activation, against torch float64 and the round-to-nearest error bound."""
+    M, N, K = 5, 9, 64
+    p = _small("bf16", "none", M, N, K, act=act, bias=True, residual=True,
+               residual_pre_act=pre)
+    p.A = np.zeros_like(p.A)
+    Y = oracle.linear(p)
+    b, r = _bf16(p.bias), _bf16(p.residual)
+    F = torch.nn.functional
+    f = {"none": lambda x: x, "relu": F.relu, "gelu_erf": F.gelu,
+         "gelu_tanh": lambda x: F.gelu(x, approximate="tanh"), "silu": F.silu}[act]
+    ref = f(b[None, :] + r) if pre else f(b)[None, :] + r
+    got = _bf16(Y)
+    assert torch.all((got - ref).abs() <= 2.0 ** -8 * ref.abs() + 1e-30)
+
+
+def test_scale_bias_act_residual_chain_special_case():
+    """Token/channel scale, bias, SiLU and residual together, against torch
+    float64 on decoded inputs (W = identity, so acc = A exactly)."""
+    M, K = 6, 128
+    p = _small("e4m3", "token_channel", M, K, K, act="silu", bias=True, residual=True)
+    p.W = np.where(np.eye(K, dtype=bool), 0x38, 0).astype(np.uint8)
+    Y = oracle.linear(p)
+    a = _torch_decode(p, p.A)
+    v = a * torch.from_numpy(p.s_a).double()[:, None] * torch.from_numpy(p.s_w).double()[None, :]
+    ref = torch.nn.functional.silu(v + _bf16(p.bias)[None, :]) + _bf16(p.residual)
+    got = _bf16(Y)
+    assert torch.all((got - ref).abs() <= 2.0 ** -8 * ref.abs() + 1e-30)
+
+
+def test_bf16_no_epilogue_is_rounded_matmul():
+    p = _small("bf16", "none", 17, 33, 320)
+    Y = oracle.linear(p)
+    ref = _torch_decode(p, p.A) @ _torch_decode(p, p.W).T
+    got = _bf16(Y)
+    assert torch.all((got - ref).abs() <= 2.0 ** -8 * ref.abs())
+
+
+# --------------------------------------------------------------- invariants --
+
+@pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel"),
+                                         ("int8", "token_channel")])
+def test_swap_ab_identity(dtype, scale):
+    """(W A^T)^T = A W^T: the oracle run with the operands' roles swapped gives
+    the transposed accumulator bit for bit."""
+    p = _small(dtype, scale, 7, 11, 256)
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    q = _small(dtype, scale, 11, 7, 256)
+    q.A, q.W, q.s_a, q.s_w = p.W, p.A, p.s_w, p.s_a
+    _, acc_t, _ = oracle.linear(q, want_acc=True)
+    assert np.array_equal(acc, acc_t.T)
+
+
+@pytest.mark.parametrize("dtype,scale,kunit", [("bf16", "none", 64), ("e4m3", "token_channel", 128),
+                                               ("int8", "token_channel", 128), ("e4m3", "block", 128)])
+@pytest.mark.parametrize("S", [1, 2, 3, 5])
+def test_split_k_invariance(dtype, scale, kunit, S):
+    p = _small(dtype, scale, 4, 6, 640)
+    _, acc, acc64 = oracle.linear(p, want_acc=True)
+    sacc, sacc64 = oracle.accum_splitk(p, S, kunit)
+    if dtype == "int8":
+        assert np.array_equal(acc64, sacc64)
+    rms = math.sqrt(float(np.mean(acc ** 2)))
+    assert np.max(np.abs(acc - sacc)) <= 1e-12 * rms
+
+
+def test_naive_and_threaded_agree_bitwise():
+    for dtype, scale in [("bf16", "none"), ("e4m3", "token_channel"),
+                         ("int8", "token_channel"), ("e4m3", "block")]:
+        p = _small(dtype, scale, 3, 130, 256, act="gelu_tanh", bias=True, residual=True)
+        y1, a1, _ = oracle.linear(p, want_acc=True, nthreads=3)
+        y2, a2, _ = oracle.linear(p, want_acc=True, naive=True)
+        assert np.array_equal(y1, y2) and np.array_equal(a1, a2)
+
+
+def test_points_match_full():
+    p = _small("e4m3", "token_channel", 6, 50, 256, act="silu", bias=True)
+    Y, acc, _ = oracle.linear(p, want_acc=True)
+    ms = np.array([0, 5, 3, 2]); ns = np.array([0, 49, 17, 2])
+    yp, ap = oracle.linear_points(p, ms, ns)
+    assert np.array_equal(yp, Y[ms, ns]) and np.array_equal(ap, acc[ms, ns])
+
+
+def test_brute_force_python_tiny():
+    """Pure-Python loops with the math module, M,N,K tiny, all flags on."""
+    for act in ("gelu_erf", "gelu_tanh", "silu", "relu"):
+        for pre in (False, True):
+            p = _small("bf16", "none", 2, 3, 4, act=act, bias=True, residual=True,
+                       residual_pre_act=pre)
+            Y = oracle.linear(p)
+            dec = lambda b: float(torch.tensor([int(b)], dtype=torch.int32).to(torch.int16)
+                                  .view(torch.bfloat16).double().item())
+            for m in range(2):
+                for n in range(3):
+                    s = sum(dec(p.A[m, k]) * dec(p.W[n, k]) for k in range(4))
+                    s += dec(p.bias[n])
+                    r = dec(p.residual[m, n])
+                    f = {"relu": lambda x: max(x, 0.0),
+                         "gelu_erf": lambda x: 0.5 * x * (1 + math.erf(x / math.sqrt(2))),
+                         "gelu_tanh": lambda x: 0.5 * x * (1 + math.tanh(
+                             math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3))),
+                         "silu": lambda x: x / (1 + math.exp(-x))}[act]
+                    v = f(s + r) if pre else f(s) + r
+                    got = dec(Y[m, n])
+                    assert abs(got - v) <= 2.0 ** -8 * abs(v) + 1e-30
+
+
+def test_degenerate_shapes():
+    for M, N, K in [(0, 5, 64), (3, 0, 64), (1, 1, 64), (2, 3, 0)]:
+        p = inputs.make_problem(M, N, K, "bf16", bias=True, seed=0)
+        Y, acc, _ = oracle.linear(p, want_acc=True)
+        assert Y.shape == (M, N)
+        if K == 0 and M and N:
+            assert np.all(acc == 0) and np.array_equal(Y, np.tile(p.bias, (M, 1)))
+
+
+def test_oracle_rejects_bad_arguments():
+    p = _small("e4m3", "block", 2, 130, 200)   # K % 128 != 0 for block scaling
+    with pytest.raises(ValueError):
+        oracle.linear(p)
