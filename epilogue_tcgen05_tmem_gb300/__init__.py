@@ -1,0 +1,257 @@
+"""GB300 (sm_103a) fused scaled linear layer: thin Python binding of the C ABI.
+
+Every function here marshals arguments into ``libeg.so`` (``include/eg.h``);
+every step of the computation runs in that library's CUDA kernels.  There is
+no fallback: when the library is missing or fails to load, the calls raise.
+Build it with ``__graft_entry__.build()`` (or ``python -m
+epilogue_tcgen05_tmem_gb300._build``).
+
+Names follow the C ABI: ``eg_plan_create``, ``eg_plan_run``,
+``eg_plan_run_unfused``, ``eg_plan_destroy``, ... and a small ``Plan`` class
+that takes torch tensors and passes their device pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libeg.so")
+
+# eg_status
+EG_OK, EG_ERR_INVALID_ARG, EG_ERR_UNSUPPORTED, EG_ERR_NO_MEMORY, EG_ERR_CUDA, \
+    EG_ERR_DEVICE_TIMEOUT, EG_ERR_NOT_TUNED = range(7)
+# eg_in_dtype / eg_scale_mode / eg_act
+DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2}
+SCALES = {"none": 0, "token_channel": 1, "block": 2}
+ACTS = {"none": 0, "relu": 1, "gelu_erf": 2, "gelu_tanh": 3, "silu": 4}
+EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RUN_GRAPH = 1, 2, 4, 8, 16
+
+EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "eg_plan_run",
+            "eg_plan_run_unfused", "eg_plan_device_status", "eg_plan_destroy",
+            "eg_plan_last_launch_count", "eg_plan_set_test_stall", "eg_status_string",
+            "eg_last_error_detail")
+
+
+class eg_problem(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
+
+
+class eg_tuning(ctypes.Structure):
+    _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {"tile_n": self.tile_n, "stages": self.stages, "split_k": self.split_k,
+                "swap_ab": self.swap_ab}
+
+
+class eg_args(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("W", ctypes.c_void_p), ("s_a", ctypes.c_void_p),
+                ("s_w", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p),
+                ("Y", ctypes.c_void_p), ("lda", ctypes.c_int64), ("ldw", ctypes.c_int64),
+                ("ldr", ctypes.c_int64), ("ldy", ctypes.c_int64)]
+
+
+class EgError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{status_string(status)}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libeg.so; raises when it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"CUDA library not built: {LIB_PATH} is missing "
+                                  "(run __graft_entry__.build())")
+            L = ctypes.CDLL(LIB_PATH)
+            vp = ctypes.c_void_p
+            L.eg_plan_create.argtypes = [ctypes.POINTER(eg_problem), ctypes.POINTER(eg_tuning),
+                                         ctypes.POINTER(vp)]
+            L.eg_plan_workspace_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+            L.eg_plan_get_tuning.argtypes = [vp, ctypes.POINTER(eg_tuning)]
+            L.eg_plan_run.argtypes = [vp, ctypes.POINTER(eg_args), vp]
+            L.eg_plan_run_unfused.argtypes = [vp, ctypes.POINTER(eg_args), vp, vp, vp]
+            L.eg_plan_device_status.argtypes = [vp]
+            L.eg_plan_destroy.argtypes = [vp]
+            L.eg_plan_last_launch_count.argtypes = [vp]
+            L.eg_plan_last_launch_count.restype = ctypes.c_int32
+            L.eg_plan_set_test_stall.argtypes = [vp, ctypes.c_uint64, ctypes.c_int32]
+            for f in ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning",
+                      "eg_plan_run", "eg_plan_run_unfused", "eg_plan_device_status",
+                      "eg_plan_destroy", "eg_plan_set_test_stall"):
+                getattr(L, f).restype = ctypes.c_int
+            L.eg_status_string.argtypes = [ctypes.c_int]
+            L.eg_status_string.restype = ctypes.c_char_p
+            L.eg_last_error_detail.argtypes = []
+            L.eg_last_error_detail.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().eg_status_string(s).decode()
+
+
+def last_error_detail() -> str:
+    return lib().eg_last_error_detail().decode()
+
+
+def _check(status: int):
+    if status != EG_OK:
+        raise EgError(status, last_error_detail())
+
+
+def make_problem(M, N, K, dtype="bf16", scale="none", act="none", flags=0) -> eg_problem:
+    return eg_problem(M, N, K, DTYPES[dtype], SCALES[scale], ACTS[act], flags)
+
+
+def make_tuning(tile_n, stages, split_k, swap_ab) -> eg_tuning:
+    return eg_tuning(tile_n, stages, split_k, int(bool(swap_ab)))
+
+
+# ------------------------------------------------------ C-ABI functions ---
+
+def eg_plan_create(problem: eg_problem, tuning: eg_tuning | None = None):
+    """Returns (status, plan handle or None)."""
+    h = ctypes.c_void_p()
+    s = lib().eg_plan_create(ctypes.byref(problem),
+                             ctypes.byref(tuning) if tuning is not None else None,
+                             ctypes.byref(h))
+    return s, (h.value if s == EG_OK else None)
+
+
+def eg_plan_run(plan, args: eg_args, stream: int | None) -> int:
+    return lib().eg_plan_run(plan, ctypes.byref(args), stream)
+
+
+def eg_plan_run_unfused(plan, args: eg_args, t1: int, t2: int, stream: int | None) -> int:
+    return lib().eg_plan_run_unfused(plan, ctypes.byref(args), t1, t2, stream)
+
+
+def eg_plan_destroy(plan) -> int:
+    return lib().eg_plan_destroy(plan)
+
+
+def eg_plan_device_status(plan) -> int:
+    return lib().eg_plan_device_status(plan)
+
+
+def eg_plan_get_tuning(plan) -> eg_tuning:
+    t = eg_tuning()
+    _check(lib().eg_plan_get_tuning(plan, ctypes.byref(t)))
+    return t
+
+
+def eg_plan_workspace_bytes(plan) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().eg_plan_workspace_bytes(plan, ctypes.byref(n)))
+    return n.value
+
+
+def eg_plan_last_launch_count(plan) -> int:
+    return lib().eg_plan_last_launch_count(plan)
+
+
+def eg_plan_set_test_stall(plan, wait_limit_ns: int, stall_producer: bool) -> int:
+    return lib().eg_plan_set_test_stall(plan, wait_limit_ns, int(bool(stall_producer)))
+
+
+# -------------------------------------------------------------- Plan -------
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class Plan:
+    """A plan for one problem; ``run`` takes torch CUDA tensors.
+
+    A [M,K] and W [N,K] hold the input codes (torch.bfloat16, torch.uint8 for
+    e4m3 codes or torch.int8), s_a/s_w float32, bias [N] and residual [M,N]
+    bf16, Y [M,N] bf16 (float32/int32 in debug mode).
+    """
+
+    def __init__(self, M, N, K, dtype="bf16", scale="none", act="none", bias=False,
+                 residual=False, residual_pre_act=False, debug_accum=False, graph=False,
+                 tuning: dict | None = None):
+        flags = 0
+        if bias:
+            flags |= EG_EPI_BIAS
+        if residual:
+            flags |= EG_EPI_RESIDUAL_PRE_ACT if residual_pre_act else EG_EPI_RESIDUAL
+        if debug_accum:
+            flags |= EG_OUT_DEBUG_ACCUM
+        if graph:
+            flags |= EG_RUN_GRAPH
+        self.problem = make_problem(M, N, K, dtype, scale, act, flags)
+        t = make_tuning(**tuning) if tuning is not None else None
+        s, h = eg_plan_create(self.problem, t)
+        _check(s)
+        self.handle = h
+        self.M, self.N, self.K = M, N, K
+
+    @property
+    def tuning(self) -> dict:
+        return eg_plan_get_tuning(self.handle).as_dict()
+
+    @property
+    def workspace_bytes(self) -> int:
+        return eg_plan_workspace_bytes(self.handle)
+
+    def args(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None) -> eg_args:
+        return eg_args(_ptr(A), _ptr(W), _ptr(s_a), _ptr(s_w), _ptr(bias), _ptr(residual),
+                       _ptr(Y), A.stride(0) if A is not None else 0,
+                       W.stride(0) if W is not None else 0,
+                       residual.stride(0) if residual is not None else 0, Y.stride(0))
+
+    @staticmethod
+    def _stream(stream):
+        if stream is None:
+            import torch
+            return torch.cuda.current_stream().cuda_stream
+        return stream
+
+    def run(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None, stream=None):
+        _check(eg_plan_run(self.handle, self.args(A, W, Y, s_a, s_w, bias, residual),
+                           self._stream(stream)))
+        return Y
+
+    def run_args(self, args: eg_args, stream=None):
+        _check(eg_plan_run(self.handle, args, self._stream(stream)))
+
+    def run_unfused(self, A, W, Y, T1, T2, s_a=None, s_w=None, bias=None, residual=None,
+                    stream=None):
+        _check(eg_plan_run_unfused(self.handle, self.args(A, W, Y, s_a, s_w, bias, residual),
+                                   _ptr(T1), _ptr(T2), self._stream(stream)))
+        return Y
+
+    def device_status(self) -> int:
+        return eg_plan_device_status(self.handle)
+
+    def last_launch_count(self) -> int:
+        return eg_plan_last_launch_count(self.handle)
+
+    def set_test_stall(self, wait_limit_ns: int, stall_producer: bool):
+        _check(eg_plan_set_test_stall(self.handle, wait_limit_ns, stall_producer))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            eg_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

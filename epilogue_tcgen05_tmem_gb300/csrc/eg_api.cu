@@ -1,0 +1,648 @@
+// eg_api.cu -- host side of the C ABI declared in include/eg.h: problem and
+// argument validation, tuning lookup, TMA descriptor encoding, launches,
+// CUDA-graph capture/replay, and the unfused comparison path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/eg.h"
+#include "eg_kernel.cuh"
+#include "eg_registry.h"
+#include "eg_tuning.h"
+
+namespace {
+
+thread_local std::string g_detail;
+
+eg_status fail(eg_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return s;
+}
+
+eg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(e == cudaErrorMemoryAllocation ? EG_ERR_NO_MEMORY : EG_ERR_CUDA, "%s: %s (%s)",
+              what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define EG_CUDA(call, what)                  \
+  do {                                       \
+    cudaError_t e_ = (call);                 \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library needs no link-time dependency on libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                        &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int elt_bytes(int dtype) { return dtype == EG_IN_BF16 ? 2 : 1; }
+
+uint64_t default_wait_limit_ns() {
+  const char* e = getenv("EG_WAIT_CAP_MS");
+  if (e && *e) {
+    const double ms = atof(e);
+    if (ms > 0) return static_cast<uint64_t>(ms * 1e6);
+  }
+  return 2000000000ull;  // 2 s
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct GraphEntry {
+  eg_args args;
+  cudaGraphExec_t exec;
+};
+
+struct eg_plan {
+  eg_problem prob{};
+  eg_tuning tune{};
+  int device = -1;
+  eg::KernelEntry ke{};
+  uint32_t smem = 0;
+  int rows = 0, cols = 0, tiles_rows = 0, tiles_cols = 0, k_tiles = 0, grid = 0;
+  int kb_count = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int* counters = nullptr;
+  int* status = nullptr;
+  uint64_t wait_limit_ns = 0;
+  int stall = 0;
+  // TMA descriptor cache (re-encoded when A/W or their strides change)
+  bool maps_valid = false;
+  const void* mapA = nullptr;
+  const void* mapW = nullptr;
+  int64_t map_lda = 0, map_ldw = 0;
+  CUtensorMap tmP{}, tmQ{};
+  std::vector<GraphEntry> graphs;
+  cudaStream_t cap_stream = nullptr;
+  int last_launches = 0;
+};
+
+namespace {
+
+eg_status validate_problem(const eg_problem* p) {
+  if (!p) return fail(EG_ERR_INVALID_ARG, "problem is NULL");
+  if (p->M < 0 || p->N < 0 || p->K < 0)
+    return fail(EG_ERR_INVALID_ARG, "negative dimension (M=%lld N=%lld K=%lld)", (long long)p->M,
+                (long long)p->N, (long long)p->K);
+  if (p->M > INT32_MAX || p->N > INT32_MAX || p->K > INT32_MAX)
+    return fail(EG_ERR_UNSUPPORTED, "dimensions must fit in int32");
+  const bool dt_ok = p->dtype == EG_IN_BF16 || p->dtype == EG_IN_E4M3 || p->dtype == EG_IN_INT8;
+  if (!dt_ok) return fail(EG_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
+  switch (p->scale) {
+    case EG_SCALE_NONE:
+      if (p->dtype != EG_IN_BF16)
+        return fail(EG_ERR_INVALID_ARG, "8-bit inputs need a scale mode");
+      break;
+    case EG_SCALE_TOKEN_CHANNEL:
+      if (p->dtype == EG_IN_BF16)
+        return fail(EG_ERR_INVALID_ARG, "bf16 inputs take EG_SCALE_NONE");
+      break;
+    case EG_SCALE_BLOCK:
+      if (p->dtype != EG_IN_E4M3)
+        return fail(EG_ERR_INVALID_ARG, "block scaling is defined for e4m3 inputs");
+      if (p->K % 128)
+        return fail(EG_ERR_INVALID_ARG, "block scaling needs K %% 128 == 0 (K=%lld)",
+                    (long long)p->K);
+      break;
+    default:
+      return fail(EG_ERR_INVALID_ARG, "unknown scale mode %d", p->scale);
+  }
+  if (p->act < EG_ACT_NONE || p->act > EG_ACT_SILU)
+    return fail(EG_ERR_INVALID_ARG, "unknown activation %d", p->act);
+  const uint32_t known =
+      EG_EPI_BIAS | EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH;
+  if (p->flags & ~known) return fail(EG_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if ((p->flags & EG_EPI_RESIDUAL) && (p->flags & EG_EPI_RESIDUAL_PRE_ACT))
+    return fail(EG_ERR_INVALID_ARG, "EG_EPI_RESIDUAL and EG_EPI_RESIDUAL_PRE_ACT exclude each other");
+  if ((p->K * elt_bytes(p->dtype)) % 16)
+    return fail(EG_ERR_INVALID_ARG, "K * element size must be a multiple of 16 bytes (K=%lld)",
+                (long long)p->K);
+  if (p->dtype == EG_IN_INT8 && p->K > 133144)
+    return fail(EG_ERR_UNSUPPORTED, "INT8 needs K <= 133144 so the int32 accumulator cannot overflow");
+  return EG_OK;
+}
+
+bool lookup_kernel(const eg_problem& p, int swap, int bn, eg::KernelEntry* ke) {
+  if (p.dtype == EG_IN_BF16) return eg::lookup_bf16(swap, bn, ke);
+  if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
+    return eg::lookup_e4m3_tc(swap, bn, ke);
+  if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_BLOCK)
+    return eg::lookup_e4m3_block(swap, bn, ke);
+  if (p.dtype == EG_IN_INT8) return eg::lookup_int8_tc(swap, bn, ke);
+  return false;
+}
+
+constexpr uint32_t kMaxSmem = 232448;  // opt-in dynamic shared memory per block on sm_100/103
+
+eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEntry* ke,
+                          uint32_t* smem, int* k_tiles) {
+  if (t.swap_ab != 0 && t.swap_ab != 1)
+    return fail(EG_ERR_INVALID_ARG, "swap_ab must be 0 or 1");
+  if (!lookup_kernel(p, t.swap_ab, t.tile_n, ke))
+    return fail(EG_ERR_UNSUPPORTED, "no kernel for tile_n=%d swap_ab=%d with this dtype/scale",
+                t.tile_n, t.swap_ab);
+  if (t.stages < 2 || t.stages > 8)
+    return fail(EG_ERR_UNSUPPORTED, "stages must be in 2..8 (got %d)", t.stages);
+  const uint64_t s = ke->fixed_bytes + uint64_t(t.stages) * ke->stage_bytes;
+  if (s > kMaxSmem)
+    return fail(EG_ERR_UNSUPPORTED, "%d stages need %llu bytes of shared memory (max %u)", t.stages,
+                (unsigned long long)s, kMaxSmem);
+  *smem = static_cast<uint32_t>(s);
+  const int kt = static_cast<int>((p.K + ke->elems_per_stage - 1) / ke->elems_per_stage);
+  *k_tiles = kt;
+  if (t.split_k < 1 || t.split_k > 256)
+    return fail(EG_ERR_UNSUPPORTED, "split_k must be in 1..256 (got %d)", t.split_k);
+  if (t.split_k > (kt > 0 ? kt : 1))
+    return fail(EG_ERR_UNSUPPORTED, "split_k=%d exceeds the %d K tiles", t.split_k, kt);
+  return EG_OK;
+}
+
+int sm_count_of(int dev) {
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  return n;
+}
+
+eg_status encode_map(CUtensorMap* m, const void* base, int dtype, int64_t rows, int64_t K,
+                     int64_t ld, int box_k, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(EG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int eb = elt_bytes(dtype);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * eb)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == EG_IN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(EG_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for rows=%lld K=%lld ld=%lld",
+                static_cast<int>(r), (long long)rows, (long long)K, (long long)ld);
+  return EG_OK;
+}
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+  if (!a || !b || an == 0 || bn == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
+  if (!a) return fail(EG_ERR_INVALID_ARG, "args is NULL");
+  const eg_problem& p = pl->prob;
+  if (p.M == 0 || p.N == 0) return EG_OK;
+  const int eb = elt_bytes(p.dtype);
+  if (!a->Y) return fail(EG_ERR_INVALID_ARG, "Y is NULL");
+  if (p.K > 0 && (!a->A || !a->W)) return fail(EG_ERR_INVALID_ARG, "A or W is NULL");
+  if (p.K > 0) {
+    if (!aligned16(a->A) || !aligned16(a->W))
+      return fail(EG_ERR_INVALID_ARG, "A and W must be 16-byte aligned");
+    if (a->lda < p.K || a->ldw < p.K)
+      return fail(EG_ERR_INVALID_ARG, "lda/ldw must be >= K");
+    if ((a->lda * eb) % 16 || (a->ldw * eb) % 16)
+      return fail(EG_ERR_INVALID_ARG, "lda and ldw must be multiples of 16 bytes");
+  }
+  if (p.scale != EG_SCALE_NONE) {
+    if (!a->s_a || !a->s_w) return fail(EG_ERR_INVALID_ARG, "scaled modes need s_a and s_w");
+    if (!aligned16(a->s_a) || !aligned16(a->s_w))
+      return fail(EG_ERR_INVALID_ARG, "s_a and s_w must be 16-byte aligned");
+  }
+  const int esz = debug_out ? 4 : 2;
+  if (!aligned16(a->Y)) return fail(EG_ERR_INVALID_ARG, "Y must be 16-byte aligned");
+  if (a->ldy < p.N || (a->ldy * esz) % 16)
+    return fail(EG_ERR_INVALID_ARG, "ldy must be >= N and a multiple of 16 bytes");
+  if (!debug_out && (p.flags & EG_EPI_BIAS)) {
+    if (!a->bias) return fail(EG_ERR_INVALID_ARG, "EG_EPI_BIAS needs bias");
+    if (!aligned16(a->bias)) return fail(EG_ERR_INVALID_ARG, "bias must be 16-byte aligned");
+  }
+  const bool res = (p.flags & (EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT)) != 0;
+  if (!debug_out && res) {
+    if (!a->residual) return fail(EG_ERR_INVALID_ARG, "a residual flag needs residual");
+    if (!aligned16(a->residual)) return fail(EG_ERR_INVALID_ARG, "residual must be 16-byte aligned");
+    if (a->ldr < p.N || (a->ldr * 2) % 16)
+      return fail(EG_ERR_INVALID_ARG, "ldr must be >= N and a multiple of 16 bytes");
+  }
+  const size_t ybytes = size_t(p.M - 1) * size_t(a->ldy) * esz + size_t(p.N) * esz;
+  if (overlaps(a->Y, ybytes, a->A, size_t(p.M - 1) * a->lda * eb + size_t(p.K) * eb) ||
+      overlaps(a->Y, ybytes, a->W, size_t(p.N - 1) * a->ldw * eb + size_t(p.K) * eb) ||
+      (res && !debug_out &&
+       overlaps(a->Y, ybytes, a->residual, size_t(p.M - 1) * a->ldr * 2 + size_t(p.N) * 2)))
+    return fail(EG_ERR_INVALID_ARG, "Y must not alias A, W or the residual");
+  return EG_OK;
+}
+
+eg_status ensure_maps(eg_plan* pl, const eg_args* a) {
+  const eg_problem& p = pl->prob;
+  if (p.K == 0) return EG_OK;
+  if (pl->maps_valid && pl->mapA == a->A && pl->mapW == a->W && pl->map_lda == a->lda &&
+      pl->map_ldw == a->ldw)
+    return EG_OK;
+  const int box_k = pl->ke.elems_per_stage;
+  const int bn = pl->tune.tile_n;
+  CUtensorMap mA, mW;
+  eg_status s;
+  const bool swap = pl->tune.swap_ab != 0;
+  if ((s = encode_map(&mA, a->A, p.dtype, p.M, p.K, a->lda, box_k, swap ? bn : 128)) != EG_OK) return s;
+  if ((s = encode_map(&mW, a->W, p.dtype, p.N, p.K, a->ldw, box_k, swap ? 128 : bn)) != EG_OK) return s;
+  pl->tmP = swap ? mW : mA;
+  pl->tmQ = swap ? mA : mW;
+  pl->mapA = a->A;
+  pl->mapW = a->W;
+  pl->map_lda = a->lda;
+  pl->map_ldw = a->ldw;
+  pl->maps_valid = true;
+  return EG_OK;
+}
+
+eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t flags, void* Y,
+                        int64_t ldy) {
+  const eg_problem& p = pl->prob;
+  eg::KParams k{};
+  k.M = static_cast<int32_t>(p.M);
+  k.N = static_cast<int32_t>(p.N);
+  k.K = static_cast<int32_t>(p.K);
+  k.rows = pl->rows;
+  k.cols = pl->cols;
+  k.tiles_rows = pl->tiles_rows;
+  k.tiles_cols = pl->tiles_cols;
+  k.k_tiles = pl->k_tiles;
+  k.split_k = pl->tune.split_k;
+  k.stages = pl->tune.stages;
+  k.act = act;
+  k.flags = flags;
+  k.kb_count = pl->kb_count;
+  k.s_a = a->s_a;
+  k.s_w = a->s_w;
+  k.bias = static_cast<const __nv_bfloat16*>(a->bias);
+  k.R = static_cast<const __nv_bfloat16*>(a->residual);
+  k.ldr = a->ldr;
+  k.Y = Y;
+  k.ldy = ldy;
+  k.ws = static_cast<float*>(pl->ws);
+  k.counters = pl->counters;
+  k.status = pl->status;
+  k.wait_limit_ns = pl->wait_limit_ns;
+  k.stall_producer = pl->stall;
+  // streamed weights: hint L2 to evict them first when the grid reads each
+  // weight tile once (one tile column / row over the tokens)
+  const bool w_once = pl->tune.swap_ab ? (pl->tiles_cols == 1) : (pl->tiles_rows == 1);
+  k.evict_first_p = pl->tune.swap_ab ? w_once : 0;
+  k.evict_first_q = pl->tune.swap_ab ? 0 : w_once;
+  return k;
+}
+
+uint32_t epi_flags(uint32_t f) {
+  uint32_t k = 0;
+  if (f & EG_EPI_BIAS) k |= eg::F_BIAS;
+  if (f & EG_EPI_RESIDUAL) k |= eg::F_RES;
+  if (f & EG_EPI_RESIDUAL_PRE_ACT) k |= eg::F_RES_PRE;
+  if (f & EG_OUT_DEBUG_ACCUM) k |= eg::F_DEBUG;
+  return k;
+}
+
+eg_status launch_fused(eg_plan* pl, const eg::KParams& kp, cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(pl->grid);
+  cfg.blockDim = dim3(pl->ke.threads);
+  cfg.dynamicSmemBytes = pl->smem;
+  cfg.stream = st;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  void* args[3] = {const_cast<CUtensorMap*>(&pl->tmP), const_cast<CUtensorMap*>(&pl->tmQ),
+                   const_cast<eg::KParams*>(&kp)};
+  EG_CUDA(cudaLaunchKernelExC(&cfg, pl->ke.fn, args), "launching the fused kernel");
+  return EG_OK;
+}
+
+}  // namespace
+
+// --------------------------------------------------------- elementwise ----
+// Kernels of the unfused comparison path (8 bf16 per thread, 16-byte access).
+
+namespace eg {
+
+__device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// T2 = T1 + bias (+ R when the residual comes before the activation)
+__global__ void unfused_bias_kernel(const __nv_bfloat16* T1, const __nv_bfloat16* bias,
+                                    const __nv_bfloat16* R, int64_t ldr, __nv_bfloat16* T2,
+                                    int64_t M, int64_t N, int has_bias, int res_pre) {
+  const int64_t nv = N / 8;
+  const int64_t total = M * nv;
+  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t m = v / nv, n = (v % nv) * 8;
+    const uint4 t = *reinterpret_cast<const uint4*>(T1 + m * N + n);
+    uint4 b = make_uint4(0, 0, 0, 0), r = make_uint4(0, 0, 0, 0);
+    if (has_bias) b = *reinterpret_cast<const uint4*>(bias + n);
+    if (res_pre) r = *reinterpret_cast<const uint4*>(R + m * ldr + n);
+    const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, bw[4] = {b.x, b.y, b.z, b.w},
+                   rw[4] = {r.x, r.y, r.z, r.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint16_t e[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float x = bf(uint16_t(tw[h] >> (16 * q)));
+        if (has_bias) x += bf(uint16_t(bw[h] >> (16 * q)));
+        if (res_pre) x += bf(uint16_t(rw[h] >> (16 * q)));
+        e[q] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      }
+      o[h] = uint32_t(e[0]) | (uint32_t(e[1]) << 16);
+    }
+    *reinterpret_cast<uint4*>(T2 + m * N + n) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Y = act(T2) (+ R when the residual comes after the activation)
+__global__ void unfused_act_kernel(const __nv_bfloat16* T2, const __nv_bfloat16* R, int64_t ldr,
+                                   __nv_bfloat16* Y, int64_t ldy, int64_t M, int64_t N, int act,
+                                   int res_post) {
+  const int64_t nv = N / 8;
+  const int64_t total = M * nv;
+  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t m = v / nv, n = (v % nv) * 8;
+    const uint4 t = *reinterpret_cast<const uint4*>(T2 + m * N + n);
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if (res_post) r = *reinterpret_cast<const uint4*>(R + m * ldr + n);
+    const uint32_t tw[4] = {t.x, t.y, t.z, t.w}, rw[4] = {r.x, r.y, r.z, r.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint16_t e[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float x = act_apply(act, bf(uint16_t(tw[h] >> (16 * q))));
+        if (res_post) x += bf(uint16_t(rw[h] >> (16 * q)));
+        e[q] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      }
+      o[h] = uint32_t(e[0]) | (uint32_t(e[1]) << 16);
+    }
+    *reinterpret_cast<uint4*>(Y + m * ldy + n) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace eg
+
+// ------------------------------------------------------------------ ABI ----
+
+extern "C" {
+
+const char* eg_status_string(eg_status s) {
+  switch (s) {
+    case EG_OK: return "EG_OK";
+    case EG_ERR_INVALID_ARG: return "EG_ERR_INVALID_ARG";
+    case EG_ERR_UNSUPPORTED: return "EG_ERR_UNSUPPORTED";
+    case EG_ERR_NO_MEMORY: return "EG_ERR_NO_MEMORY";
+    case EG_ERR_CUDA: return "EG_ERR_CUDA";
+    case EG_ERR_DEVICE_TIMEOUT: return "EG_ERR_DEVICE_TIMEOUT";
+    case EG_ERR_NOT_TUNED: return "EG_ERR_NOT_TUNED";
+  }
+  return "EG_ERR_UNKNOWN";
+}
+
+const char* eg_last_error_detail(void) { return g_detail.c_str(); }
+
+eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_plan** out) {
+  if (!out) return fail(EG_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  eg_status s = validate_problem(problem);
+  if (s != EG_OK) return s;
+  const eg_problem& p = *problem;
+
+  // device checks come after the argument checks, so invalid problems are
+  // rejected without touching the GPU
+  int dev = -1;
+  EG_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  int major = 0, minor = 0;
+  EG_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "device query");
+  EG_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "device query");
+  if (major != 10 || minor != 3)
+    return fail(EG_ERR_UNSUPPORTED, "the kernels are built for sm_103a; device %d is sm_%d%d", dev,
+                major, minor);
+
+  eg_tuning t{};
+  if (tuning) {
+    t = *tuning;
+  } else if (!eg::tuning_lookup(p, sm_count_of(dev), &t)) {
+    return fail(EG_ERR_NOT_TUNED, "no tuning entry or default for this problem");
+  }
+  eg::KernelEntry ke;
+  uint32_t smem = 0;
+  int k_tiles = 0;
+  if ((s = validate_tuning(p, t, &ke, &smem, &k_tiles)) != EG_OK) return s;
+
+  eg_plan* pl = new eg_plan();
+  pl->prob = p;
+  pl->tune = t;
+  pl->device = dev;
+  pl->ke = ke;
+  pl->smem = smem;
+  pl->k_tiles = k_tiles;
+  pl->kb_count = static_cast<int>(p.K / 128);
+  const bool swap = t.swap_ab != 0;
+  pl->rows = static_cast<int>(swap ? p.N : p.M);
+  pl->cols = static_cast<int>(swap ? p.M : p.N);
+  pl->tiles_rows = (pl->rows + 127) / 128;
+  pl->tiles_cols = (pl->cols + t.tile_n - 1) / t.tile_n;
+  pl->grid = pl->tiles_rows * pl->tiles_cols * t.split_k;
+  pl->wait_limit_ns = default_wait_limit_ns();
+  auto cleanup = [&](eg_status st) {
+    eg_plan_destroy(pl);
+    return st;
+  };
+  cudaError_t e = cudaFuncSetAttribute(ke.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaFuncSetAttribute"));
+  const size_t tiles = size_t(pl->tiles_rows) * pl->tiles_cols;
+  if (t.split_k > 1 && tiles > 0) {
+    pl->ws_bytes = size_t(t.split_k) * tiles * size_t(t.tile_n) * 128 * 4;
+    if ((e = cudaMalloc(&pl->ws, pl->ws_bytes)) != cudaSuccess)
+      return cleanup(cuda_fail(e, "allocating the split-K workspace"));
+  }
+  if ((e = cudaMalloc(reinterpret_cast<void**>(&pl->counters), (tiles + 1) * sizeof(int))) !=
+          cudaSuccess ||
+      (e = cudaMalloc(reinterpret_cast<void**>(&pl->status), sizeof(int))) != cudaSuccess)
+    return cleanup(cuda_fail(e, "allocating plan counters"));
+  if ((e = cudaMemset(pl->counters, 0, (tiles + 1) * sizeof(int))) != cudaSuccess ||
+      (e = cudaMemset(pl->status, 0, sizeof(int))) != cudaSuccess ||
+      (e = cudaDeviceSynchronize()) != cudaSuccess)
+    return cleanup(cuda_fail(e, "zeroing plan counters"));
+  *out = pl;
+  return EG_OK;
+}
+
+eg_status eg_plan_workspace_bytes(const eg_plan* plan, size_t* out) {
+  if (!plan || !out) return fail(EG_ERR_INVALID_ARG, "NULL argument");
+  *out = plan->ws_bytes;
+  return EG_OK;
+}
+
+eg_status eg_plan_get_tuning(const eg_plan* plan, eg_tuning* out) {
+  if (!plan || !out) return fail(EG_ERR_INVALID_ARG, "NULL argument");
+  *out = plan->tune;
+  return EG_OK;
+}
+
+int32_t eg_plan_last_launch_count(const eg_plan* plan) { return plan ? plan->last_launches : 0; }
+
+eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns, int32_t stall_producer) {
+  if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
+  plan->wait_limit_ns = wait_limit_ns ? wait_limit_ns : default_wait_limit_ns();
+  plan->stall = stall_producer ? 1 : 0;
+  return EG_OK;
+}
+
+static eg_status run_direct(eg_plan* pl, const eg_args* a, cudaStream_t st) {
+  const eg_problem& p = pl->prob;
+  eg_status s = ensure_maps(pl, a);
+  if (s != EG_OK) return s;
+  const eg::KParams kp = make_params(pl, a, p.act, epi_flags(p.flags), a->Y, a->ldy);
+  return launch_fused(pl, kp, st);
+}
+
+eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream) {
+  if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
+  const eg_problem& p = plan->prob;
+  eg_status s = validate_args(plan, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0);
+  if (s != EG_OK) return s;
+  plan->last_launches = 0;
+  if (p.M == 0 || p.N == 0) return EG_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!(p.flags & EG_RUN_GRAPH)) {
+    if ((s = run_direct(plan, args, st)) != EG_OK) return s;
+    plan->last_launches = 1;
+    return EG_OK;
+  }
+  // graph mode: one captured graph per distinct argument set
+  for (auto& g : plan->graphs) {
+    if (memcmp(&g.args, args, sizeof(eg_args)) == 0) {
+      EG_CUDA(cudaGraphLaunch(g.exec, st), "cudaGraphLaunch");
+      plan->last_launches = 1;
+      return EG_OK;
+    }
+  }
+  if (!plan->cap_stream)
+    EG_CUDA(cudaStreamCreateWithFlags(&plan->cap_stream, cudaStreamNonBlocking), "creating the capture stream");
+  EG_CUDA(cudaStreamBeginCapture(plan->cap_stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+  s = run_direct(plan, args, plan->cap_stream);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(plan->cap_stream, &graph);
+  if (s != EG_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return s;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "end capture");
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+  plan->graphs.push_back(GraphEntry{*args, exec});
+  EG_CUDA(cudaGraphLaunch(exec, st), "cudaGraphLaunch");
+  plan->last_launches = 1;
+  return EG_OK;
+}
+
+eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1, void* T2,
+                              void* stream) {
+  if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
+  const eg_problem& p = plan->prob;
+  if (p.flags & EG_OUT_DEBUG_ACCUM)
+    return fail(EG_ERR_INVALID_ARG, "the unfused path has no debug output mode");
+  eg_status s = validate_args(plan, args, false);
+  if (s != EG_OK) return s;
+  plan->last_launches = 0;
+  if (p.M == 0 || p.N == 0) return EG_OK;
+  if (!T1 || !T2 || !aligned16(T1) || !aligned16(T2))
+    return fail(EG_ERR_INVALID_ARG, "T1 and T2 must be non-NULL and 16-byte aligned");
+  if (p.N % 8) return fail(EG_ERR_UNSUPPORTED, "the unfused path needs N %% 8 == 0");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = ensure_maps(plan, args)) != EG_OK) return s;
+  // 1) the same GEMM kernel with no epilogue terms: T1 = bf16(scaled acc)
+  const eg::KParams kp = make_params(plan, args, eg::ACT_NONE, 0u, T1, p.N);
+  if ((s = launch_fused(plan, kp, st)) != EG_OK) return s;
+  const int64_t nv = p.M * (p.N / 8);
+  const int threads = 256;
+  const int blocks = static_cast<int>((nv + threads - 1) / threads < 65535 ? (nv + threads - 1) / threads : 65535);
+  const bool pre = (p.flags & EG_EPI_RESIDUAL_PRE_ACT) != 0;
+  const bool post = (p.flags & EG_EPI_RESIDUAL) != 0;
+  // 2) T2 = T1 + bias (+ R before the activation)
+  eg::unfused_bias_kernel<<<blocks, threads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(T1), static_cast<const __nv_bfloat16*>(args->bias),
+      static_cast<const __nv_bfloat16*>(args->residual), args->ldr, static_cast<__nv_bfloat16*>(T2),
+      p.M, p.N, (p.flags & EG_EPI_BIAS) ? 1 : 0, pre ? 1 : 0);
+  EG_CUDA(cudaGetLastError(), "launching the unfused bias kernel");
+  // 3) Y = act(T2) (+ R after the activation)
+  eg::unfused_act_kernel<<<blocks, threads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(T2), static_cast<const __nv_bfloat16*>(args->residual),
+      args->ldr, static_cast<__nv_bfloat16*>(args->Y), args->ldy, p.M, p.N, p.act, post ? 1 : 0);
+  EG_CUDA(cudaGetLastError(), "launching the unfused activation kernel");
+  plan->last_launches = 3;
+  return EG_OK;
+}
+
+eg_status eg_plan_device_status(eg_plan* plan) {
+  if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
+  EG_CUDA(cudaDeviceSynchronize(), "synchronising");
+  int st = 0;
+  EG_CUDA(cudaMemcpy(&st, plan->status, sizeof(int), cudaMemcpyDeviceToHost), "reading the status word");
+  if (st != 0) {
+    EG_CUDA(cudaMemset(plan->status, 0, sizeof(int)), "clearing the status word");
+    EG_CUDA(cudaDeviceSynchronize(), "synchronising");
+    static const char* where[] = {"", "load warp", "UMMA warp", "epilogue warps", "transform warps",
+                                  "teardown"};
+    return fail(EG_ERR_DEVICE_TIMEOUT, "a device pipeline wait ran past its limit (%s)",
+                (st > 0 && st <= 5) ? where[st] : "unknown");
+  }
+  return EG_OK;
+}
+
+eg_status eg_plan_destroy(eg_plan* plan) {
+  if (!plan) return EG_OK;
+  if (plan->device >= 0) cudaDeviceSynchronize();
+  for (auto& g : plan->graphs) cudaGraphExecDestroy(g.exec);
+  if (plan->cap_stream) cudaStreamDestroy(plan->cap_stream);
+  if (plan->ws) cudaFree(plan->ws);
+  if (plan->counters) cudaFree(plan->counters);
+  if (plan->status) cudaFree(plan->status);
+  delete plan;
+  return EG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,733 @@
+// eg_kernel.cuh -- the fused scaled linear-layer kernel for sm_103a.
+//
+// One kernel computes Y = epilogue(A . W^T) and stores each output once.
+// The method follows "Helion + TorchInductor co-operation: operator fusion"
+// (sections on prologue/epilogue fusion strategies and on extensible
+// epilogues: fp32 accumulator; bias broadcast over rows; ReLU/GELU; masked
+// tails read as zero; narrowing right before the single store) and "Helion
+// linear backend in vLLM" (section "One kernel instead of three": the
+// FP8_Dynamic / W8A8_INT8 / Block_FP8 scale formats; split_k and swap_ab as
+// tunables of the one kernel).  The Hopper/A100 tile kernels described
+// there keep the accumulator in registers; on sm_103a it lives in tensor
+// memory (TMEM) and the epilogue reads it back with tcgen05.ld.
+//
+// Roles inside a CTA (one work unit = one 128 x BN output tile and one
+// K-split):
+//   warp 0      TMA producer: 2-D bulk-tensor loads of the row operand P and
+//               the column operand Q into a `stages`-deep shared-memory ring
+//               (128-byte swizzle, zero fill outside the tensor).
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (UMMA 128 x BN) and
+//               tcgen05.commit; frees TMEM at the end.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (lane quarter
+//               warp%4), per-element scale, bias, activation, residual,
+//               bf16 rounding and the single store; split-K partials go
+//               through an fp32 workspace, the last CTA of a tile to arrive
+//               reduces them in split order and runs the epilogue.
+//   warps 6..9  (INT8 only) prologue transform: int8 tiles -> fp16 tiles
+//               (exact) in the UMMA layout.
+// Rows of the UMMA are M (P = A, Q = W) or, with swap-AB, N (P = W, Q = A),
+// so TMEM lane = row and column = the other dimension.
+//
+// Promotion: for Block_FP8 each 128-wide K block is accumulated into one of
+// two TMEM buffers and the epilogue warps add s_a[m][kb] * s_w[n/128][kb] *
+// block into fp32 registers while UMMA fills the other buffer.  INT8 uses
+// the same double-buffered rhythm: each 128-wide K chunk of the fp16 UMMA
+// is an exact integer below 2^21 in fp32 and is added into int32 registers,
+// so the int32 accumulator is exact.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "eg_ptx.cuh"
+
+namespace eg {
+
+enum : int { IN_BF16 = 0, IN_E4M3 = 1, IN_INT8 = 2 };
+enum : int { SC_NONE = 0, SC_TC = 1, SC_BLOCK = 2 };
+enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_ERF = 2, ACT_GELU_TANH = 3, ACT_SILU = 4 };
+enum : uint32_t { F_BIAS = 1, F_RES = 2, F_RES_PRE = 4, F_DEBUG = 8 };
+// Device status codes (first failure wins).
+enum : int { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_EPILOGUE = 3,
+             ST_TIMEOUT_CONVERT = 4, ST_TIMEOUT_TEARDOWN = 5 };
+
+struct KParams {
+  int32_t M, N, K;
+  int32_t rows, cols;             // extents along UMMA rows / columns
+  int32_t tiles_rows, tiles_cols;
+  int32_t k_tiles;                // K tiles of 128 bytes of the input type
+  int32_t split_k;
+  int32_t stages;
+  int32_t act;
+  uint32_t flags;
+  int32_t kb_count;               // K / 128 (block scales)
+  const float* s_a;
+  const float* s_w;
+  const __nv_bfloat16* bias;
+  const __nv_bfloat16* R;
+  int64_t ldr;
+  void* Y;
+  int64_t ldy;
+  float* ws;                      // split-K partials (fp32 or int32 bits)
+  int* counters;                  // per-tile arrival counters
+  int* status;                    // device status word
+  uint64_t wait_limit_ns;
+  int32_t stall_producer;         // failure-detection test hook
+  int32_t evict_first_p;          // L2 evict-first hint on the P operand
+  int32_t evict_first_q;          // ... on the Q operand
+};
+
+template <int IN, int SC, bool SWAP, int BN>
+struct Cfg {
+  static constexpr bool kConvert = (IN == IN_INT8);
+  static constexpr bool kPromote = (SC == SC_BLOCK) || kConvert;
+  static constexpr int kAtoms = kConvert ? 2 : 1;          // 128-byte K atoms per UMMA stage
+  static constexpr int kElemsPerStage = (IN == IN_BF16) ? 64 : 128;
+  static constexpr uint32_t kPBytes = 128u * 128u * kAtoms; // UMMA operand P per stage
+  static constexpr uint32_t kQBytes = uint32_t(BN) * 128u * kAtoms;
+  static constexpr uint32_t kP8Bytes = kConvert ? 128u * 128u : 0u;  // int8 staging
+  static constexpr uint32_t kQ8Bytes = kConvert ? uint32_t(BN) * 128u : 0u;
+  static constexpr uint32_t kStageBytes = kPBytes + kQBytes + kP8Bytes + kQ8Bytes;
+  static constexpr uint32_t kTxBytes = (128u + BN) * 128u;  // bytes one stage's TMA delivers
+  static constexpr int kThreads = kConvert ? 320 : 192;
+  static constexpr int kCW = BN < 32 ? BN : 32;            // TMEM load chunk (columns)
+  static constexpr uint32_t kTmemCols =
+      (kPromote ? 2 * BN : BN) <= 32 ? 32 : (kPromote ? 2 * BN : BN);
+  static constexpr uint32_t kIdesc =
+      (IN == IN_BF16) ? idesc_f32acc(1, 1, 128, BN)
+                      : idesc_f32acc(0, 0, 128, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+  static_assert(!kPromote || BN <= 128, "promotion keeps BN fp32 values per thread");
+};
+
+template <int IN, int SC, bool SWAP, int BN>
+constexpr uint32_t smem_bytes_for(int stages) {
+  using C = Cfg<IN, SC, SWAP, BN>;
+  return 1024u + uint32_t(stages) * C::kStageBytes + 512u;
+}
+
+// ------------------------------------------------------------- helpers ----
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float act_apply(int act, float v) {
+  switch (act) {
+    case ACT_RELU: return fmaxf(v, 0.0f);
+    case ACT_GELU_ERF: return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    case ACT_GELU_TANH: {
+      const float u = 0.7978845608028654f * (v + 0.044715f * v * v * v);
+      return 0.5f * v * (1.0f + tanh_fast(u));
+    }
+    case ACT_SILU: return __fdividef(v, 1.0f + __expf(-v));
+    default: return v;
+  }
+}
+
+// Float pair (hi + lo) arithmetic for the INT8 epilogue, so that
+// acc * s_a * s_w + R is formed to ~2^-44 relative before the single bf16
+// rounding (the oracle forms it in float64).
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+__device__ __forceinline__ DF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ DF df_add(DF x, float b) {
+  const DF s = two_sum(x.hi, b);
+  return two_sum(s.hi, __fadd_rn(s.lo, x.lo));
+}
+// Exact-input product acc * (sa * sw) as a float pair.
+__device__ __forceinline__ DF df_scale_int(int32_t acc, float sa, float sw) {
+  const DF s = two_prod(sa, sw);                 // exact
+  const int32_t a0i = acc & 0xFFF;               // 0..4095
+  const int32_t a1i = acc - a0i;                 // multiple of 4096: exact in fp32
+  const float a1 = static_cast<float>(a1i), a0 = static_cast<float>(a0i);
+  const DF p = two_prod(a1, s.hi);
+  const DF q = two_prod(a0, s.hi);
+  const float t = __fmaf_rn(a1, s.lo, __fmul_rn(a0, s.lo));
+  const DF r = two_sum(p.hi, q.hi);
+  const float tail = __fadd_rn(__fadd_rn(p.lo, q.lo), __fadd_rn(t, r.lo));
+  return two_sum(r.hi, tail);
+}
+// Round hi + lo to bf16, nearest even, deciding exact ties of hi by lo.
+__device__ __forceinline__ uint16_t bf16_bits_from_df(DF v) {
+  const uint32_t u = __float_as_uint(v.hi);
+  if ((u & 0x7F800000u) == 0x7F800000u)
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v.hi));
+  const uint32_t rem = u & 0xFFFFu;
+  const uint32_t base = u >> 16;
+  bool up;
+  if (rem > 0x8000u)
+    up = true;
+  else if (rem < 0x8000u)
+    up = false;
+  else if (v.lo == 0.0f)
+    up = (base & 1u) != 0;
+  else
+    up = (v.lo > 0.0f) == (v.hi > 0.0f);
+  return static_cast<uint16_t>(base + (up ? 1u : 0u));
+}
+
+__device__ __forceinline__ float bf16_to_f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// One output element of the epilogue (float path).  `bias` and `r` are the
+// bf16 inputs already widened; unused ones are ignored by the flags.
+__device__ __forceinline__ float epi_value(float v, float scale, float bias, float r, int act,
+                                           uint32_t flags) {
+  v = v * scale;
+  if (flags & F_BIAS) v += bias;
+  if (flags & F_RES_PRE) {
+    v += r;
+    v = act_apply(act, v);
+  } else {
+    v = act_apply(act, v);
+    if (flags & F_RES) v += r;
+  }
+  return v;
+}
+
+// INT8 epilogue element: exact int32 accumulator -> bf16 bits.
+__device__ __forceinline__ uint16_t epi_int8(int32_t acc, float sa, float sw, float bias, float r,
+                                             int act, uint32_t flags) {
+  DF v = df_scale_int(acc, sa, sw);
+  if (flags & F_BIAS) v = df_add(v, bias);
+  if (flags & F_RES_PRE) {
+    v = df_add(v, r);
+    if (act != ACT_NONE) v = DF{act_apply(act, __fadd_rn(v.hi, v.lo)), 0.0f};
+  } else {
+    if (act != ACT_NONE) v = DF{act_apply(act, __fadd_rn(v.hi, v.lo)), 0.0f};
+    if (flags & F_RES) v = df_add(v, r);
+  }
+  return bf16_bits_from_df(v);
+}
+
+// ------------------------------------------------------------ epilogue ----
+
+// Apply the epilogue to CW consecutive accumulator columns of one TMEM lane
+// (= one UMMA row) and store them.  `vals` holds fp32 bits, or int32 for
+// INT8.  row = tile row index + lane row; c0 = first column of the chunk.
+template <int IN, int SC, bool SWAP, int CW>
+__device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int col0,
+                                               const uint32_t (&vals)[CW]) {
+  const bool debug = (p.flags & F_DEBUG) != 0;
+  const bool has_bias = (p.flags & F_BIAS) != 0;
+  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
+  if (!SWAP) {
+    // row = m, columns = n: a thread owns CW consecutive outputs of one row.
+    const int m = row;
+    if (m >= p.M) return;
+    if (debug) {
+      uint32_t* y = reinterpret_cast<uint32_t*>(p.Y) + static_cast<int64_t>(m) * p.ldy;
+#pragma unroll
+      for (int j = 0; j < CW; ++j)
+        if (col0 + j < p.N) y[col0 + j] = vals[j];
+      return;
+    }
+    const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
+    __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<int64_t>(m) * p.ldy;
+    const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
+    if (col0 + CW <= p.N) {
+      // full chunk: 16-byte vector loads of bias / R and vector stores of Y
+      uint32_t out[CW / 2];
+#pragma unroll
+      for (int g = 0; g < CW / 8; ++g) {
+        uint4 bv = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+        if (has_bias) bv = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + g);
+        if (has_res) rv = __ldg(reinterpret_cast<const uint4*>(rrow + col0) + g);
+        float4 sw0 = make_float4(1, 1, 1, 1), sw1 = make_float4(1, 1, 1, 1);
+        if (SC == SC_TC) {
+          sw0 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g);
+          sw1 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g + 1);
+        }
+        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+        const float sws[8] = {sw0.x, sw0.y, sw0.z, sw0.w, sw1.x, sw1.y, sw1.z, sw1.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint16_t o[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = g * 8 + h * 2 + e;
+            const float b = bf16_to_f(static_cast<uint16_t>(bw[h] >> (16 * e)));
+            const float r = bf16_to_f(static_cast<uint16_t>(rw[h] >> (16 * e)));
+            if (IN == IN_INT8) {
+              o[e] = epi_int8(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.act,
+                              p.flags);
+            } else {
+              const float s = (SC == SC_TC) ? sa * sws[h * 2 + e] : 1.0f;
+              o[e] = __bfloat16_as_ushort(__float2bfloat16_rn(
+                  epi_value(__uint_as_float(vals[j]), s, b, r, p.act, p.flags)));
+            }
+          }
+          out[g * 4 + h] = static_cast<uint32_t>(o[0]) | (static_cast<uint32_t>(o[1]) << 16);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < CW / 8; ++g)
+        reinterpret_cast<uint4*>(yrow + col0)[g] =
+            make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < CW; ++j) {
+        const int n = col0 + j;
+        if (n >= p.N) break;
+        const float b = has_bias ? __bfloat162float(p.bias[n]) : 0.0f;
+        const float r = has_res ? __bfloat162float(rrow[n]) : 0.0f;
+        const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
+        uint16_t o;
+        if (IN == IN_INT8)
+          o = epi_int8(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.act, p.flags);
+        else
+          o = __bfloat16_as_ushort(__float2bfloat16_rn(
+              epi_value(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r, p.act,
+                        p.flags)));
+        yrow[n] = __ushort_as_bfloat16(o);
+      }
+    }
+  } else {
+    // row = n, columns = m: lanes of a warp hold consecutive n, so each
+    // column's loads of R and stores of Y are coalesced across the warp.
+    const int n = row;
+    if (n >= p.N) return;
+    if (debug) {
+      uint32_t* y = reinterpret_cast<uint32_t*>(p.Y);
+#pragma unroll
+      for (int j = 0; j < CW; ++j) {
+        const int m = col0 + j;
+        if (m < p.M) y[static_cast<int64_t>(m) * p.ldy + n] = vals[j];
+      }
+      return;
+    }
+    const float b = has_bias ? __bfloat162float(p.bias[n]) : 0.0f;
+    const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
+    __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y);
+#pragma unroll
+    for (int j = 0; j < CW; ++j) {
+      const int m = col0 + j;
+      if (m >= p.M) break;
+      const float r = has_res ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+      const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
+      uint16_t o;
+      if (IN == IN_INT8)
+        o = epi_int8(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.act, p.flags);
+      else
+        o = __bfloat16_as_ushort(__float2bfloat16_rn(
+            epi_value(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r, p.act,
+                      p.flags)));
+      Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
+    }
+  }
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[CW]) {
+  if constexpr (CW == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    tmem_ld16(taddr, r);
+  }
+}
+
+// Split-K: store this split's partial for (tile, split); valid entries only.
+// Layout: [split][tile][column][128 lanes] so a warp's stores coalesce.
+template <int BN>
+__device__ __forceinline__ uint32_t* ws_slot(const KParams& p, int split, int tile, int col,
+                                             int lane_row) {
+  const int64_t tiles = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols;
+  return reinterpret_cast<uint32_t*>(p.ws) +
+         ((static_cast<int64_t>(split) * tiles + tile) * BN + col) * 128 + lane_row;
+}
+
+// ---------------------------------------------------------------- kernel ---
+
+template <int IN, int SC, bool SWAP, int BN>
+__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads, 1)
+    fused_linear_kernel(const __grid_constant__ CUtensorMap tmP,
+                        const __grid_constant__ CUtensorMap tmQ, const KParams p) {
+  using C = Cfg<IN, SC, SWAP, BN>;
+  constexpr int CW = C::kCW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  // ring layout: per stage [P | Q | P8 | Q8], each part a multiple of 1 KB
+  auto stage_base = [&](int s) { return smem + static_cast<uint32_t>(s) * C::kStageBytes; };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<uint32_t>(S) * C::kStageBytes);
+  uint64_t* full = bars;              // TMA landed (expect_tx)
+  uint64_t* empty = bars + S;         // slot free (UMMA commit, or converter)
+  uint64_t* bfull = bars + 2 * S;     // converted operands ready (INT8)
+  uint64_t* bempty = bars + 3 * S;    // converted operands consumed (INT8)
+  uint64_t* tfull = bars + 4 * S;     // [2] TMEM buffer holds a finished block
+  uint64_t* tempty = tfull + 2;       // [2] TMEM buffer drained by the epilogue
+  uint64_t* accum_full = tempty + 2;  // whole accumulator finished
+  uint64_t* mma_done = accum_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int unit = blockIdx.x;
+  const int split = unit % p.split_k;
+  const int tile = unit / p.split_k;
+  const int tile_r = tile % p.tiles_rows;
+  const int tile_c = tile / p.tiles_rows;
+  const int row0 = tile_r * 128;
+  const int col0 = tile_c * BN;
+  const int kt0 = static_cast<int>(static_cast<int64_t>(split) * p.k_tiles / p.split_k);
+  const int kt1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.k_tiles / p.split_k);
+  const int nk = kt1 - kt0;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::kConvert ? 128 : 1);
+      mbar_init(&bfull[s], 128);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(accum_full, 1);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    if (lane == 0 && !p.stall_producer && nk > 0) {
+      tma_prefetch_desc(&tmP);
+      tma_prefetch_desc(&tmQ);
+      const uint64_t pol_first = policy_evict_first();
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % S;
+        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, lim)) {
+          record_status(p.status, ST_TIMEOUT_PRODUCER);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+        uint8_t* base = stage_base(s);
+        uint8_t* dP = C::kConvert ? base + C::kPBytes + C::kQBytes : base;
+        uint8_t* dQ = C::kConvert ? base + C::kPBytes + C::kQBytes + C::kP8Bytes : base + C::kPBytes;
+        const int kx = (kt0 + i) * C::kElemsPerStage;
+        if (p.evict_first_p)
+          tma_load_2d_hint(dP, &tmP, &full[s], kx, row0, pol_first);
+        else
+          tma_load_2d(dP, &tmP, &full[s], kx, row0);
+        if (p.evict_first_q)
+          tma_load_2d_hint(dQ, &tmQ, &full[s], kx, col0, pol_first);
+        else
+          tma_load_2d(dQ, &tmQ, &full[s], kx, col0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------- UMMA issuer ----
+    if (lane == 0 && nk > 0) {
+      bool ok = true;
+      for (int i = 0; i < nk && ok; ++i) {
+        const int s = i % S;
+        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+        const int b = i & 1;
+        if (C::kPromote && !mbar_wait(&tempty[b], ((static_cast<uint32_t>(i) >> 1) & 1u) ^ 1u, lim)) {
+          record_status(p.status, ST_TIMEOUT_MMA);
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(C::kConvert ? &bfull[s] : &full[s], ph, lim)) {
+          record_status(p.status, ST_TIMEOUT_MMA);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (C::kPromote ? static_cast<uint32_t>(b * BN) : 0u);
+        const uint32_t pa = smem_u32(stage_base(s));
+        const uint32_t qa = pa + C::kPBytes;
+#pragma unroll
+        for (int a = 0; a < C::kAtoms; ++a) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = sdesc_k_sw128(pa + static_cast<uint32_t>(a) * 128u * 128u + 32u * k);
+            const uint64_t bd = sdesc_k_sw128(qa + static_cast<uint32_t>(a) * BN * 128u + 32u * k);
+            const uint32_t accum = C::kPromote ? ((a | k) != 0) : ((i | a | k) != 0);
+            if (IN == IN_E4M3)
+              umma_f8(d, ad, bd, C::kIdesc, accum);
+            else
+              umma_f16(d, ad, bd, C::kIdesc, accum);
+          }
+        }
+        umma_commit(C::kConvert ? &bempty[s] : &empty[s]);
+        if (C::kPromote) umma_commit(&tfull[b]);
+      }
+      if (!C::kPromote && ok) umma_commit(accum_full);
+      umma_commit(mma_done);
+    }
+  } else if (warp >= 6) {
+    // ---------------------------------- INT8 -> fp16 prologue transform ----
+    if constexpr (C::kConvert) {
+      const int ct = threadIdx.x - 192;  // 0..127
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % S;
+        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
+        if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[s], ph ^ 1u, lim)) {
+          record_status(p.status, ST_TIMEOUT_CONVERT);
+          break;
+        }
+        uint8_t* base = stage_base(s);
+        // Q8 follows P8; both have 128-byte swizzled rows of 128 int8.
+        // Output atoms: P16 = base (2 atoms of 128 rows), Q16 = base + kPBytes.
+#pragma unroll 1
+        for (int q = ct; q < (128 + BN) * 8; q += 128) {
+          const bool isP = q < 128 * 8;
+          const int rr = isP ? (q >> 3) : ((q - 1024) >> 3);
+          const int j = q & 7;
+          const uint8_t* src = base + C::kPBytes + C::kQBytes + (isP ? 0u : C::kP8Bytes) +
+                               rr * 128 + ((j ^ (rr & 7)) << 4);
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t x = w4[t] ^ 0x80808080u;  // byte b -> b + 128 (unsigned)
+            uint32_t lo, hi;
+            asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+            asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+            // fp16 0x64XX = 1024 + XX; subtract 1152 = 1024 + 128 -> b (exact)
+            const __half2 c = __floats2half2_rn(1152.0f, 1152.0f);
+            __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), c);
+            __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), c);
+            h[2 * t] = *reinterpret_cast<uint32_t*>(&l2);
+            h[2 * t + 1] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          // 16 fp16 = two 16-byte chunks, in atom j/4, chunks 2*(j%4), +1
+          uint8_t* atom = base + (isP ? 0u : C::kPBytes) +
+                          static_cast<uint32_t>(j >> 2) * (isP ? 128u : static_cast<uint32_t>(BN)) * 128u;
+          const int c0 = 2 * (j & 3);
+          *reinterpret_cast<uint4*>(atom + rr * 128 + (((c0) ^ (rr & 7)) << 4)) =
+              make_uint4(h[0], h[1], h[2], h[3]);
+          *reinterpret_cast<uint4*>(atom + rr * 128 + (((c0 + 1) ^ (rr & 7)) << 4)) =
+              make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&empty[s]);
+        mbar_arrive(&bfull[s]);
+      }
+    }
+  } else {
+    // ----------------------------------------------------- epilogue ----
+    const int quarter = warp & 3;
+    const int lane_row = quarter * 32 + lane;
+    const int row = row0 + lane_row;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int ept = threadIdx.x - 64;  // 0..127
+    bool ok = true;
+
+    if constexpr (C::kPromote) {
+      // ---- promotion: per 128-K block, TMEM buffer -> registers ----
+      uint32_t acc[BN];
+#pragma unroll
+      for (int c = 0; c < BN; ++c) acc[c] = 0u;  // +0.0f or int 0
+      for (int i = 0; i < nk; ++i) {
+        const int b = i & 1;
+        const uint32_t bph = (static_cast<uint32_t>(i) >> 1) & 1u;
+        float srow = 1.0f;  // scale shared by the thread's row
+        if constexpr (SC == SC_BLOCK) {
+          const int kb = kt0 + i;
+          if (!SWAP) {
+            const float sw = __ldg(p.s_w + (col0 / 128) * p.kb_count + kb);
+            srow = (row < p.M) ? __ldg(p.s_a + static_cast<int64_t>(row) * p.kb_count + kb) * sw
+                               : 0.0f;
+          } else {
+            srow = __ldg(p.s_w + tile_r * p.kb_count + kb);
+          }
+        }
+        if (!mbar_wait(&tfull[b], bph, lim)) {
+          record_status(p.status, ST_TIMEOUT_EPILOGUE);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BN; c += CW) {
+          uint32_t r[CW];
+          tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(b * BN + c), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            if constexpr (SC == SC_BLOCK) {
+              float s = srow;
+              if (SWAP) {
+                const int m = col0 + c + j;
+                s = (m < p.M) ? srow * __ldg(p.s_a + static_cast<int64_t>(m) * p.kb_count + kt0 + i)
+                              : 0.0f;
+              }
+              acc[c + j] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[j]),
+                                                      __uint_as_float(acc[c + j])));
+            } else {
+              acc[c + j] = static_cast<uint32_t>(static_cast<int32_t>(acc[c + j]) +
+                                                 __float2int_rn(__uint_as_float(r[j])));
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[b]);
+      }
+      if (ok) {
+        bool do_epi = true;
+        if (p.split_k > 1) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (row < p.rows && col0 + c < p.cols) __stcg(ws_slot<BN>(p, split, tile, c, lane_row), acc[c]);
+          __threadfence();
+          epi_bar_sync();
+          if (ept == 0) {
+            const int prev = atomicAdd(p.counters + tile, 1);
+            const int last = (prev == p.split_k - 1);
+            if (last) atomicExch(p.counters + tile, 0);
+            *last_flag = last;
+          }
+          epi_bar_sync();
+          do_epi = *last_flag != 0;
+          if (do_epi) {
+            __threadfence();
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+              uint32_t tot = 0u;
+              if (row < p.rows && col0 + c < p.cols) {
+                for (int s2 = 0; s2 < p.split_k; ++s2) {
+                  const uint32_t v = (s2 == split) ? acc[c] : __ldcg(ws_slot<BN>(p, s2, tile, c, lane_row));
+                  if (IN == IN_INT8)
+                    tot = static_cast<uint32_t>(static_cast<int32_t>(tot) + static_cast<int32_t>(v));
+                  else
+                    tot = __float_as_uint(s2 == 0 ? __uint_as_float(v)
+                                                  : __fadd_rn(__uint_as_float(tot), __uint_as_float(v)));
+                }
+              }
+              acc[c] = tot;
+            }
+          }
+        }
+        if (do_epi) {
+#pragma unroll
+          for (int c = 0; c < BN; c += CW) {
+            uint32_t r[CW];
+#pragma unroll
+            for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
+            epilogue_chunk<IN, SC, SWAP, CW>(p, row, col0 + c, r);
+          }
+        }
+      }
+    } else {
+      // ---- accumulator stays in TMEM until the end ----
+      if (nk > 0) {
+        if (!mbar_wait(accum_full, 0, lim)) {
+          record_status(p.status, ST_TIMEOUT_EPILOGUE);
+          ok = false;
+        }
+        tc_fence_after();
+      }
+      if (ok) {
+        bool do_epi = true;
+        if (p.split_k > 1) {
+#pragma unroll 1
+          for (int c = 0; c < BN; c += CW) {
+            uint32_t r[CW];
+            tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(c), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < CW; ++j)
+              if (row < p.rows && col0 + c + j < p.cols)
+                __stcg(ws_slot<BN>(p, split, tile, c + j, lane_row), r[j]);
+          }
+          __threadfence();
+          epi_bar_sync();
+          if (ept == 0) {
+            const int prev = atomicAdd(p.counters + tile, 1);
+            const int last = (prev == p.split_k - 1);
+            if (last) atomicExch(p.counters + tile, 0);
+            *last_flag = last;
+          }
+          epi_bar_sync();
+          do_epi = *last_flag != 0;
+          if (do_epi) __threadfence();
+        }
+        if (do_epi) {
+#pragma unroll 1
+          for (int c = 0; c < BN; c += CW) {
+            uint32_t r[CW];
+            if (nk > 0) {
+              tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(c), r);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int j = 0; j < CW; ++j) r[j] = 0u;
+            }
+            if (p.split_k > 1) {
+#pragma unroll
+              for (int j = 0; j < CW; ++j) {
+                float tot = 0.0f;
+                if (row < p.rows && col0 + c + j < p.cols) {
+                  for (int s2 = 0; s2 < p.split_k; ++s2) {
+                    const float v = (s2 == split) ? __uint_as_float(r[j])
+                                                  : __uint_as_float(__ldcg(ws_slot<BN>(p, s2, tile, c + j, lane_row)));
+                    tot = (s2 == 0) ? v : __fadd_rn(tot, v);
+                  }
+                }
+                r[j] = __float_as_uint(tot);
+              }
+            }
+            epilogue_chunk<IN, SC, SWAP, CW>(p, row, col0 + c, r);
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown ---
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    if (nk > 0) {
+      // every UMMA this CTA issued has completed before TMEM is released
+      bool done = true;
+      if (lane == 0) done = mbar_wait(mma_done, 0, lim);
+      done = __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
+      if (!done && lane == 0) record_status(p.status, ST_TIMEOUT_TEARDOWN);
+    }
+    __syncwarp();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace eg

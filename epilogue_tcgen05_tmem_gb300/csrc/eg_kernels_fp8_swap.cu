@@ -1,0 +1,19 @@
+// eg_kernels_fp8_swap.cu -- fused kernel instantiations,
+// IN_E4M3 / SC_TC, swap_ab = 1.
+#include "eg_kernel.cuh"
+#include "eg_registry.h"
+
+namespace eg {
+
+bool lookup_e4m3_tc_swap(int bn, KernelEntry* out) {
+  switch (bn) {
+    case 16: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, true, 16);
+    case 32: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, true, 32);
+    case 64: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, true, 64);
+    case 128: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, true, 128);
+    case 256: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, true, 256);
+    default: return false;
+  }
+}
+
+}  // namespace eg

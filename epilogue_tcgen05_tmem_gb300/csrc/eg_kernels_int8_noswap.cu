@@ -1,0 +1,17 @@
+// eg_kernels_int8_noswap.cu -- fused kernel instantiations,
+// IN_INT8 / SC_TC, swap_ab = 0.
+#include "eg_kernel.cuh"
+#include "eg_registry.h"
+
+namespace eg {
+
+bool lookup_int8_tc_noswap(int bn, KernelEntry* out) {
+  switch (bn) {
+    case 16: EG_KERNEL_ENTRY(IN_INT8, SC_TC, false, 16);
+    case 32: EG_KERNEL_ENTRY(IN_INT8, SC_TC, false, 32);
+    case 64: EG_KERNEL_ENTRY(IN_INT8, SC_TC, false, 64);
+    default: return false;
+  }
+}
+
+}  // namespace eg

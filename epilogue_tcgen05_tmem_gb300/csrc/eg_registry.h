@@ -1,0 +1,40 @@
+// eg_registry.h -- host-side table of the fused kernel's instantiations.
+#pragma once
+#include <cstdint>
+
+namespace eg {
+
+struct KernelEntry {
+  const void* fn = nullptr;      // __global__ function
+  uint32_t stage_bytes = 0;      // shared memory per ring stage
+  uint32_t fixed_bytes = 0;      // alignment slack + barriers
+  int threads = 0;
+  int elems_per_stage = 0;       // K elements one stage covers
+};
+
+// Each returns false when bn has no instantiation for that kind and swap.
+#define EG_DECLARE_LOOKUP(name)                      \
+  bool name##_noswap(int bn, KernelEntry* out);      \
+  bool name##_swap(int bn, KernelEntry* out);        \
+  inline bool name(int swap, int bn, KernelEntry* out) { \
+    return swap ? name##_swap(bn, out) : name##_noswap(bn, out); \
+  }
+EG_DECLARE_LOOKUP(lookup_bf16)
+EG_DECLARE_LOOKUP(lookup_e4m3_tc)
+EG_DECLARE_LOOKUP(lookup_e4m3_block)
+EG_DECLARE_LOOKUP(lookup_int8_tc)
+#undef EG_DECLARE_LOOKUP
+
+}  // namespace eg
+
+// Instantiation helper used by the eg_kernels_*.cu files.
+#define EG_KERNEL_ENTRY(IN, SC, SWAP, BN)                                              \
+  do {                                                                                 \
+    using C_ = ::eg::Cfg<IN, SC, SWAP, BN>;                                            \
+    out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN>); \
+    out->stage_bytes = C_::kStageBytes;                                                \
+    out->fixed_bytes = 1024u + 512u;                                                   \
+    out->threads = C_::kThreads;                                                       \
+    out->elems_per_stage = C_::kElemsPerStage;                                         \
+    return true;                                                                       \
+  } while (0)

@@ -1,0 +1,202 @@
+/*
+ * eg.h -- C ABI of the fused scaled linear layer for GB300 (sm_103a).
+ *
+ * One kernel computes  Y = epilogue(A . W^T)  for a dense linear layer and
+ * stores Y once, in bf16.  The operation is defined on the pages this
+ * library follows:
+ *
+ *  - "Helion + TorchInductor co-operation: operator fusion", section
+ *    "Operator fusion strategies: prologues and epilogues": prologue fusion
+ *    applies input transforms (dequantisation, scaling) inside the tile-load
+ *    loop; epilogue fusion applies bias, residual, GELU/SiLU and the
+ *    FP32->narrow conversion to the accumulator tile right before its store.
+ *    Section "Designing extensible epilogues in Helion": an fp32
+ *    accumulator, bias broadcast over rows, ReLU or tanh-GELU, masked tails
+ *    with zero fill, a single masked store.  Section "Registering the
+ *    operator": the op checks that the inner dimensions match and allocates
+ *    nothing but its output.
+ *  - "Helion linear backend in vLLM", section "One kernel instead of three":
+ *    the scale formats FP8_Dynamic (per-token activation scale, per-channel
+ *    weight scale), W8A8_INT8 (the same scaling in INT8) and Block_FP8
+ *    (1x128 activation blocks, 128x128 weight blocks); split_k (powers of two
+ *    up to 256) and swap_ab (A@B computed as (B^T A^T)^T) are tunable
+ *    parameters of that one kernel.  Sections "Hybrid dispatch" and "How the
+ *    autotuner searches": small token counts (1..32) run a per-shape tuned
+ *    configuration under CUDA Graph replay.
+ *
+ * Per output element (m, n), with acc = sum_k a[m][k] * w[n][k]:
+ *
+ *   EG_SCALE_TOKEN_CHANNEL:  v = acc * s_a[m] * s_w[n]
+ *   EG_SCALE_BLOCK:          v = sum_kb s_a[m][kb] * s_w[n/128][kb] * (sum_{k in kb} a*w)
+ *   EG_SCALE_NONE:           v = acc
+ *   if EG_EPI_BIAS:              v += bias[n]
+ *   if EG_EPI_RESIDUAL_PRE_ACT:  v += R[m][n]; v = act(v)
+ *   else:                        v = act(v); if EG_EPI_RESIDUAL: v += R[m][n]
+ *   Y[m][n] = bf16_round_nearest_even(v)
+ *
+ * Layouts (all row-major, leading dimensions in ELEMENTS):
+ *   A  [M][lda]  activations, K contiguous (bf16, e4m3 or int8 codes)
+ *   W  [N][ldw]  weights, K contiguous (same element type as A)
+ *   s_a float32: [M] (token/channel) or [M][K/128] (block), contiguous
+ *   s_w float32: [N] (token/channel) or [ceil(N/128)][K/128] (block)
+ *   bias bf16 [N];  R bf16 [M][ldr];  Y bf16 [M][ldy]
+ *   With EG_OUT_DEBUG_ACCUM, Y is [M][ldy] of 4-byte elements instead and
+ *   receives the reduced accumulator before the epilogue: int32 for INT8
+ *   (exact), float32 otherwise (block mode: already block-scaled).
+ *
+ * Alignment rules (TMA bulk-tensor loads and 16-byte vector access):
+ *   A, W, Y, R, bias, s_a, s_w are 16-byte aligned; lda*elt, ldw*elt,
+ *   ldr*2 and ldy*2 (ldy*4 in debug mode) are multiples of 16 bytes;
+ *   K*elt is a multiple of 16 bytes.  Block scaling needs K % 128 == 0.
+ *   INT8 needs K <= 133144 so that |acc| <= 127^2 K fits in int32.
+ *
+ * Ownership: the caller owns every tensor and keeps it alive until the work
+ * queued on the stream has finished.  A plan owns its split-K workspace,
+ * its per-tile arrival counters (zeroed at creation and reset by the kernel
+ * itself), its device status word, its cached TMA descriptors and its
+ * captured graphs; eg_plan_destroy frees them after synchronising the
+ * plan's device work.  eg_plan_run allocates nothing, reads no device memory
+ * and does not synchronise.  Runs of one plan must not overlap on the GPU
+ * (they share the workspace and counters): queue them on one stream.
+ *
+ * Errors: every call returns an eg_status; eg_last_error_detail() returns a
+ * thread-local description of the last failure.  Argument errors are
+ * detected before any device work is queued.  A device-side pipeline wait
+ * that exceeds its time limit makes the kernel record the failure in the
+ * plan's status word and return without hanging; eg_plan_device_status()
+ * reports it as EG_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef EG_H
+#define EG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define EG_API __attribute__((visibility("default")))
+#else
+#define EG_API
+#endif
+
+typedef enum {
+  EG_OK = 0,
+  EG_ERR_INVALID_ARG = 1,   /* null / misaligned / inconsistent argument */
+  EG_ERR_UNSUPPORTED = 2,   /* valid but not supported (device, shape, tuning) */
+  EG_ERR_NO_MEMORY = 3,     /* device allocation failed */
+  EG_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
+  EG_ERR_DEVICE_TIMEOUT = 5,/* a device pipeline wait ran past its limit */
+  EG_ERR_NOT_TUNED = 6      /* no tuning entry and no default applies */
+} eg_status;
+
+typedef enum { EG_IN_BF16 = 0, EG_IN_E4M3 = 1, EG_IN_INT8 = 2 } eg_in_dtype;
+
+typedef enum {
+  EG_SCALE_NONE = 0,          /* bf16 inputs only */
+  EG_SCALE_TOKEN_CHANNEL = 1, /* FP8_Dynamic / W8A8_INT8: s_a[m] * s_w[n] */
+  EG_SCALE_BLOCK = 2          /* Block_FP8: 1x128 activation, 128x128 weight */
+} eg_scale_mode;
+
+typedef enum {
+  EG_ACT_NONE = 0,
+  EG_ACT_RELU = 1,
+  EG_ACT_GELU_ERF = 2,   /* 0.5 v (1 + erf(v / sqrt 2)) */
+  EG_ACT_GELU_TANH = 3,  /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) */
+  EG_ACT_SILU = 4        /* v / (1 + exp(-v)) */
+} eg_act;
+
+enum {
+  EG_EPI_BIAS = 1,
+  EG_EPI_RESIDUAL = 2,          /* v = act(v) + R */
+  EG_EPI_RESIDUAL_PRE_ACT = 4,  /* v = act(v + R)  (excludes EG_EPI_RESIDUAL) */
+  EG_OUT_DEBUG_ACCUM = 8,       /* write the raw reduced accumulator */
+  EG_RUN_GRAPH = 16             /* eg_plan_run replays a captured CUDA graph */
+};
+
+typedef struct {
+  int64_t M, N, K;
+  int32_t dtype;  /* eg_in_dtype */
+  int32_t scale;  /* eg_scale_mode */
+  int32_t act;    /* eg_act */
+  uint32_t flags; /* EG_EPI_* | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH */
+} eg_problem;
+
+/* One point of the kernel's tuning space.  The UMMA tile is 128 rows by
+ * tile_n columns; rows run over M, or over N when swap_ab is set. */
+typedef struct {
+  int32_t tile_n;   /* UMMA N: 16, 32, 64, 128 or 256 */
+  int32_t stages;   /* shared-memory ring depth, 2..8 */
+  int32_t split_k;  /* 1..256, at most the number of K tiles */
+  int32_t swap_ab;  /* 0: rows over M;  1: rows over N (Y^T = W A^T) */
+} eg_tuning;
+
+typedef struct {
+  const void* A;
+  const void* W;
+  const float* s_a;
+  const float* s_w;
+  const void* bias;      /* bf16 [N], needed with EG_EPI_BIAS */
+  const void* residual;  /* bf16 [M][ldr], needed with a residual flag */
+  void* Y;
+  int64_t lda, ldw, ldr, ldy;
+} eg_args;
+
+typedef struct eg_plan eg_plan;
+
+/* Validate `problem`, pick a tuning (`tuning` overrides the built-in table;
+ * NULL uses the table, then a default rule), allocate the plan's workspace,
+ * counters and status word on the current device.  Returns
+ * EG_ERR_INVALID_ARG for an inconsistent problem, EG_ERR_UNSUPPORTED for an
+ * unsupported device or tuning, EG_ERR_NO_MEMORY / EG_ERR_CUDA on device
+ * failures.  On success *out owns a new plan. */
+EG_API eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning,
+                         eg_plan** out);
+
+/* Bytes of split-K workspace the plan holds (0 when split_k == 1). */
+EG_API eg_status eg_plan_workspace_bytes(const eg_plan* plan, size_t* out);
+
+/* The tuning the plan runs. */
+EG_API eg_status eg_plan_get_tuning(const eg_plan* plan, eg_tuning* out);
+
+/* Queue one fused linear-layer call on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream).  With EG_RUN_GRAPH the call is captured once per
+ * distinct argument set into a CUDA graph and replayed on later calls. */
+EG_API eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream);
+
+/* The unfused comparison path of the same problem: the same GEMM kernel
+ * with no epilogue writes bf16 T1 [M][N]; a second kernel writes
+ * T2 = T1 + bias (+ R for the pre-activation order); a third writes
+ * Y = act(T2) (+ R for the default order).  T1 and T2 are caller-owned bf16
+ * [M][N] buffers (row stride N).  Three launches; for measurement only. */
+EG_API eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1,
+                              void* T2, void* stream);
+
+/* Synchronise the plan's last queued work and report a device-side wait
+ * timeout recorded by its kernels (EG_ERR_DEVICE_TIMEOUT, then cleared). */
+EG_API eg_status eg_plan_device_status(eg_plan* plan);
+
+/* Free everything the plan owns.  NULL is accepted. */
+EG_API eg_status eg_plan_destroy(eg_plan* plan);
+
+/* Number of kernel launches the last eg_plan_run / eg_plan_run_unfused
+ * queued (a graph replay counts the kernels inside it). */
+EG_API int32_t eg_plan_last_launch_count(const eg_plan* plan);
+
+/* Testing hook for failure detection: limit every device pipeline wait of
+ * this plan to `wait_limit_ns` nanoseconds (0 restores the default of
+ * 2 s), and, when `stall_producer` is non-zero, have the load warp issue no
+ * loads so that the first wait runs out.  No fault, trap or hang results:
+ * the kernel records EG_ERR_DEVICE_TIMEOUT and returns. */
+EG_API eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns,
+                                 int32_t stall_producer);
+
+EG_API const char* eg_status_string(eg_status s);
+EG_API const char* eg_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EG_H */

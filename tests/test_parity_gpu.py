@@ -1,0 +1,269 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bounds:
+  * INT8: int32 accumulators bit-exact (debug output), bf16 outputs within
+    1 bf16 ulp without split-K (checked with split-K too);
+  * everything else: max |Y - Y_oracle| <= 1e-2 * rms(Y_oracle);
+  * float32 debug accumulators: max |acc - acc_oracle| <= 1e-4 * rms.
+"""
+import numpy as np
+import pytest
+import torch
+
+import epilogue_tcgen05_tmem_gb300 as eg
+import oracle
+from epilogue_tcgen05_tmem_gb300 import inputs
+from tests._gpu_helpers import (assert_close_rms, bits, make_plan, run, to_device,
+                                ulp_dist)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from epilogue_tcgen05_tmem_gb300 import _build
+    _build.build()
+    eg.lib()
+
+
+def check_full(p, tuning=None, rel=1e-2):
+    y, _ = run(p, tuning)
+    ref = oracle.linear(p)
+    if p.dtype == "int8" and (tuning is None or tuning.get("split_k", 1) >= 1):
+        d = ulp_dist(bits(y), ref)
+        assert d.max() <= 1, f"int8 ulp distance {d.max()}"
+    else:
+        assert_close_rms(bits(y), ref, rel)
+    return y
+
+
+# ------------------------------------------------------------ bf16 -------
+
+def test_bf16_small_workload_default_tuning():
+    # M=64 N=256 K=512, +bias, exact GELU
+    check_full(inputs.workload("bf16_small"))
+
+
+@pytest.mark.parametrize("tuning", [
+    dict(tile_n=64, stages=2, split_k=1, swap_ab=0),
+    dict(tile_n=128, stages=4, split_k=1, swap_ab=0),
+    dict(tile_n=256, stages=3, split_k=1, swap_ab=0),
+    dict(tile_n=16, stages=4, split_k=1, swap_ab=0),
+    dict(tile_n=64, stages=4, split_k=1, swap_ab=1),
+    dict(tile_n=128, stages=4, split_k=2, swap_ab=0),
+    dict(tile_n=64, stages=3, split_k=4, swap_ab=1),
+])
+def test_bf16_small_workload_tunings(tuning):
+    check_full(inputs.workload("bf16_small"), tuning)
+
+
+ODD = [(1, 8, 64), (3, 24, 72), (17, 136, 200), (31, 200, 136), (33, 64, 512),
+       (130, 264, 520), (129, 129 + 7, 64 * 3 + 8)]
+
+
+@pytest.mark.parametrize("M,N,K", ODD)
+@pytest.mark.parametrize("swap", [0, 1])
+def test_bf16_ragged_shapes(M, N, K, swap):
+    p = inputs.make_problem(M, N, K, "bf16", act="gelu_tanh", bias=True, residual=True, seed=11)
+    bn = 64 if not swap else (16 if M <= 16 else 32 if M <= 32 else 64)
+    check_full(p, dict(tile_n=bn, stages=3, split_k=1, swap_ab=swap))
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu_erf", "gelu_tanh", "silu"])
+@pytest.mark.parametrize("pre", [False, True])
+def test_bf16_every_epilogue(act, pre):
+    p = inputs.make_problem(70, 192, 320, "bf16", act=act, bias=True, residual=True,
+                            residual_pre_act=pre, seed=5)
+    check_full(p)
+    check_full(p, dict(tile_n=32, stages=4, split_k=3, swap_ab=1))
+
+
+@pytest.mark.parametrize("S", [2, 3, 5, 8])
+@pytest.mark.parametrize("swap", [0, 1])
+def test_split_k_bf16_and_determinism(S, swap):
+    p = inputs.make_problem(40, 320, 1024, "bf16", act="silu", bias=True, seed=7)
+    t = dict(tile_n=64, stages=4, split_k=S, swap_ab=swap)
+    plan = make_plan(p, t)
+    assert plan.workspace_bytes > 0
+    d = to_device(p)
+    y1, _ = run(p, plan=plan, d=d)
+    y2, _ = run(p, plan=plan, d=d)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), "split-K not deterministic"
+    assert_close_rms(bits(y1), oracle.linear(p))
+    plan.close()
+
+
+def test_k_zero_and_empty_problems():
+    p = inputs.make_problem(5, 24, 0, "bf16", act="gelu_erf", bias=True, seed=1)
+    y, _ = run(p)
+    assert np.array_equal(bits(y), oracle.linear(p))
+    for M, N in [(0, 16), (4, 0)]:
+        q = inputs.make_problem(M, N, 64, "bf16", seed=1)
+        plan = make_plan(q)
+        d = to_device(q)
+        plan.run(d["A"], d["W"], d["Y"])
+        assert plan.last_launch_count() == 0
+        plan.close()
+
+
+# ------------------------------------------------------------ FP8 -------
+
+@pytest.mark.parametrize("M", inputs.DECODE_TOKENS)
+def test_fp8_token_channel_small(M):
+    p = inputs.make_problem(M, 384, 1024, "e4m3", "token_channel", act="silu", bias=True,
+                            outlier_frac=0.01, seed=2)
+    check_full(p)
+    check_full(p, dict(tile_n=32 if M > 16 else 16, stages=4, split_k=4, swap_ab=1))
+    check_full(p, dict(tile_n=64, stages=4, split_k=2, swap_ab=0))
+
+
+def test_fp8_token_channel_large_m():
+    p = inputs.make_problem(300, 520, 768, "e4m3", "token_channel", act="gelu_tanh",
+                            bias=True, residual=True, seed=4)
+    check_full(p)
+    check_full(p, dict(tile_n=256, stages=4, split_k=1, swap_ab=0))
+
+
+def _sampled(p, y, npts=3000, seed=0, int8_ulp=False):
+    rng = np.random.default_rng(seed)
+    ms = np.concatenate([rng.integers(0, p.M, npts), np.full(8, p.M - 1), np.zeros(8, int)])
+    ns = np.concatenate([rng.integers(0, p.N, npts), np.arange(p.N - 8, p.N), np.arange(8)])
+    ref, _ = oracle.linear_points(p, ms, ns)
+    got = bits(y)[ms, ns]
+    if int8_ulp:
+        assert ulp_dist(got, ref).max() <= 1
+    else:
+        assert_close_rms(got, ref)
+
+
+@pytest.mark.parametrize("M", inputs.DECODE_TOKENS)
+def test_fp8_dynamic_full_size_sampled(M):
+    """K=4096 N=12288 decode linear, default (bench) tuning, sampled outputs."""
+    p = inputs.workload("fp8_dynamic", M)
+    y, _ = run(p)
+    _sampled(p, y)
+
+
+# ------------------------------------------------------------ INT8 ------
+
+@pytest.mark.parametrize("M,N,K", [(1, 136, 384), (7, 256, 1024), (32, 384, 2048), (130, 200, 640)])
+def test_int8_exact_accumulator_and_one_ulp(M, N, K):
+    p = inputs.make_problem(M, N, K, "int8", "token_channel", residual=True, seed=9)
+    yacc, _ = run(p, debug=True)
+    _, _, acc64 = oracle.linear(p, want_acc=True)
+    assert np.array_equal(yacc.numpy().astype(np.int64), acc64), "int32 accumulator not exact"
+    for t in (None, dict(tile_n=16 if M <= 16 else 32 if M <= 32 else 64, stages=3,
+                         split_k=3, swap_ab=1),
+              dict(tile_n=64, stages=3, split_k=1, swap_ab=0)):
+        y, _ = run(p, t)
+        d = ulp_dist(bits(y), oracle.linear(p))
+        assert d.max() <= 1, f"tuning {t}: {d.max()} ulp"
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_w8a8_int8_full_size(M):
+    p = inputs.workload("w8a8_int8", M)
+    yacc, _ = run(p, debug=True)
+    rng = np.random.default_rng(1)
+    ms = rng.integers(0, M, 2000)
+    ns = rng.integers(0, p.N, 2000)
+    _, acc = oracle.linear_points(p, ms, ns)
+    assert np.array_equal(yacc.numpy()[ms, ns].astype(np.int64), acc.astype(np.int64))
+    y, _ = run(p)
+    _sampled(p, y, int8_ulp=True)
+
+
+# ------------------------------------------------------- Block FP8 ------
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (8, 384, 1024), (32, 130, 384), (200, 264, 640)])
+def test_block_fp8_small(M, N, K):
+    p = inputs.make_problem(M, N, K, "e4m3", "block", seed=13)
+    check_full(p)
+    check_full(p, dict(tile_n=32, stages=4, split_k=2, swap_ab=1))
+    check_full(p, dict(tile_n=128, stages=4, split_k=1, swap_ab=0))
+
+
+@pytest.mark.parametrize("M", [1, 32])
+def test_block_fp8_full_size_sampled(M):
+    p = inputs.workload("block_fp8", M)
+    y, _ = run(p)
+    _sampled(p, y)
+
+
+# ------------------------------------------------- debug accumulators ---
+
+@pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel"),
+                                         ("e4m3", "block")])
+def test_debug_float_accumulators(dtype, scale):
+    p = inputs.make_problem(20, 256, 512, dtype, scale, seed=21)
+    yacc, _ = run(p, debug=True)
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    rms = float(np.sqrt(np.mean(acc ** 2)))
+    assert float(np.max(np.abs(yacc.numpy().astype(np.float64) - acc))) <= 1e-4 * rms
+
+
+# ------------------------------------------------ graphs / unfused ------
+
+def test_graph_mode_matches_direct_and_recaptures():
+    p = inputs.make_problem(16, 512, 1024, "e4m3", "token_channel", act="silu", bias=True, seed=3)
+    ref = oracle.linear(p)
+    plan = make_plan(p, graph=True)
+    d1, d2 = to_device(p), to_device(p)
+    for _ in range(3):
+        y1, _ = run(p, plan=plan, d=d1)
+        assert plan.last_launch_count() == 1
+    y2, _ = run(p, plan=plan, d=d2)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert_close_rms(bits(y2), ref)
+    plan.close()
+
+
+@pytest.mark.parametrize("pre", [False, True])
+def test_unfused_path(pre):
+    p = inputs.make_problem(96, 512, 768, "bf16", act="gelu_tanh", bias=True, residual=True,
+                            residual_pre_act=pre, seed=8)
+    plan = make_plan(p)
+    d = to_device(p)
+    T1 = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
+    T2 = torch.empty_like(T1)
+    plan.run_unfused(d["A"], d["W"], d["Y"], T1, T2, d["s_a"], d["s_w"], d["bias"], d["residual"])
+    torch.cuda.synchronize()
+    assert plan.last_launch_count() == 3
+    assert_close_rms(bits(d["Y"].cpu()), oracle.linear(p))
+    plan.run(d["A"], d["W"], d["Y"], d["s_a"], d["s_w"], d["bias"], d["residual"])
+    assert plan.last_launch_count() == 1
+    plan.close()
+
+
+# ---------------------------------------------- failure detection -------
+
+def test_device_wait_timeout_reported_without_hang():
+    p = inputs.make_problem(8, 256, 512, "bf16", seed=1)
+    plan = make_plan(p)
+    d = to_device(p)
+    plan.set_test_stall(5_000_000, True)           # 5 ms, load warp idle
+    plan.run(d["A"], d["W"], d["Y"])
+    assert plan.device_status() == eg.EG_ERR_DEVICE_TIMEOUT
+    plan.set_test_stall(0, False)
+    y, _ = run(p, plan=plan, d=d)
+    assert_close_rms(bits(y), oracle.linear(p))
+    plan.close()
+
+
+def test_run_argument_errors():
+    p = inputs.make_problem(8, 64, 128, "bf16", bias=True, seed=1)
+    plan = make_plan(p)
+    d = to_device(p)
+    bad = plan.args(d["A"], d["W"], d["Y"], bias=d["bias"])
+    bad.A = bad.A + 2                                          # misaligned
+    assert eg.eg_plan_run(plan.handle, bad, None) == eg.EG_ERR_INVALID_ARG
+    alias = plan.args(d["A"], d["W"], d["Y"], bias=d["bias"])
+    alias.Y = alias.A                                          # Y aliases A
+    assert eg.eg_plan_run(plan.handle, alias, None) == eg.EG_ERR_INVALID_ARG
+    nob = plan.args(d["A"], d["W"], d["Y"])
+    assert eg.eg_plan_run(plan.handle, nob, None) == eg.EG_ERR_INVALID_ARG
+    with pytest.raises(eg.EgError):
+        make_plan(p, dict(tile_n=48, stages=4, split_k=1, swap_ab=0))
+    with pytest.raises(eg.EgError):
+        make_plan(p, dict(tile_n=64, stages=4, split_k=3, swap_ab=0))   # 2 K tiles only
+    plan.close()
