@@ -16,8 +16,9 @@ here).  Per-bucket microseconds per call are reported beside it.
 
 ``--impl reference`` times the CPU oracle (plain C, float64) on a bounded
 sample of the same workload instead.
-``--config NAME`` measures another workload (bf16_small, w8a8_int8,
-block_fp8, prefill_bf16, prefill_unfused) and prints its own line.
+``--config NAME`` measures another workload (bf16_small, fp8_calls,
+w8a8_int8, block_fp8, prefill_bf16, prefill_unfused; ``--m`` picks token
+counts) and prints its own line.
 """
 from __future__ import annotations
 
@@ -50,6 +51,7 @@ def parse():
     ap.add_argument("--config", default="fp8_dynamic")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--m", default=None, help="token counts for --config runs, e.g. 1,16")
     return ap.parse_args()
 
 
@@ -169,12 +171,11 @@ def run_native(args):
     # ---- workload: token buckets x weight sets -----------------------------
     base = inputs.workload("fp8_dynamic", 32, seed=0)
     tokens = list(inputs.DECODE_TOKENS)
-    wsets = [(base.W, base.s_w, base.bias)]
     Wd = [weight_set(base, 0, torch)] + [weight_set(base, 100 + i, torch) for i in range(NSETS - 1)]
     plans, acts = {}, {}
     for M in tokens:
         p = inputs.take_tokens(base, M)
-        plans[M] = eg.Plan(M, p.N, p.K, p.dtype, p.scale, p.act, bias=True)
+        plans[M] = eg.Plan(M, p.N, p.K, p.dtype, p.scale, p.act, bias=True, pdl=True)
         d = device_problem(p, torch)
         acts[M] = d
     bytes_per_call = {M: traffic.algorithmic_bytes(M, base.N, base.K, "e4m3", "token_channel",
@@ -415,16 +416,21 @@ def run_config(args):
     unfused = name == "prefill_unfused"
     wl = "prefill_bf16" if unfused else name
     Ms = [None]
-    if wl == "w8a8_int8":
+    if wl in ("w8a8_int8", "fp8_calls"):
         Ms = list(inputs.DECODE_TOKENS)
     elif wl == "block_fp8":
         Ms = [1, 8, 32, 2048]
+    if args.m:
+        Ms = [int(x) for x in args.m.split(",")]
+    if wl == "fp8_calls":
+        wl = "fp8_dynamic"
     rows = []
     for M in Ms:
         p = inputs.workload(wl, M)
         d = device_problem(p, torch)
         plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
-                       residual=p.residual is not None, residual_pre_act=p.residual_pre_act)
+                       residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
+                       pdl=not unfused)
         nb = traffic.problem_bytes(p)
         fl = traffic.flops(p.M, p.N, p.K)
         # rotate weight copies so repeated calls do not hit L2

@@ -26,12 +26,16 @@ EG_OK, EG_ERR_INVALID_ARG, EG_ERR_UNSUPPORTED, EG_ERR_NO_MEMORY, EG_ERR_CUDA, \
 DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2}
 SCALES = {"none": 0, "token_channel": 1, "block": 2}
 ACTS = {"none": 0, "relu": 1, "gelu_erf": 2, "gelu_tanh": 3, "silu": 4}
-EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RUN_GRAPH = 1, 2, 4, 8, 16
+EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RUN_GRAPH, \
+    EG_RUN_PDL = 1, 2, 4, 8, 16, 32
 
 EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "eg_plan_run",
             "eg_plan_run_unfused", "eg_plan_device_status", "eg_plan_destroy",
-            "eg_plan_last_launch_count", "eg_plan_set_test_stall", "eg_status_string",
-            "eg_last_error_detail")
+            "eg_plan_last_launch_count", "eg_plan_set_test_stall", "eg_plan_get_launch",
+            "eg_plan_set_trace", "eg_status_string", "eg_last_error_detail")
+EG_TRACE_POINTS = 8
+TRACE_POINT_NAMES = ("start", "setup", "first_tma", "first_operands", "last_commit",
+                     "first_acc", "epilogue_done", "end")
 
 
 class eg_problem(ctypes.Structure):
@@ -42,11 +46,12 @@ class eg_problem(ctypes.Structure):
 
 class eg_tuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32)]
+                ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
+                ("stream_k", ctypes.c_int32)]
 
     def as_dict(self):
         return {"tile_n": self.tile_n, "stages": self.stages, "split_k": self.split_k,
-                "swap_ab": self.swap_ab}
+                "swap_ab": self.swap_ab, "stream_k": self.stream_k}
 
 
 class eg_args(ctypes.Structure):
@@ -54,6 +59,15 @@ class eg_args(ctypes.Structure):
                 ("s_w", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p),
                 ("Y", ctypes.c_void_p), ("lda", ctypes.c_int64), ("ldw", ctypes.c_int64),
                 ("ldr", ctypes.c_int64), ("ldy", ctypes.c_int64)]
+
+
+class eg_launch_info(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("units", ctypes.c_int32),
+                ("blocks_per_sm", ctypes.c_int32), ("regs_per_thread", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
 
 class EgError(RuntimeError):
@@ -88,9 +102,12 @@ def lib() -> ctypes.CDLL:
             L.eg_plan_last_launch_count.argtypes = [vp]
             L.eg_plan_last_launch_count.restype = ctypes.c_int32
             L.eg_plan_set_test_stall.argtypes = [vp, ctypes.c_uint64, ctypes.c_int32]
+            L.eg_plan_get_launch.argtypes = [vp, ctypes.POINTER(eg_launch_info)]
+            L.eg_plan_set_trace.argtypes = [vp, vp, ctypes.c_int32]
             for f in ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning",
                       "eg_plan_run", "eg_plan_run_unfused", "eg_plan_device_status",
-                      "eg_plan_destroy", "eg_plan_set_test_stall"):
+                      "eg_plan_destroy", "eg_plan_set_test_stall", "eg_plan_get_launch",
+                      "eg_plan_set_trace"):
                 getattr(L, f).restype = ctypes.c_int
             L.eg_status_string.argtypes = [ctypes.c_int]
             L.eg_status_string.restype = ctypes.c_char_p
@@ -117,8 +134,8 @@ def make_problem(M, N, K, dtype="bf16", scale="none", act="none", flags=0) -> eg
     return eg_problem(M, N, K, DTYPES[dtype], SCALES[scale], ACTS[act], flags)
 
 
-def make_tuning(tile_n, stages, split_k, swap_ab) -> eg_tuning:
-    return eg_tuning(tile_n, stages, split_k, int(bool(swap_ab)))
+def make_tuning(tile_n, stages, split_k, swap_ab, stream_k=0) -> eg_tuning:
+    return eg_tuning(tile_n, stages, split_k, int(bool(swap_ab)), stream_k)
 
 
 # ------------------------------------------------------ C-ABI functions ---
@@ -184,7 +201,7 @@ class Plan:
 
     def __init__(self, M, N, K, dtype="bf16", scale="none", act="none", bias=False,
                  residual=False, residual_pre_act=False, debug_accum=False, graph=False,
-                 tuning: dict | None = None):
+                 pdl=False, tuning: dict | None = None):
         flags = 0
         if bias:
             flags |= EG_EPI_BIAS
@@ -194,6 +211,8 @@ class Plan:
             flags |= EG_OUT_DEBUG_ACCUM
         if graph:
             flags |= EG_RUN_GRAPH
+        if pdl:
+            flags |= EG_RUN_PDL
         self.problem = make_problem(M, N, K, dtype, scale, act, flags)
         t = make_tuning(**tuning) if tuning is not None else None
         s, h = eg_plan_create(self.problem, t)
@@ -208,6 +227,20 @@ class Plan:
     @property
     def workspace_bytes(self) -> int:
         return eg_plan_workspace_bytes(self.handle)
+
+    @property
+    def launch_info(self) -> dict:
+        li = eg_launch_info()
+        _check(lib().eg_plan_get_launch(self.handle, ctypes.byref(li)))
+        return li.as_dict()
+
+    def set_trace(self, buf=None):
+        """Record a per-CTA timeline into ``buf`` (int64 CUDA tensor of
+        [ctas, EG_TRACE_POINTS]); None turns tracing off."""
+        if buf is None:
+            _check(lib().eg_plan_set_trace(self.handle, None, 0))
+        else:
+            _check(lib().eg_plan_set_trace(self.handle, buf.data_ptr(), buf.shape[0]))
 
     def args(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None) -> eg_args:
         return eg_args(_ptr(A), _ptr(W), _ptr(s_a), _ptr(s_w), _ptr(bias), _ptr(residual),

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -97,6 +98,10 @@ struct eg_plan {
   int* status = nullptr;
   uint64_t wait_limit_ns = 0;
   int stall = 0;
+  int l2_prefetch = 1;  // EG_PDL_L2_PREFETCH=0 turns the L2 weight prefetch off
+  int units = 0, blocks_per_sm = 0, regs = 0, max_contrib = 1;
+  uint64_t* trace = nullptr;
+  int trace_ctas = 0;
   // TMA descriptor cache (re-encoded when A/W or their strides change)
   bool maps_valid = false;
   const void* mapA = nullptr;
@@ -141,7 +146,8 @@ eg_status validate_problem(const eg_problem* p) {
   if (p->act < EG_ACT_NONE || p->act > EG_ACT_SILU)
     return fail(EG_ERR_INVALID_ARG, "unknown activation %d", p->act);
   const uint32_t known =
-      EG_EPI_BIAS | EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH;
+      EG_EPI_BIAS | EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH |
+      EG_RUN_PDL;
   if (p->flags & ~known) return fail(EG_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
   if ((p->flags & EG_EPI_RESIDUAL) && (p->flags & EG_EPI_RESIDUAL_PRE_ACT))
     return fail(EG_ERR_INVALID_ARG, "EG_EPI_RESIDUAL and EG_EPI_RESIDUAL_PRE_ACT exclude each other");
@@ -185,6 +191,12 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
     return fail(EG_ERR_UNSUPPORTED, "split_k must be in 1..256 (got %d)", t.split_k);
   if (t.split_k > (kt > 0 ? kt : 1))
     return fail(EG_ERR_UNSUPPORTED, "split_k=%d exceeds the %d K tiles", t.split_k, kt);
+  if (t.stream_k < 0 || t.stream_k > 8)
+    return fail(EG_ERR_UNSUPPORTED, "stream_k must be in 0..8 CTAs per SM (got %d)", t.stream_k);
+  if (t.stream_k > 0 && t.split_k != 1)
+    return fail(EG_ERR_INVALID_ARG, "balanced split-K (stream_k > 0) takes split_k = 1");
+  if (t.stream_k > 0 && kt == 0)
+    return fail(EG_ERR_UNSUPPORTED, "balanced split-K needs K > 0");
   return EG_OK;
 }
 
@@ -242,9 +254,9 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
       return fail(EG_ERR_INVALID_ARG, "s_a and s_w must be 16-byte aligned");
   }
   const int esz = debug_out ? 4 : 2;
-  if (!aligned16(a->Y)) return fail(EG_ERR_INVALID_ARG, "Y must be 16-byte aligned");
-  if (a->ldy < p.N || (a->ldy * esz) % 16)
-    return fail(EG_ERR_INVALID_ARG, "ldy must be >= N and a multiple of 16 bytes");
+  if (reinterpret_cast<uintptr_t>(a->Y) % esz)
+    return fail(EG_ERR_INVALID_ARG, "Y must be aligned to its element size");
+  if (a->ldy < p.N) return fail(EG_ERR_INVALID_ARG, "ldy must be >= N");
   if (!debug_out && (p.flags & EG_EPI_BIAS)) {
     if (!a->bias) return fail(EG_ERR_INVALID_ARG, "EG_EPI_BIAS needs bias");
     if (!aligned16(a->bias)) return fail(EG_ERR_INVALID_ARG, "bias must be 16-byte aligned");
@@ -252,9 +264,9 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
   const bool res = (p.flags & (EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT)) != 0;
   if (!debug_out && res) {
     if (!a->residual) return fail(EG_ERR_INVALID_ARG, "a residual flag needs residual");
-    if (!aligned16(a->residual)) return fail(EG_ERR_INVALID_ARG, "residual must be 16-byte aligned");
-    if (a->ldr < p.N || (a->ldr * 2) % 16)
-      return fail(EG_ERR_INVALID_ARG, "ldr must be >= N and a multiple of 16 bytes");
+    if (reinterpret_cast<uintptr_t>(a->residual) % 2)
+      return fail(EG_ERR_INVALID_ARG, "residual must be 2-byte aligned");
+    if (a->ldr < p.N) return fail(EG_ERR_INVALID_ARG, "ldr must be >= N");
   }
   const size_t ybytes = size_t(p.M - 1) * size_t(a->ldy) * esz + size_t(p.N) * esz;
   if (overlaps(a->Y, ybytes, a->A, size_t(p.M - 1) * a->lda * eb + size_t(p.K) * eb) ||
@@ -301,6 +313,8 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.tiles_cols = pl->tiles_cols;
   k.k_tiles = pl->k_tiles;
   k.split_k = pl->tune.split_k;
+  k.stream_k = pl->tune.stream_k > 0 ? 1 : 0;
+  k.max_contrib = pl->max_contrib;
   k.stages = pl->tune.stages;
   k.act = act;
   k.flags = flags;
@@ -317,6 +331,13 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.status = pl->status;
   k.wait_limit_ns = pl->wait_limit_ns;
   k.stall_producer = pl->stall;
+  const bool res = (flags & (eg::F_RES | eg::F_RES_PRE)) != 0;
+  k.vec_ok = aligned16(Y) && (ldy * 2) % 16 == 0 &&
+             (!res || (aligned16(a->residual) && (a->ldr * 2) % 16 == 0));
+  k.pdl = (p.flags & EG_RUN_PDL) ? 1 : 0;
+  k.l2_prefetch = pl->l2_prefetch;
+  k.trace = pl->trace;
+  k.trace_ctas = pl->trace_ctas;
   // streamed weights: hint L2 to evict them first when the grid reads each
   // weight tile once (one tile column / row over the tokens)
   const bool w_once = pl->tune.swap_ab ? (pl->tiles_cols == 1) : (pl->tiles_rows == 1);
@@ -340,8 +361,11 @@ eg_status launch_fused(eg_plan* pl, const eg::KParams& kp, cudaStream_t st) {
   cfg.blockDim = dim3(pl->ke.threads);
   cfg.dynamicSmemBytes = pl->smem;
   cfg.stream = st;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kp.pdl ? 1 : 0;
   void* args[3] = {const_cast<CUtensorMap*>(&pl->tmP), const_cast<CUtensorMap*>(&pl->tmQ),
                    const_cast<eg::KParams*>(&kp)};
   EG_CUDA(cudaLaunchKernelExC(&cfg, pl->ke.fn, args), "launching the fused kernel");
@@ -481,8 +505,9 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   pl->cols = static_cast<int>(swap ? p.M : p.N);
   pl->tiles_rows = (pl->rows + 127) / 128;
   pl->tiles_cols = (pl->cols + t.tile_n - 1) / t.tile_n;
-  pl->grid = pl->tiles_rows * pl->tiles_cols * t.split_k;
+  const int units = pl->tiles_rows * pl->tiles_cols * t.split_k;
   pl->wait_limit_ns = default_wait_limit_ns();
+  if (const char* e2 = getenv("EG_PDL_L2_PREFETCH")) pl->l2_prefetch = atoi(e2) != 0;
   auto cleanup = [&](eg_status st) {
     eg_plan_destroy(pl);
     return st;
@@ -490,9 +515,60 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   cudaError_t e = cudaFuncSetAttribute(ke.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaFuncSetAttribute"));
+  // operands arrive through TMA into shared memory: prefer the largest
+  // shared-memory carveout so that several CTAs can be resident per SM
+  e = cudaFuncSetAttribute(ke.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "setting the shared-memory carveout"));
+  cudaFuncAttributes fa{};
+  if ((e = cudaFuncGetAttributes(&fa, ke.fn)) != cudaSuccess)
+    return cleanup(cuda_fail(e, "cudaFuncGetAttributes"));
+  pl->regs = fa.numRegs;
+  // persistent grid: every resident CTA slot, at most one per work unit.
+  // Residency from the SM's limits: shared memory (with the per-block
+  // reservation), registers (allocated per warp in units of 256), threads,
+  // blocks, and the 512 TMEM columns.
+  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0, sm_blocks = 0;
+  if ((e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev)) != cudaSuccess)
+    return cleanup(cuda_fail(e, "device limits"));
+  const int warps = (ke.threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  int per_sm = sm_smem / static_cast<int>(smem + reserved);
+  per_sm = std::min(per_sm, sm_regs / std::max(1, regs_warp * warps));
+  per_sm = std::min(per_sm, sm_threads / ke.threads);
+  per_sm = std::min(per_sm, sm_blocks);
+  per_sm = std::min(per_sm, 512 / ke.tmem_cols);
+  if (per_sm < 1) return cleanup(fail(EG_ERR_UNSUPPORTED, "the kernel does not fit on an SM"));
   const size_t tiles = size_t(pl->tiles_rows) * pl->tiles_cols;
-  if (t.split_k > 1 && tiles > 0) {
-    pl->ws_bytes = size_t(t.split_k) * tiles * size_t(t.tile_n) * 128 * 4;
+  pl->blocks_per_sm = per_sm;
+  pl->max_contrib = t.split_k;
+  if (t.stream_k > 0) {
+    // balanced split-K: G CTAs share I = tiles x K-tiles iterations; CTA c
+    // owns [floor(c I/G), floor((c+1) I/G)); a tile has as many partial sums
+    // as CTAs whose ranges overlap it
+    const long long iters = static_cast<long long>(tiles) * k_tiles;
+    long long G = static_cast<long long>(sm_count_of(dev)) * std::min(per_sm, t.stream_k);
+    if (G > iters) G = iters;
+    pl->grid = static_cast<int>(G);
+    pl->units = static_cast<int>(std::min<long long>(iters, INT32_MAX));
+    int mc = 1;
+    for (size_t tile = 0; tile < tiles && G > 0; ++tile) {
+      const long long b = static_cast<long long>(tile) * k_tiles, e2 = b + k_tiles;
+      const long long first = ((b + 1) * G - 1) / iters, last = (e2 * G - 1) / iters;
+      mc = std::max(mc, static_cast<int>(last - first + 1));
+    }
+    pl->max_contrib = mc;
+  } else {
+    const long long slots = static_cast<long long>(sm_count_of(dev)) * per_sm;
+    pl->grid = static_cast<int>(units < slots ? units : slots);
+    pl->units = units;
+  }
+  if (pl->max_contrib > 1 && tiles > 0) {
+    pl->ws_bytes = size_t(pl->max_contrib) * tiles * size_t(t.tile_n) * 128 * 4;
     if ((e = cudaMalloc(&pl->ws, pl->ws_bytes)) != cudaSuccess)
       return cleanup(cuda_fail(e, "allocating the split-K workspace"));
   }
@@ -521,6 +597,29 @@ eg_status eg_plan_get_tuning(const eg_plan* plan, eg_tuning* out) {
 }
 
 int32_t eg_plan_last_launch_count(const eg_plan* plan) { return plan ? plan->last_launches : 0; }
+
+eg_status eg_plan_get_launch(const eg_plan* plan, eg_launch_info* out) {
+  if (!plan || !out) return fail(EG_ERR_INVALID_ARG, "NULL argument");
+  out->grid = plan->grid;
+  out->block = plan->ke.threads;
+  out->smem_bytes = static_cast<int32_t>(plan->smem);
+  out->units = plan->units;
+  out->blocks_per_sm = plan->blocks_per_sm;
+  out->regs_per_thread = plan->regs;
+  return EG_OK;
+}
+
+eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace_ctas) {
+  if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
+  if (trace && (trace_ctas < 0 || (reinterpret_cast<uintptr_t>(trace) & 7u)))
+    return fail(EG_ERR_INVALID_ARG, "trace must be 8-byte aligned with trace_ctas >= 0");
+  plan->trace = trace;
+  plan->trace_ctas = trace ? trace_ctas : 0;
+  // graphs captured earlier hold the old parameters
+  for (auto& g : plan->graphs) cudaGraphExecDestroy(g.exec);
+  plan->graphs.clear();
+  return EG_OK;
+}
 
 eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns, int32_t stall_producer) {
   if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");

@@ -74,7 +74,23 @@ struct KParams {
   int32_t stall_producer;         // failure-detection test hook
   int32_t evict_first_p;          // L2 evict-first hint on the P operand
   int32_t evict_first_q;          // ... on the Q operand
+  int32_t vec_ok;                 // Y (and R) rows 16-byte aligned: vector path
+  int32_t pdl;                    // launched as a programmatic dependent
+  int32_t l2_prefetch;            // ... and prefetches its weight range into L2
+  uint64_t* trace;                // per-CTA timeline (nullable), kTracePoints each
+  int32_t trace_ctas;             // CTAs the trace buffer holds
+  int32_t stream_k;               // balanced split-K over the grid (else split_k)
+  int32_t max_contrib;            // workspace slots per tile
 };
+
+constexpr int kTracePoints = 8;
+enum : int { TR_START = 0, TR_SETUP = 1, TR_FIRST_TMA = 2, TR_FIRST_OPERANDS = 3,
+             TR_LAST_COMMIT = 4, TR_FIRST_ACC = 5, TR_EPI_DONE = 6, TR_END = 7 };
+
+__device__ __forceinline__ void trace_point(const KParams& p, int point) {
+  if (p.trace != nullptr && static_cast<int>(blockIdx.x) < p.trace_ctas)
+    p.trace[static_cast<int64_t>(blockIdx.x) * kTracePoints + point] = global_timer_ns();
+}
 
 template <int IN, int SC, bool SWAP, int BN>
 struct Cfg {
@@ -89,9 +105,17 @@ struct Cfg {
   static constexpr uint32_t kStageBytes = kPBytes + kQBytes + kP8Bytes + kQ8Bytes;
   static constexpr uint32_t kTxBytes = (128u + BN) * 128u;  // bytes one stage's TMA delivers
   static constexpr int kThreads = kConvert ? 320 : 192;
+  // Small tiles (decode) are meant to run two CTAs per SM; cap registers so
+  // two fit.  Promotion with wide tiles keeps BN accumulators per thread.
+  // Decode tiles (BN 16) keep a third slot per SM free so that the next
+  // call's CTAs (programmatic dependents) become resident while this grid
+  // still runs.
+  static constexpr int kMinBlocks =
+      kConvert ? (BN <= 16 ? 2 : 1)
+               : ((kPromote && BN >= 64) || BN >= 128) ? 1 : (BN <= 16 ? 3 : 2);
   static constexpr int kCW = BN < 32 ? BN : 32;            // TMEM load chunk (columns)
-  static constexpr uint32_t kTmemCols =
-      (kPromote ? 2 * BN : BN) <= 32 ? 32 : (kPromote ? 2 * BN : BN);
+  // two accumulator buffers (per unit, or per K block when promoting)
+  static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN;
   static constexpr uint32_t kIdesc =
       (IN == IN_BF16) ? idesc_f32acc(1, 1, 128, BN)
                       : idesc_f32acc(0, 0, 128, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
@@ -223,6 +247,55 @@ __device__ __forceinline__ uint16_t epi_int8(int32_t acc, float sa, float sw, fl
 
 // ------------------------------------------------------------ epilogue ----
 
+// Swap-AB epilogue inputs of one TMEM lane (output channel n) and CW tokens
+// col0..col0+CW-1.  None depends on the accumulator, so the decode path loads
+// them before it waits for the mainloop; every load is independent and
+// predicated, so their latencies overlap.
+template <int CW>
+struct SwapIn {
+  float b, sw;
+  float sa[CW], r[CW];
+};
+
+template <int SC, int CW>
+__device__ __forceinline__ void load_swap_inputs(const KParams& p, int n, int col0, SwapIn<CW>& in) {
+  const bool nv = n < p.N;
+  const bool has_bias = (p.flags & F_BIAS) != 0;
+  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
+  in.b = (has_bias && nv) ? __bfloat162float(p.bias[n]) : 0.0f;
+  in.sw = (SC == SC_TC && nv) ? __ldg(p.s_w + n) : 1.0f;
+#pragma unroll
+  for (int j = 0; j < CW; ++j) {
+    const int m = col0 + j;
+    const bool ok = nv && m < p.M;
+    in.sa[j] = (SC == SC_TC && ok) ? __ldg(p.s_a + m) : 1.0f;
+    in.r[j] = (has_res && ok) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+  }
+}
+
+// Swap-AB epilogue compute and store: lanes of a warp hold consecutive n, so
+// each token's stores of Y are coalesced across the warp.
+template <int IN, int SC, int CW>
+__device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
+                                           const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
+  if (n >= p.N) return;
+  __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y);
+#pragma unroll
+  for (int j = 0; j < CW; ++j) {
+    const int m = col0 + j;
+    if (m < p.M) {
+      uint16_t o;
+      if (IN == IN_INT8)
+        o = epi_int8(static_cast<int32_t>(vals[j]), in.sa[j], in.sw, in.b, in.r[j], p.act, p.flags);
+      else
+        o = __bfloat16_as_ushort(__float2bfloat16_rn(
+            epi_value(__uint_as_float(vals[j]), (SC == SC_TC) ? in.sa[j] * in.sw : 1.0f, in.b,
+                      in.r[j], p.act, p.flags)));
+      Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
+    }
+  }
+}
+
 // Apply the epilogue to CW consecutive accumulator columns of one TMEM lane
 // (= one UMMA row) and store them.  `vals` holds fp32 bits, or int32 for
 // INT8.  row = tile row index + lane row; c0 = first column of the chunk.
@@ -246,7 +319,7 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
     const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
     __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<int64_t>(m) * p.ldy;
     const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
-    if (col0 + CW <= p.N) {
+    if (p.vec_ok && col0 + CW <= p.N) {
       // full chunk: 16-byte vector loads of bias / R and vector stores of Y
       uint32_t out[CW / 2];
 #pragma unroll
@@ -318,24 +391,9 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
       }
       return;
     }
-    const float b = has_bias ? __bfloat162float(p.bias[n]) : 0.0f;
-    const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
-    __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y);
-#pragma unroll
-    for (int j = 0; j < CW; ++j) {
-      const int m = col0 + j;
-      if (m >= p.M) break;
-      const float r = has_res ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
-      const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
-      uint16_t o;
-      if (IN == IN_INT8)
-        o = epi_int8(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.act, p.flags);
-      else
-        o = __bfloat16_as_ushort(__float2bfloat16_rn(
-            epi_value(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r, p.act,
-                      p.flags)));
-      Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
-    }
+    SwapIn<CW> in;
+    load_swap_inputs<SC, CW>(p, n, col0, in);
+    store_swap<IN, SC, CW>(p, n, col0, vals, in);
   }
 }
 
@@ -360,8 +418,153 @@ __device__ __forceinline__ uint32_t* ws_slot(const KParams& p, int split, int ti
 
 // ---------------------------------------------------------------- kernel ---
 
+// INT8 prologue transform of one ring stage: the int8 staging tiles (TMA,
+// 128-byte swizzled rows of 128 codes) become fp16 tiles in the UMMA layout
+// (two 128-byte K atoms per tile).  Exact: every int8 value is an fp16 value.
+template <int BN, class C>
+__device__ __forceinline__ void convert_stage(uint8_t* base, int ct) {
+#pragma unroll 1
+  for (int q = ct; q < (128 + BN) * 8; q += 128) {
+    const bool isP = q < 128 * 8;
+    const int rr = isP ? (q >> 3) : ((q - 1024) >> 3);
+    const int j = q & 7;
+    const uint8_t* src = base + C::kPBytes + C::kQBytes + (isP ? 0u : C::kP8Bytes) + rr * 128 +
+                         ((j ^ (rr & 7)) << 4);
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t x = w4[t] ^ 0x80808080u;  // byte b -> b + 128 (unsigned)
+      uint32_t lo, hi;
+      asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+      asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+      // fp16 0x64XX = 1024 + XX; subtracting 1152 = 1024 + 128 gives b exactly
+      const __half2 c = __floats2half2_rn(1152.0f, 1152.0f);
+      __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), c);
+      __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), c);
+      h[2 * t] = *reinterpret_cast<uint32_t*>(&l2);
+      h[2 * t + 1] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    // 16 fp16 values = two 16-byte chunks: atom j/4, chunks 2*(j%4) and +1
+    uint8_t* atom = base + (isP ? 0u : C::kPBytes) +
+                    static_cast<uint32_t>(j >> 2) * (isP ? 128u : static_cast<uint32_t>(BN)) * 128u;
+    const int c0 = 2 * (j & 3);
+    *reinterpret_cast<uint4*>(atom + rr * 128 + ((c0 ^ (rr & 7)) << 4)) =
+        make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(atom + rr * 128 + (((c0 + 1) ^ (rr & 7)) << 4)) =
+        make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+// One work unit = one 128 x BN output tile and one K split.
+// A work unit: K tiles [kt0, kt0 + nk) of one 128 x BN output tile.  The
+// tile's K range is cut into `contrib` parts; this is part `j` (parts reduce
+// in the order j = 0..contrib-1).
+struct Unit {
+  int j, contrib, tile, tile_r, tile_c, row0, col0, kt0, nk;
+};
+
+__device__ __forceinline__ void unit_tile(const KParams& p, int tile, int bn, Unit& w) {
+  w.tile = tile;
+  w.tile_r = tile % p.tiles_rows;
+  w.tile_c = tile / p.tiles_rows;
+  w.row0 = w.tile_r * 128;
+  w.col0 = w.tile_c * bn;
+}
+
+// Work assignment of this CTA.  Split-K: units u = blockIdx.x, +gridDim.x,
+// ... each one (tile, split) with even K splits.  Balanced split-K (stream
+// K): the tiles x K-tiles iteration space is cut into gridDim.x equal
+// contiguous ranges; CTA c owns [floor(c I / G), floor((c+1) I / G)) and
+// walks it tile by tile, so a tile's K range is shared by the CTAs whose
+// ranges overlap it.
+struct WorkIter {
+  int64_t pos, end;
+};
+
+__device__ __forceinline__ WorkIter work_begin(const KParams& p) {
+  WorkIter it;
+  if (p.stream_k) {
+    const int64_t I = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols * p.k_tiles;
+    it.pos = I * blockIdx.x / gridDim.x;
+    it.end = I * (blockIdx.x + 1) / gridDim.x;
+  } else {
+    it.pos = blockIdx.x;
+    it.end = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols * p.split_k;
+  }
+  return it;
+}
+
+__device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it, Unit& w) {
+  if (it.pos >= it.end) return false;
+  if (!p.stream_k) {
+    const int u = static_cast<int>(it.pos);
+    it.pos += gridDim.x;
+    w.j = u % p.split_k;
+    w.contrib = p.split_k;
+    unit_tile(p, u / p.split_k, bn, w);
+    w.kt0 = static_cast<int>(static_cast<int64_t>(w.j) * p.k_tiles / p.split_k);
+    w.nk = static_cast<int>(static_cast<int64_t>(w.j + 1) * p.k_tiles / p.split_k) - w.kt0;
+    return true;
+  }
+  const int64_t KT = p.k_tiles;
+  const int64_t I = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols * KT;
+  const int64_t G = gridDim.x;
+  const int tile = static_cast<int>(it.pos / KT);
+  const int64_t tile_begin = tile * KT, tile_end = tile_begin + KT;
+  const int64_t seg_end = it.end < tile_end ? it.end : tile_end;
+  unit_tile(p, tile, bn, w);
+  w.kt0 = static_cast<int>(it.pos - tile_begin);
+  w.nk = static_cast<int>(seg_end - it.pos);
+  // owner of iteration i: the CTA c with floor(c I/G) <= i < floor((c+1) I/G)
+  const int first = static_cast<int>(((tile_begin + 1) * G - 1) / I);
+  const int last = static_cast<int>((tile_end * G - 1) / I);
+  w.contrib = last - first + 1;
+  w.j = static_cast<int>(blockIdx.x) - first;
+  it.pos = seg_end;
+  return true;
+}
+
+// Split-K arrival: after this CTA's partial is in the workspace, count it;
+// true for the last of the tile's splits to arrive (which then reduces).
+// The CTA barrier orders every epilogue thread's partial stores before one
+// thread's release-acquire increment at GPU scope; the last CTA's acquire,
+// followed by the barrier, orders its reads of the other partials after
+// them (the semaphore pattern of split-K GEMMs).
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ bool split_arrive_last(const KParams& p, int tile, int contrib, int ept,
+                                                  int* last_flag) {
+  epi_bar_sync();
+  if (ept == 0) {
+    const int prev = atom_add_acq_rel_gpu(p.counters + tile, 1);
+    const int last = (prev == contrib - 1);
+    if (last) p.counters[tile] = 0;  // ready for the next call (stream-ordered)
+    *last_flag = last;
+  }
+  epi_bar_sync();
+  const bool last = *last_flag != 0;
+  epi_bar_sync();  // the flag is rewritten by the next unit
+  return last;
+}
+
+// ---------------------------------------------------------------- kernel ---
+//
+// Persistent: CTA b handles work units b, b + gridDim.x, ...  Ring stages,
+// TMEM accumulator buffers and promotion buffers carry their phases across
+// units, so the epilogue of one unit overlaps the UMMA mainloop of the next.
+
 template <int IN, int SC, bool SWAP, int BN>
-__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
+                                  Cfg<IN, SC, SWAP, BN>::kMinBlocks)
     fused_linear_kernel(const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmQ, const KParams p) {
   using C = Cfg<IN, SC, SWAP, BN>;
@@ -377,28 +580,22 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads, 1)
   uint64_t* empty = bars + S;         // slot free (UMMA commit, or converter)
   uint64_t* bfull = bars + 2 * S;     // converted operands ready (INT8)
   uint64_t* bempty = bars + 3 * S;    // converted operands consumed (INT8)
-  uint64_t* tfull = bars + 4 * S;     // [2] TMEM buffer holds a finished block
+  uint64_t* tfull = bars + 4 * S;     // [2] TMEM buffer holds a finished K block / tile
   uint64_t* tempty = tfull + 2;       // [2] TMEM buffer drained by the epilogue
-  uint64_t* accum_full = tempty + 2;  // whole accumulator finished
-  uint64_t* mma_done = accum_full + 1;
+  uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  const int unit = blockIdx.x;
-  const int split = unit % p.split_k;
-  const int tile = unit / p.split_k;
-  const int tile_r = tile % p.tiles_rows;
-  const int tile_c = tile / p.tiles_rows;
-  const int row0 = tile_r * 128;
-  const int col0 = tile_c * BN;
-  const int kt0 = static_cast<int>(static_cast<int64_t>(split) * p.k_tiles / p.split_k);
-  const int kt1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.k_tiles / p.split_k);
-  const int nk = kt1 - kt0;
   const uint64_t lim = p.wait_limit_ns;
+  const bool has_work = p.k_tiles > 0;
 
+  if (threadIdx.x == 0) trace_point(p, TR_START);
+  if (warp == 0 && lane == 0 && has_work) {
+    tma_prefetch_desc(&tmP);
+    tma_prefetch_desc(&tmQ);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -410,7 +607,6 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads, 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 128);
     }
-    mbar_init(accum_full, 1);
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
@@ -422,218 +618,254 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (p.pdl && threadIdx.x == 0) griddep_launch_dependents();
+  if (threadIdx.x == 0) trace_point(p, TR_SETUP);
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    if (lane == 0 && !p.stall_producer && nk > 0) {
-      tma_prefetch_desc(&tmP);
-      tma_prefetch_desc(&tmQ);
+    if (lane == 0 && !p.stall_producer && has_work) {
       const uint64_t pol_first = policy_evict_first();
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % S;
-        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, lim)) {
-          record_status(p.status, ST_TIMEOUT_PRODUCER);
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+      // The weight operand (P with swap-AB, else Q) is constant across calls;
+      // the activation operand may be written by the previous kernel.
+      auto load_op = [&](bool weight, const Unit& w, int i, int s) {
         uint8_t* base = stage_base(s);
-        uint8_t* dP = C::kConvert ? base + C::kPBytes + C::kQBytes : base;
-        uint8_t* dQ = C::kConvert ? base + C::kPBytes + C::kQBytes + C::kP8Bytes : base + C::kPBytes;
-        const int kx = (kt0 + i) * C::kElemsPerStage;
-        if (p.evict_first_p)
-          tma_load_2d_hint(dP, &tmP, &full[s], kx, row0, pol_first);
+        const bool isP = (weight == SWAP);
+        uint8_t* dst = C::kConvert
+                           ? base + C::kPBytes + C::kQBytes + (isP ? 0u : C::kP8Bytes)
+                           : base + (isP ? 0u : C::kPBytes);
+        const int kx = (w.kt0 + i) * C::kElemsPerStage;
+        const CUtensorMap* map = isP ? &tmP : &tmQ;
+        const int y = isP ? w.row0 : w.col0;
+        if (isP ? p.evict_first_p : p.evict_first_q)
+          tma_load_2d_hint(dst, map, &full[s], kx, y, pol_first);
         else
-          tma_load_2d(dP, &tmP, &full[s], kx, row0);
-        if (p.evict_first_q)
-          tma_load_2d_hint(dQ, &tmQ, &full[s], kx, col0, pol_first);
-        else
-          tma_load_2d(dQ, &tmQ, &full[s], kx, col0);
+          tma_load_2d(dst, map, &full[s], kx, y);
+      };
+      uint32_t g = 0;  // ring iteration across units
+      bool first = true;
+      bool ok = true;
+      WorkIter it = work_begin(p);
+      Unit w;
+      while (ok && work_next(p, BN, it, w)) {
+        int i0 = 0;
+        if (first) {
+          first = false;
+          // As a programmatic dependent: stream the first ring of weight
+          // tiles, and send the rest of this unit's weight range to L2, while
+          // the previous kernel finishes; then wait for its results.
+          const int pre = p.pdl ? (w.nk < S ? w.nk : S) : 0;
+          for (int i = 0; i < pre; ++i) {
+            mbar_arrive_expect_tx(&full[i], C::kTxBytes);
+            load_op(true, w, i, i);
+          }
+          if (p.pdl && p.l2_prefetch) {
+            const CUtensorMap* wmap = SWAP ? &tmP : &tmQ;
+            const int wy = SWAP ? w.row0 : w.col0;
+            for (int i = pre; i < w.nk; ++i)
+              tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy);
+          }
+          griddep_wait();
+          for (int i = 0; i < pre; ++i) load_op(false, w, i, i);
+          trace_point(p, TR_FIRST_TMA);
+          i0 = pre;
+          g = pre;
+        }
+        for (int i = i0; i < w.nk; ++i, ++g) {
+          const int s = static_cast<int>(g % S);
+          const uint32_t ph = (g / S) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, lim)) {
+            record_status(p.status, ST_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+          load_op(true, w, i, s);
+          load_op(false, w, i, s);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------- UMMA issuer ----
-    if (lane == 0 && nk > 0) {
+    if (lane == 0 && has_work) {
+      uint32_t g = 0;     // ring iteration
+      uint32_t blk = 0;   // TMEM buffer use (per K block when promoting, else per unit)
       bool ok = true;
-      for (int i = 0; i < nk && ok; ++i) {
-        const int s = i % S;
-        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
-        const int b = i & 1;
-        if (C::kPromote && !mbar_wait(&tempty[b], ((static_cast<uint32_t>(i) >> 1) & 1u) ^ 1u, lim)) {
-          record_status(p.status, ST_TIMEOUT_MMA);
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(C::kConvert ? &bfull[s] : &full[s], ph, lim)) {
-          record_status(p.status, ST_TIMEOUT_MMA);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem_base + (C::kPromote ? static_cast<uint32_t>(b * BN) : 0u);
-        const uint32_t pa = smem_u32(stage_base(s));
-        const uint32_t qa = pa + C::kPBytes;
-#pragma unroll
-        for (int a = 0; a < C::kAtoms; ++a) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sdesc_k_sw128(pa + static_cast<uint32_t>(a) * 128u * 128u + 32u * k);
-            const uint64_t bd = sdesc_k_sw128(qa + static_cast<uint32_t>(a) * BN * 128u + 32u * k);
-            const uint32_t accum = C::kPromote ? ((a | k) != 0) : ((i | a | k) != 0);
-            if (IN == IN_E4M3)
-              umma_f8(d, ad, bd, C::kIdesc, accum);
-            else
-              umma_f16(d, ad, bd, C::kIdesc, accum);
+      WorkIter it = work_begin(p);
+      Unit w;
+      while (ok && work_next(p, BN, it, w)) {
+        if (!C::kPromote) {
+          // one TMEM buffer per unit; wait until the epilogue drained it
+          const int b = blk & 1;
+          if (!mbar_wait(&tempty[b], ((blk >> 1) & 1u) ^ 1u, lim)) {
+            record_status(p.status, ST_TIMEOUT_MMA);
+            ok = false;
+            break;
           }
         }
-        umma_commit(C::kConvert ? &bempty[s] : &empty[s]);
-        if (C::kPromote) umma_commit(&tfull[b]);
+        for (int i = 0; i < w.nk; ++i, ++g) {
+          const int s = static_cast<int>(g % S);
+          const uint32_t ph = (g / S) & 1u;
+          const int b = blk & 1;
+          if (C::kPromote && !mbar_wait(&tempty[b], ((blk >> 1) & 1u) ^ 1u, lim)) {
+            record_status(p.status, ST_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(C::kConvert ? &bfull[s] : &full[s], ph, lim)) {
+            record_status(p.status, ST_TIMEOUT_MMA);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
+          const uint32_t pa = smem_u32(stage_base(s));
+          const uint32_t qa = pa + C::kPBytes;
+#pragma unroll
+          for (int a = 0; a < C::kAtoms; ++a) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_k_sw128(pa + static_cast<uint32_t>(a) * 128u * 128u + 32u * k);
+              const uint64_t bd = sdesc_k_sw128(qa + static_cast<uint32_t>(a) * BN * 128u + 32u * k);
+              const uint32_t accum = C::kPromote ? ((a | k) != 0) : ((i | a | k) != 0);
+              if (IN == IN_E4M3)
+                umma_f8(d, ad, bd, C::kIdesc, accum);
+              else
+                umma_f16(d, ad, bd, C::kIdesc, accum);
+            }
+          }
+          umma_commit(C::kConvert ? &bempty[s] : &empty[s]);
+          if (C::kPromote) {
+            umma_commit(&tfull[b]);
+            ++blk;
+          }
+        }
+        if (!C::kPromote && ok) {
+          if (w.nk > 0) umma_commit(&tfull[blk & 1]);
+          ++blk;
+        }
       }
-      if (!C::kPromote && ok) umma_commit(accum_full);
+      trace_point(p, TR_LAST_COMMIT);
       umma_commit(mma_done);
     }
   } else if (warp >= 6) {
     // ---------------------------------- INT8 -> fp16 prologue transform ----
     if constexpr (C::kConvert) {
       const int ct = threadIdx.x - 192;  // 0..127
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % S;
-        const uint32_t ph = static_cast<uint32_t>(i / S) & 1u;
-        if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[s], ph ^ 1u, lim)) {
-          record_status(p.status, ST_TIMEOUT_CONVERT);
-          break;
-        }
-        uint8_t* base = stage_base(s);
-        // Q8 follows P8; both have 128-byte swizzled rows of 128 int8.
-        // Output atoms: P16 = base (2 atoms of 128 rows), Q16 = base + kPBytes.
-#pragma unroll 1
-        for (int q = ct; q < (128 + BN) * 8; q += 128) {
-          const bool isP = q < 128 * 8;
-          const int rr = isP ? (q >> 3) : ((q - 1024) >> 3);
-          const int j = q & 7;
-          const uint8_t* src = base + C::kPBytes + C::kQBytes + (isP ? 0u : C::kP8Bytes) +
-                               rr * 128 + ((j ^ (rr & 7)) << 4);
-          const uint4 v = *reinterpret_cast<const uint4*>(src);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-          uint32_t h[8];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t x = w4[t] ^ 0x80808080u;  // byte b -> b + 128 (unsigned)
-            uint32_t lo, hi;
-            asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
-            asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
-            // fp16 0x64XX = 1024 + XX; subtract 1152 = 1024 + 128 -> b (exact)
-            const __half2 c = __floats2half2_rn(1152.0f, 1152.0f);
-            __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), c);
-            __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), c);
-            h[2 * t] = *reinterpret_cast<uint32_t*>(&l2);
-            h[2 * t + 1] = *reinterpret_cast<uint32_t*>(&h2);
+      uint32_t g = 0;
+      bool ok = true;
+      WorkIter it = work_begin(p);
+      Unit w;
+      while (ok && work_next(p, BN, it, w)) {
+        for (int i = 0; i < w.nk; ++i, ++g) {
+          const int s = static_cast<int>(g % S);
+          const uint32_t ph = (g / S) & 1u;
+          if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[s], ph ^ 1u, lim)) {
+            record_status(p.status, ST_TIMEOUT_CONVERT);
+            ok = false;
+            break;
           }
-          // 16 fp16 = two 16-byte chunks, in atom j/4, chunks 2*(j%4), +1
-          uint8_t* atom = base + (isP ? 0u : C::kPBytes) +
-                          static_cast<uint32_t>(j >> 2) * (isP ? 128u : static_cast<uint32_t>(BN)) * 128u;
-          const int c0 = 2 * (j & 3);
-          *reinterpret_cast<uint4*>(atom + rr * 128 + (((c0) ^ (rr & 7)) << 4)) =
-              make_uint4(h[0], h[1], h[2], h[3]);
-          *reinterpret_cast<uint4*>(atom + rr * 128 + (((c0 + 1) ^ (rr & 7)) << 4)) =
-              make_uint4(h[4], h[5], h[6], h[7]);
+          convert_stage<BN, C>(stage_base(s), ct);
+          fence_proxy_async_smem();
+          mbar_arrive(&empty[s]);
+          mbar_arrive(&bfull[s]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&empty[s]);
-        mbar_arrive(&bfull[s]);
       }
     }
   } else {
     // ----------------------------------------------------- epilogue ----
     const int quarter = warp & 3;
     const int lane_row = quarter * 32 + lane;
-    const int row = row0 + lane_row;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const int ept = threadIdx.x - 64;  // 0..127
+    griddep_wait();
+    uint32_t blk = 0;
     bool ok = true;
-
-    if constexpr (C::kPromote) {
-      // ---- promotion: per 128-K block, TMEM buffer -> registers ----
-      uint32_t acc[BN];
+    WorkIter it = work_begin(p);
+    Unit w;
+    while (ok && work_next(p, BN, it, w)) {
+      const int row = w.row0 + lane_row;
+      if constexpr (C::kPromote) {
+        // ---- promotion: per 128-K block, TMEM buffer -> registers ----
+        uint32_t acc[BN];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) acc[c] = 0u;  // +0.0f or int 0
-      for (int i = 0; i < nk; ++i) {
-        const int b = i & 1;
-        const uint32_t bph = (static_cast<uint32_t>(i) >> 1) & 1u;
-        float srow = 1.0f;  // scale shared by the thread's row
-        if constexpr (SC == SC_BLOCK) {
-          const int kb = kt0 + i;
-          if (!SWAP) {
-            const float sw = __ldg(p.s_w + (col0 / 128) * p.kb_count + kb);
-            srow = (row < p.M) ? __ldg(p.s_a + static_cast<int64_t>(row) * p.kb_count + kb) * sw
-                               : 0.0f;
-          } else {
-            srow = __ldg(p.s_w + tile_r * p.kb_count + kb);
+        for (int c = 0; c < BN; ++c) acc[c] = 0u;  // +0.0f or int 0
+        auto row_scale = [&](int kb) -> float {
+          if constexpr (SC == SC_BLOCK) {
+            if (!SWAP) {
+              const float sw = __ldg(p.s_w + (w.col0 / 128) * p.kb_count + kb);
+              return (row < p.M) ? __ldg(p.s_a + static_cast<int64_t>(row) * p.kb_count + kb) * sw
+                                 : 0.0f;
+            }
+            return __ldg(p.s_w + w.tile_r * p.kb_count + kb);
           }
-        }
-        if (!mbar_wait(&tfull[b], bph, lim)) {
-          record_status(p.status, ST_TIMEOUT_EPILOGUE);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+          return 1.0f;
+        };
+        float srow_next = (w.nk > 0) ? row_scale(w.kt0) : 1.0f;
+        for (int i = 0; i < w.nk; ++i, ++blk) {
+          const int b = blk & 1;
+          const uint32_t bph = (blk >> 1) & 1u;
+          const float srow = srow_next;  // loaded one block ahead
+          if (i + 1 < w.nk) srow_next = row_scale(w.kt0 + i + 1);
+          if (!mbar_wait(&tfull[b], bph, lim)) {
+            record_status(p.status, ST_TIMEOUT_EPILOGUE);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
 #pragma unroll
-        for (int c = 0; c < BN; c += CW) {
-          uint32_t r[CW];
-          tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(b * BN + c), r);
-          tmem_ld_wait();
+          for (int c = 0; c < BN; c += CW) {
+            uint32_t r[CW];
+            tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(b * BN + c), r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < CW; ++j) {
-            if constexpr (SC == SC_BLOCK) {
-              float s = srow;
-              if (SWAP) {
-                const int m = col0 + c + j;
-                s = (m < p.M) ? srow * __ldg(p.s_a + static_cast<int64_t>(m) * p.kb_count + kt0 + i)
-                              : 0.0f;
+            for (int j = 0; j < CW; ++j) {
+              if constexpr (SC == SC_BLOCK) {
+                float s = srow;
+                if (SWAP) {
+                  const int m = w.col0 + c + j;
+                  s = (m < p.M)
+                          ? srow * __ldg(p.s_a + static_cast<int64_t>(m) * p.kb_count + w.kt0 + i)
+                          : 0.0f;
+                }
+                acc[c + j] = __float_as_uint(
+                    __fmaf_rn(s, __uint_as_float(r[j]), __uint_as_float(acc[c + j])));
+              } else {
+                acc[c + j] = static_cast<uint32_t>(static_cast<int32_t>(acc[c + j]) +
+                                                   __float2int_rn(__uint_as_float(r[j])));
               }
-              acc[c + j] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[j]),
-                                                      __uint_as_float(acc[c + j])));
-            } else {
-              acc[c + j] = static_cast<uint32_t>(static_cast<int32_t>(acc[c + j]) +
-                                                 __float2int_rn(__uint_as_float(r[j])));
             }
           }
+          tc_fence_before();
+          mbar_arrive(&tempty[b]);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[b]);
-      }
-      if (ok) {
+        if (!ok) break;
         bool do_epi = true;
-        if (p.split_k > 1) {
+        if (w.contrib > 1) {
 #pragma unroll
           for (int c = 0; c < BN; ++c)
-            if (row < p.rows && col0 + c < p.cols) __stcg(ws_slot<BN>(p, split, tile, c, lane_row), acc[c]);
-          __threadfence();
-          epi_bar_sync();
-          if (ept == 0) {
-            const int prev = atomicAdd(p.counters + tile, 1);
-            const int last = (prev == p.split_k - 1);
-            if (last) atomicExch(p.counters + tile, 0);
-            *last_flag = last;
-          }
-          epi_bar_sync();
-          do_epi = *last_flag != 0;
+            if (row < p.rows && w.col0 + c < p.cols)
+              __stcg(ws_slot<BN>(p, w.j, w.tile, c, lane_row), acc[c]);
+          do_epi = split_arrive_last(p, w.tile, w.contrib, ept, last_flag);
           if (do_epi) {
-            __threadfence();
+            // partials in split order 0..S-1 (this CTA's own one is read back
+            // from the workspace too); per split, independent loads
+            const bool rv = row < p.rows;
+            for (int s2 = 0; s2 < w.contrib; ++s2) {
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              uint32_t tot = 0u;
-              if (row < p.rows && col0 + c < p.cols) {
-                for (int s2 = 0; s2 < p.split_k; ++s2) {
-                  const uint32_t v = (s2 == split) ? acc[c] : __ldcg(ws_slot<BN>(p, s2, tile, c, lane_row));
-                  if (IN == IN_INT8)
-                    tot = static_cast<uint32_t>(static_cast<int32_t>(tot) + static_cast<int32_t>(v));
-                  else
-                    tot = __float_as_uint(s2 == 0 ? __uint_as_float(v)
-                                                  : __fadd_rn(__uint_as_float(tot), __uint_as_float(v)));
-                }
+              for (int c = 0; c < BN; ++c) {
+                const bool okc = rv && w.col0 + c < p.cols;
+                const uint32_t v = okc ? __ldcg(ws_slot<BN>(p, s2, w.tile, c, lane_row)) : 0u;
+                if (IN == IN_INT8)
+                  acc[c] = (s2 == 0) ? v
+                                     : static_cast<uint32_t>(static_cast<int32_t>(acc[c]) +
+                                                             static_cast<int32_t>(v));
+                else
+                  acc[c] = (s2 == 0) ? v
+                                     : __float_as_uint(__fadd_rn(__uint_as_float(acc[c]),
+                                                                 __uint_as_float(v)));
               }
-              acc[c] = tot;
             }
           }
         }
@@ -643,82 +875,100 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads, 1)
             uint32_t r[CW];
 #pragma unroll
             for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
-            epilogue_chunk<IN, SC, SWAP, CW>(p, row, col0 + c, r);
+            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + c, r);
           }
         }
-      }
-    } else {
-      // ---- accumulator stays in TMEM until the end ----
-      if (nk > 0) {
-        if (!mbar_wait(accum_full, 0, lim)) {
-          record_status(p.status, ST_TIMEOUT_EPILOGUE);
-          ok = false;
+      } else {
+        // ---- accumulator in TMEM buffer blk&1 until the unit is done ----
+        const int b = blk & 1;
+        const uint32_t tb = t_lane + static_cast<uint32_t>(b * BN);
+        // swap-AB with one chunk (decode): epilogue inputs load while the
+        // mainloop runs
+        constexpr bool kPre = SWAP && BN == CW;
+        SwapIn<CW> pre;
+        if constexpr (kPre) {
+          if (!(p.flags & F_DEBUG)) load_swap_inputs<SC, CW>(p, row, w.col0, pre);
         }
-        tc_fence_after();
-      }
-      if (ok) {
+        if (w.nk > 0) {
+          if (!mbar_wait(&tfull[b], (blk >> 1) & 1u, lim)) {
+            record_status(p.status, ST_TIMEOUT_EPILOGUE);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
+        }
         bool do_epi = true;
-        if (p.split_k > 1) {
+        if (w.contrib > 1) {
 #pragma unroll 1
           for (int c = 0; c < BN; c += CW) {
             uint32_t r[CW];
-            tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(c), r);
+            tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < CW; ++j)
-              if (row < p.rows && col0 + c + j < p.cols)
-                __stcg(ws_slot<BN>(p, split, tile, c + j, lane_row), r[j]);
+              if (row < p.rows && w.col0 + c + j < p.cols)
+                __stcg(ws_slot<BN>(p, w.j, w.tile, c + j, lane_row), r[j]);
           }
-          __threadfence();
-          epi_bar_sync();
-          if (ept == 0) {
-            const int prev = atomicAdd(p.counters + tile, 1);
-            const int last = (prev == p.split_k - 1);
-            if (last) atomicExch(p.counters + tile, 0);
-            *last_flag = last;
-          }
-          epi_bar_sync();
-          do_epi = *last_flag != 0;
-          if (do_epi) __threadfence();
+          do_epi = split_arrive_last(p, w.tile, w.contrib, ept, last_flag);
         }
         if (do_epi) {
 #pragma unroll 1
           for (int c = 0; c < BN; c += CW) {
             uint32_t r[CW];
-            if (nk > 0) {
-              tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(c), r);
+            if (w.nk > 0) {
+              tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
               tmem_ld_wait();
             } else {
 #pragma unroll
               for (int j = 0; j < CW; ++j) r[j] = 0u;
             }
-            if (p.split_k > 1) {
+            if (w.contrib > 1) {
+              // partials summed in split order 0..S-1 (deterministic); per
+              // split, the chunk's loads are independent and overlap
+              float tot[CW];
+              const bool rv = row < p.rows;
+              for (int s2 = 0; s2 < w.contrib; ++s2) {
+                float v[CW];
 #pragma unroll
-              for (int j = 0; j < CW; ++j) {
-                float tot = 0.0f;
-                if (row < p.rows && col0 + c + j < p.cols) {
-                  for (int s2 = 0; s2 < p.split_k; ++s2) {
-                    const float v = (s2 == split) ? __uint_as_float(r[j])
-                                                  : __uint_as_float(__ldcg(ws_slot<BN>(p, s2, tile, c + j, lane_row)));
-                    tot = (s2 == 0) ? v : __fadd_rn(tot, v);
-                  }
+                for (int j = 0; j < CW; ++j) {
+                  const bool okc = rv && w.col0 + c + j < p.cols;
+                  v[j] = (s2 == w.j)
+                             ? __uint_as_float(r[j])
+                             : (okc ? __uint_as_float(__ldcg(ws_slot<BN>(p, s2, w.tile, c + j, lane_row)))
+                                    : 0.0f);
                 }
-                r[j] = __float_as_uint(tot);
+#pragma unroll
+                for (int j = 0; j < CW; ++j) tot[j] = (s2 == 0) ? v[j] : __fadd_rn(tot[j], v[j]);
+              }
+#pragma unroll
+              for (int j = 0; j < CW; ++j) r[j] = __float_as_uint(tot[j]);
+            }
+            if constexpr (kPre) {
+              if (!(p.flags & F_DEBUG)) {
+                store_swap<IN, SC, CW>(p, row, w.col0, r, pre);
+                continue;
               }
             }
-            epilogue_chunk<IN, SC, SWAP, CW>(p, row, col0 + c, r);
+            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + c, r);
           }
         }
+        // TMEM buffer b may take the unit after next
+        tc_fence_before();
+        mbar_arrive(&tempty[b]);
+        ++blk;
       }
     }
+    if (ept == 0) trace_point(p, TR_EPI_DONE);
   }
 
   // ------------------------------------------------------------ teardown ---
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_point(p, TR_END);
   if (warp == 1) {
     tc_fence_after();
-    if (nk > 0) {
+    if (has_work) {
       // every UMMA this CTA issued has completed before TMEM is released
       bool done = true;
       if (lane == 0) done = mbar_wait(mma_done, 0, lim);

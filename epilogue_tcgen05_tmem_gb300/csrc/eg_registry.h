@@ -10,6 +10,7 @@ struct KernelEntry {
   uint32_t fixed_bytes = 0;      // alignment slack + barriers
   int threads = 0;
   int elems_per_stage = 0;       // K elements one stage covers
+  int tmem_cols = 0;             // TMEM columns one CTA allocates
 };
 
 // Each returns false when bn has no instantiation for that kind and swap.
@@ -36,5 +37,6 @@ EG_DECLARE_LOOKUP(lookup_int8_tc)
     out->fixed_bytes = 1024u + 512u;                                                   \
     out->threads = C_::kThreads;                                                       \
     out->elems_per_stage = C_::kElemsPerStage;                                         \
+    out->tmem_cols = static_cast<int>(C_::kTmemCols);                                  \
     return true;                                                                       \
   } while (0)

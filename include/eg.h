@@ -44,10 +44,12 @@
  *   receives the reduced accumulator before the epilogue: int32 for INT8
  *   (exact), float32 otherwise (block mode: already block-scaled).
  *
- * Alignment rules (TMA bulk-tensor loads and 16-byte vector access):
- *   A, W, Y, R, bias, s_a, s_w are 16-byte aligned; lda*elt, ldw*elt,
- *   ldr*2 and ldy*2 (ldy*4 in debug mode) are multiples of 16 bytes;
- *   K*elt is a multiple of 16 bytes.  Block scaling needs K % 128 == 0.
+ * Alignment rules (TMA bulk-tensor loads):
+ *   A, W, bias, s_a, s_w are 16-byte aligned; lda*elt and ldw*elt are
+ *   multiples of 16 bytes; K*elt is a multiple of 16 bytes.  Y and R need
+ *   element alignment and ldy, ldr >= N; when Y, R and their row strides
+ *   are 16-byte aligned the epilogue uses 16-byte vector accesses.  Block
+ *   scaling needs K % 128 == 0.
  *   INT8 needs K <= 133144 so that |acc| <= 127^2 K fits in int32.
  *
  * Ownership: the caller owns every tensor and keeps it alive until the work
@@ -113,7 +115,14 @@ enum {
   EG_EPI_RESIDUAL = 2,          /* v = act(v) + R */
   EG_EPI_RESIDUAL_PRE_ACT = 4,  /* v = act(v + R)  (excludes EG_EPI_RESIDUAL) */
   EG_OUT_DEBUG_ACCUM = 8,       /* write the raw reduced accumulator */
-  EG_RUN_GRAPH = 16             /* eg_plan_run replays a captured CUDA graph */
+  EG_RUN_GRAPH = 16,            /* eg_plan_run replays a captured CUDA graph */
+  EG_RUN_PDL = 32               /* launch as a programmatic dependent of the
+                                   previous kernel on the stream: the kernel
+                                   starts streaming W before that kernel has
+                                   finished, and waits for it before reading
+                                   A, s_a, R, bias or s_w and before writing.
+                                   Requires that the previous kernel does not
+                                   write W. */
 };
 
 typedef struct {
@@ -131,6 +140,11 @@ typedef struct {
   int32_t stages;   /* shared-memory ring depth, 2..8 */
   int32_t split_k;  /* 1..256, at most the number of K tiles */
   int32_t swap_ab;  /* 0: rows over M;  1: rows over N (Y^T = W A^T) */
+  int32_t stream_k; /* 0: K split evenly split_k ways per tile.  n > 0:
+                       balanced split-K: n CTAs per SM share the whole
+                       tiles x K-tiles iteration space in equal contiguous
+                       ranges (split_k must be 1); a tile's partial sums
+                       reduce through the same workspace, in CTA order */
 } eg_tuning;
 
 typedef struct {
@@ -192,6 +206,24 @@ EG_API int32_t eg_plan_last_launch_count(const eg_plan* plan);
  * the kernel records EG_ERR_DEVICE_TIMEOUT and returns. */
 EG_API eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns,
                                  int32_t stall_producer);
+
+/* Launch configuration the plan uses: the kernel is persistent, so `grid`
+ * CTAs (at most `units`, at most every resident slot of the device) loop
+ * over the `units` work units (one 128 x tile_n tile and one K split each). */
+typedef struct {
+  int32_t grid, block, smem_bytes, units, blocks_per_sm, regs_per_thread;
+} eg_launch_info;
+EG_API eg_status eg_plan_get_launch(const eg_plan* plan, eg_launch_info* out);
+
+/* Tracing: when `trace` is non-NULL, every later run of this plan records,
+ * per CTA, EG_TRACE_POINTS device %globaltimer values (nanoseconds) into
+ * trace[cta * EG_TRACE_POINTS + point] for ctas < trace_ctas: CTA start,
+ * setup done, first TMA issued, first UMMA operands ready, last UMMA
+ * committed, first accumulator ready in the epilogue, epilogue done, CTA
+ * end.  The buffer is caller-owned device memory of trace_ctas *
+ * EG_TRACE_POINTS * 8 bytes.  NULL turns tracing off. */
+#define EG_TRACE_POINTS 8
+EG_API eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace_ctas);
 
 EG_API const char* eg_status_string(eg_status s);
 EG_API const char* eg_last_error_detail(void);

@@ -229,7 +229,10 @@ def test_unfused_path(pre):
     plan.run_unfused(d["A"], d["W"], d["Y"], T1, T2, d["s_a"], d["s_w"], d["bias"], d["residual"])
     torch.cuda.synchronize()
     assert plan.last_launch_count() == 3
-    assert_close_rms(bits(d["Y"].cpu()), oracle.linear(p))
+    # the unfused path rounds two intermediates to bf16: allow those steps
+    y = bits(d["Y"].cpu())
+    ref = oracle.linear(p)
+    assert_close_rms(y, ref, rel=3e-2, max_ulp_frac=1e-2)
     plan.run(d["A"], d["W"], d["Y"], d["s_a"], d["s_w"], d["bias"], d["residual"])
     assert plan.last_launch_count() == 1
     plan.close()
@@ -267,3 +270,83 @@ def test_run_argument_errors():
     with pytest.raises(eg.EgError):
         make_plan(p, dict(tile_n=64, stages=4, split_k=3, swap_ab=0))   # 2 K tiles only
     plan.close()
+
+
+def test_programmatic_dependent_launch_chain():
+    """Calls launched as programmatic dependents (weights streamed before the
+    previous kernel finishes) give the same bits as plain launches, also when
+    the previous kernel writes this call's activations."""
+    p = inputs.make_problem(8, 1024, 2048, "e4m3", "token_channel", act="silu", bias=True, seed=6)
+    plain = make_plan(p)
+    plan_pdl = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=True, pdl=True)
+    d = to_device(p)
+    y_ref, _ = run(p, plan=plain, d=d)
+    A0 = d["A"].clone()
+    for i in range(6):
+        # the previous kernel on the stream rewrites A (same values)
+        d["A"].copy_(A0)
+        plan_pdl.run(d["A"], d["W"], d["Y"], d["s_a"], d["s_w"], d["bias"])
+    torch.cuda.synchronize()
+    assert plan_pdl.device_status() == eg.EG_OK
+    assert torch.equal(d["Y"].cpu().view(torch.int16), y_ref.view(torch.int16))
+    plain.close()
+    plan_pdl.close()
+
+
+def test_unaligned_output_rows_use_scalar_path():
+    p = inputs.make_problem(5, 130, 256, "bf16", act="relu", bias=True, residual=True, seed=3)
+    check_full(p, dict(tile_n=64, stages=3, split_k=1, swap_ab=0))
+    check_full(p, dict(tile_n=16, stages=3, split_k=2, swap_ab=1))
+
+
+def test_trace_timeline_and_launch_info():
+    from epilogue_tcgen05_tmem_gb300 import trace as tr
+    p = inputs.make_problem(4, 2048, 1024, "e4m3", "token_channel", act="silu", bias=True, seed=2)
+    plan = make_plan(p)
+    li = plan.launch_info
+    assert 0 < li["grid"] <= li["units"] and li["block"] in (192, 320)
+    buf = torch.zeros(li["grid"], eg.EG_TRACE_POINTS, dtype=torch.int64, device="cuda")
+    plan.set_trace(buf)
+    y, _ = run(p, plan=plan)
+    t = buf.cpu().numpy()
+    assert (t[:, 0] > 0).all() and (t[:, 7] > 0).all()
+    assert tr.ordered(t)
+    s = tr.summarize(t)
+    assert s["end"]["p100"] >= s["start"]["p0"]
+    plan.set_trace(None)
+    assert_close_rms(bits(y), oracle.linear(p))
+    plan.close()
+
+
+@pytest.mark.parametrize("dtype,scale,M,N,K,tn,swap", [
+    ("bf16", "none", 40, 512, 1024, 64, 0),
+    ("bf16", "none", 7, 1000, 640, 16, 1),
+    ("e4m3", "token_channel", 3, 1536, 2048, 16, 1),
+    ("e4m3", "token_channel", 32, 2048, 4096, 32, 1),
+    ("e4m3", "block", 8, 1024, 1024, 16, 1),
+    ("e4m3", "block", 300, 384, 640, 128, 0),
+])
+@pytest.mark.parametrize("sk", [1, 2])
+def test_balanced_split_k(dtype, scale, M, N, K, tn, swap, sk):
+    """Balanced split-K (stream-K): CTAs share the tiles x K-tiles space in
+    equal ranges; tiles split across CTAs reduce through the workspace."""
+    p = inputs.make_problem(M, N, K, dtype, scale, act="silu", bias=True, residual=True, seed=12)
+    t = dict(tile_n=tn, stages=4, split_k=1, swap_ab=swap, stream_k=sk)
+    plan = make_plan(p, t)
+    d = to_device(p)
+    y1, _ = run(p, plan=plan, d=d)
+    y2, _ = run(p, plan=plan, d=d)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), "not deterministic"
+    assert_close_rms(bits(y1), oracle.linear(p))
+    plan.close()
+
+
+@pytest.mark.parametrize("sk", [1, 2])
+def test_balanced_split_k_int8_exact(sk):
+    p = inputs.make_problem(16, 1024, 4096, "int8", "token_channel", residual=True, seed=14)
+    t = dict(tile_n=16, stages=3, split_k=1, swap_ab=1, stream_k=sk)
+    yacc, _ = run(p, t, debug=True)
+    _, _, acc64 = oracle.linear(p, want_acc=True)
+    assert np.array_equal(yacc.numpy().astype(np.int64), acc64)
+    y, _ = run(p, t)
+    assert ulp_dist(bits(y), oracle.linear(p)).max() <= 1
