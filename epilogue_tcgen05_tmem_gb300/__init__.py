@@ -32,7 +32,8 @@ EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RU
 EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "eg_plan_run",
             "eg_plan_run_unfused", "eg_plan_device_status", "eg_plan_destroy",
             "eg_plan_last_launch_count", "eg_plan_set_test_stall", "eg_plan_get_launch",
-            "eg_plan_set_trace", "eg_status_string", "eg_last_error_detail")
+            "eg_plan_set_trace", "eg_status_string", "eg_last_error_detail",
+            "eg_linear_noalloc")
 EG_TRACE_POINTS = 8
 TRACE_POINT_NAMES = ("start", "setup", "first_tma", "first_operands", "last_commit",
                      "first_acc", "epilogue_done", "end")
@@ -104,6 +105,9 @@ def lib() -> ctypes.CDLL:
             L.eg_plan_set_test_stall.argtypes = [vp, ctypes.c_uint64, ctypes.c_int32]
             L.eg_plan_get_launch.argtypes = [vp, ctypes.POINTER(eg_launch_info)]
             L.eg_plan_set_trace.argtypes = [vp, vp, ctypes.c_int32]
+            L.eg_linear_noalloc.argtypes = [ctypes.POINTER(eg_problem), ctypes.POINTER(eg_tuning),
+                                            ctypes.POINTER(eg_args), vp]
+            L.eg_linear_noalloc.restype = ctypes.c_int
             for f in ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning",
                       "eg_plan_run", "eg_plan_run_unfused", "eg_plan_device_status",
                       "eg_plan_destroy", "eg_plan_set_test_stall", "eg_plan_get_launch",
@@ -155,6 +159,15 @@ def eg_plan_run(plan, args: eg_args, stream: int | None) -> int:
 
 def eg_plan_run_unfused(plan, args: eg_args, t1: int, t2: int, stream: int | None) -> int:
     return lib().eg_plan_run_unfused(plan, ctypes.byref(args), t1, t2, stream)
+
+
+def eg_linear_noalloc(problem: eg_problem, tuning: eg_tuning | None, args: eg_args,
+                      stream: int | None) -> int:
+    """One call that allocates no device memory (see include/eg.h): for
+    callers that cannot allocate while they run the layer."""
+    return lib().eg_linear_noalloc(ctypes.byref(problem),
+                                   ctypes.byref(tuning) if tuning is not None else None,
+                                   ctypes.byref(args), stream)
 
 
 def eg_plan_destroy(plan) -> int:

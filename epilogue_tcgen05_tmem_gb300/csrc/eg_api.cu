@@ -745,3 +745,152 @@ eg_status eg_plan_destroy(eg_plan* plan) {
 }
 
 }  // extern "C"
+
+// --------------------------------------------- no-allocation entry point ---
+//
+// Some callers cannot allocate device memory on the path where they run the
+// layer: code running inside a memory pool or arena that owns every byte of
+// the device, allocators that must not be re-entered from within a call, or
+// runtimes that forbid cudaMalloc after start-up.  eg_linear_noalloc serves
+// them: it runs the same fused kernel, but the kernel's scratch (split-K
+// partial sums, per-tile arrival counters and the device status word) lives
+// in the fixed array below, which the library's module holds on every device
+// that loads it, until the process exits.
+
+namespace {
+
+constexpr size_t kScratchCounterBytes = 64u * 1024u;          // arrival counters + status
+constexpr size_t kScratchWorkspaceBytes = 4u * 1024u * 1024u;  // split-K partial sums
+constexpr size_t kScratchCounters = kScratchCounterBytes / sizeof(int) - 1;  // last int: status
+
+// Host code may not dereference this name: on the host it is only a stand-in
+// for the device array.  The device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchCounterBytes +
+                                                                 kScratchWorkspaceBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Once per device, with that device current: the scratch array's address.
+eg_status noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(EG_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the scratch array");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return EG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
+                            const eg_args* args, void* stream) {
+  eg_status s = validate_problem(problem);
+  if (s != EG_OK) return s;
+  const eg_problem& p = *problem;
+  if (p.flags & EG_RUN_GRAPH)
+    return fail(EG_ERR_INVALID_ARG, "eg_linear_noalloc keeps no captured graphs (drop EG_RUN_GRAPH)");
+  int dev = -1;
+  EG_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  int major = 0, minor = 0;
+  EG_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "device query");
+  EG_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "device query");
+  if (major != 10 || minor != 3)
+    return fail(EG_ERR_UNSUPPORTED, "the kernels are built for sm_103a; device %d is sm_%d%d", dev,
+                major, minor);
+  eg_tuning t{};
+  if (tuning) {
+    t = *tuning;
+  } else if (!eg::tuning_lookup(p, sm_count_of(dev), &t)) {
+    return fail(EG_ERR_NOT_TUNED, "no tuning entry or default for this problem");
+  }
+  // A plan on the stack: it only carries the launch description to the
+  // shared helpers; nothing in it allocates.
+  eg_plan pl;
+  uint32_t smem = 0;
+  int k_tiles = 0;
+  if ((s = validate_tuning(p, t, &pl.ke, &smem, &k_tiles)) != EG_OK) return s;
+  pl.prob = p;
+  pl.tune = t;
+  pl.device = -1;  // not a created plan
+  pl.smem = smem;
+  pl.k_tiles = k_tiles;
+  pl.kb_count = static_cast<int>(p.K / 128);
+  const bool swap = t.swap_ab != 0;
+  pl.rows = static_cast<int>(swap ? p.N : p.M);
+  pl.cols = static_cast<int>(swap ? p.M : p.N);
+  pl.tiles_rows = (pl.rows + 127) / 128;
+  pl.tiles_cols = (pl.cols + t.tile_n - 1) / t.tile_n;
+  pl.wait_limit_ns = default_wait_limit_ns();
+  if ((s = validate_args(&pl, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0)) != EG_OK) return s;
+  if (p.M == 0 || p.N == 0) return EG_OK;
+
+  // work decomposition and scratch needs
+  const size_t tiles = size_t(pl.tiles_rows) * pl.tiles_cols;
+  cudaFuncAttributes fa{};
+  EG_CUDA(cudaFuncGetAttributes(&fa, pl.ke.fn), "cudaFuncGetAttributes");
+  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0, sm_blocks = 0;
+  EG_CUDA(cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev), "device limits");
+  const int warps = (pl.ke.threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  int per_sm = sm_smem / static_cast<int>(smem + reserved);
+  per_sm = std::min(per_sm, sm_regs / std::max(1, regs_warp * warps));
+  per_sm = std::min(per_sm, sm_threads / pl.ke.threads);
+  per_sm = std::min(per_sm, sm_blocks);
+  per_sm = std::min(per_sm, 512 / pl.ke.tmem_cols);
+  if (per_sm < 1) return fail(EG_ERR_UNSUPPORTED, "the kernel does not fit on an SM");
+  pl.max_contrib = t.split_k;
+  if (t.stream_k > 0) {
+    const long long iters = static_cast<long long>(tiles) * k_tiles;
+    long long G = static_cast<long long>(sm_count_of(dev)) * std::min(per_sm, t.stream_k);
+    if (G > iters) G = iters;
+    pl.grid = static_cast<int>(G);
+    int mc = 1;
+    for (size_t tile = 0; tile < tiles && G > 0; ++tile) {
+      const long long b = static_cast<long long>(tile) * k_tiles, e2 = b + k_tiles;
+      mc = std::max(mc, static_cast<int>((e2 * G - 1) / iters - ((b + 1) * G - 1) / iters + 1));
+    }
+    pl.max_contrib = mc;
+  } else {
+    const long long units = static_cast<long long>(tiles) * t.split_k;
+    const long long slots = static_cast<long long>(sm_count_of(dev)) * per_sm;
+    pl.grid = static_cast<int>(units < slots ? units : slots);
+  }
+  const size_t ws_need = pl.max_contrib > 1 ? size_t(pl.max_contrib) * tiles * size_t(t.tile_n) * 128 * 4 : 0;
+  if (tiles > kScratchCounters || ws_need > kScratchWorkspaceBytes)
+    return fail(EG_ERR_UNSUPPORTED,
+                "problem needs %zu tile counters and %zu bytes of split-K scratch; "
+                "eg_linear_noalloc holds %zu counters and %zu bytes",
+                tiles, ws_need, kScratchCounters, kScratchWorkspaceBytes);
+
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(dev, &scratch)) != EG_OK) return s;
+  int* counters = static_cast<int*>(scratch);
+  pl.counters = counters;
+  pl.status = counters + kScratchCounters;
+  pl.ws = static_cast<unsigned char*>(scratch) + kScratchCounterBytes;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  EG_CUDA(cudaFuncSetAttribute(pl.ke.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)),
+          "cudaFuncSetAttribute");
+  // the arrival counters and the status word start every call at zero (the
+  // array keeps whatever the previous call left)
+  EG_CUDA(cudaMemsetAsync(counters, 0, (tiles + 1) * sizeof(int), st), "clearing tile counters");
+  EG_CUDA(cudaMemsetAsync(pl.status, 0, sizeof(int), st), "clearing the status word");
+  if ((s = ensure_maps(&pl, args)) != EG_OK) return s;
+  const eg::KParams kp = make_params(&pl, args, p.act, epi_flags(p.flags), args->Y, args->ldy);
+  return launch_fused(&pl, kp, st);
+}
+
+}  // extern "C"

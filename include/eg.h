@@ -225,6 +225,33 @@ EG_API eg_status eg_plan_get_launch(const eg_plan* plan, eg_launch_info* out);
 #define EG_TRACE_POINTS 8
 EG_API eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace_ctas);
 
+/* One fused linear-layer call that allocates no device memory.  (The pages
+ * this library follows have no counterpart to this call.)
+ *
+ * For callers that cannot allocate on the path where they run the layer:
+ * code living inside a memory pool or arena that owns all of the device's
+ * memory, allocators that must not be re-entered from inside a call, or
+ * runtimes that forbid cudaMalloc once they are running.  eg_plan_create
+ * allocates the split-K workspace, tile counters and a status word; this
+ * call instead runs the same kernel with that scratch in one fixed array
+ * compiled into the library (4 MiB of split-K partial sums plus 16383 tile
+ * counters and the status word), which every device that loads the library
+ * holds until the process exits.  The caller still passes inputs and
+ * outputs; `problem`, `tuning` (NULL: the built-in table, then the default
+ * rule), `args` and `stream` mean what they mean for eg_plan_create and
+ * eg_plan_run.  EG_RUN_GRAPH is rejected.
+ *
+ * The first call on each device looks up the array's device address; make
+ * that first call before any stream capture.  Every call clears the tile
+ * counters and the status word on `stream` before its kernel; the split-K
+ * partial sums are written before they are read.  All calls share the one
+ * array: calls that overlap on the GPU (other streams, other threads) race
+ * and must not be issued.  A problem whose split-K scratch or tile count
+ * exceeds the array returns EG_ERR_UNSUPPORTED with the sizes in
+ * eg_last_error_detail().  Device-side wait timeouts are not reported. */
+EG_API eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
+                                   const eg_args* args, void* stream);
+
 EG_API const char* eg_status_string(eg_status s);
 EG_API const char* eg_last_error_detail(void);
 
