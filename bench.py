@@ -64,6 +64,21 @@ def dist_env():
     return rank, world, local
 
 
+def rank_aggregate(local_ms: float, local_units: float, dist=None):
+    """(max of the timed region over ranks, sum of the work all ranks did).
+    Replicas: every rank runs the whole workload on its own GPU; the job's
+    throughput is the total work over the slowest rank's time."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(local_ms), float(local_units)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=dev)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -222,13 +237,9 @@ def run_native(args):
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, total_bytes = rank_aggregate(e0.elapsed_time(e1), bytes_per_step * args.steps, pg)
     ms_per_step = ms / args.steps
-    value = world * bytes_per_step * args.steps / (ms * 1e-3) / 1e9
+    value = total_bytes / (ms * 1e-3) / 1e9
     avg_launch_us = ms * 1e3 / (args.steps * calls_per_step)
     achieved = (bytes_per_step / calls_per_step) / (avg_launch_us * 1e-6) / 1e9
 
