@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--m", default=None, help="token counts for --config runs, e.g. 1,16")
+    ap.add_argument("--tuning", default=None,
+                    help="tuning override for --config runs, JSON, e.g. "
+                         '\'{"tile_n":256,"stages":4,"split_k":1,"swap_ab":0,"stream_k":1}\'')
     return ap.parse_args()
 
 
@@ -441,7 +444,8 @@ def run_config(args):
         d = device_problem(p, torch)
         plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
                        residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
-                       pdl=not unfused)
+                       pdl=not unfused,
+                       tuning=json.loads(args.tuning) if args.tuning else None)
         nb = traffic.problem_bytes(p)
         fl = traffic.flops(p.M, p.N, p.K)
         # rotate weight copies so repeated calls do not hit L2

@@ -180,7 +180,8 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
                 t.tile_n, t.swap_ab);
   if (t.stages < 2 || t.stages > 8)
     return fail(EG_ERR_UNSUPPORTED, "stages must be in 2..8 (got %d)", t.stages);
-  const uint64_t s = ke->fixed_bytes + uint64_t(t.stages) * ke->stage_bytes;
+  const uint64_t s = ke->fixed_bytes + uint64_t(t.stages) * ke->stage_bytes +
+                     eg::block_scale_smem_bytes(p, t.swap_ab, t.tile_n, ke->elems_per_stage);
   if (s > kMaxSmem)
     return fail(EG_ERR_UNSUPPORTED, "%d stages need %llu bytes of shared memory (max %u)", t.stages,
                 (unsigned long long)s, kMaxSmem);
@@ -537,8 +538,11 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
     return cleanup(cuda_fail(e, "device limits"));
   const int warps = (ke.threads + 31) / 32;
   const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  // registers: 4 sub-partitions of sm_regs/4 each; the warps of all
+  // resident CTAs spread over them
+  const int warps_per_smsp = (sm_regs / 4) / std::max(1, regs_warp);
   int per_sm = sm_smem / static_cast<int>(smem + reserved);
-  per_sm = std::min(per_sm, sm_regs / std::max(1, regs_warp * warps));
+  per_sm = std::min(per_sm, (4 * warps_per_smsp) / warps);
   per_sm = std::min(per_sm, sm_threads / ke.threads);
   per_sm = std::min(per_sm, sm_blocks);
   per_sm = std::min(per_sm, 512 / ke.tmem_cols);
@@ -571,6 +575,10 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
     pl->ws_bytes = size_t(pl->max_contrib) * tiles * size_t(t.tile_n) * 128 * 4;
     if ((e = cudaMalloc(&pl->ws, pl->ws_bytes)) != cudaSuccess)
       return cleanup(cuda_fail(e, "allocating the split-K workspace"));
+    // INT8 accumulates its splits into slot 0 of each tile, which the kernel
+    // keeps at zero between calls; it starts at zero here
+    if ((e = cudaMemset(pl->ws, 0, pl->ws_bytes)) != cudaSuccess)
+      return cleanup(cuda_fail(e, "zeroing the split-K workspace"));
   }
   if ((e = cudaMalloc(reinterpret_cast<void**>(&pl->counters), (tiles + 1) * sizeof(int))) !=
           cudaSuccess ||
@@ -844,8 +852,9 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   EG_CUDA(cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev), "device limits");
   const int warps = (pl.ke.threads + 31) / 32;
   const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  const int warps_per_smsp = (sm_regs / 4) / std::max(1, regs_warp);
   int per_sm = sm_smem / static_cast<int>(smem + reserved);
-  per_sm = std::min(per_sm, sm_regs / std::max(1, regs_warp * warps));
+  per_sm = std::min(per_sm, (4 * warps_per_smsp) / warps);
   per_sm = std::min(per_sm, sm_threads / pl.ke.threads);
   per_sm = std::min(per_sm, sm_blocks);
   per_sm = std::min(per_sm, 512 / pl.ke.tmem_cols);
@@ -888,6 +897,10 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   // array keeps whatever the previous call left)
   EG_CUDA(cudaMemsetAsync(counters, 0, (tiles + 1) * sizeof(int), st), "clearing tile counters");
   EG_CUDA(cudaMemsetAsync(pl.status, 0, sizeof(int), st), "clearing the status word");
+  // INT8 split-K adds every split into one zeroed slot per tile
+  if (p.dtype == EG_IN_INT8 && pl.max_contrib > 1)
+    EG_CUDA(cudaMemsetAsync(pl.ws, 0, tiles * size_t(t.tile_n) * 128 * 4, st),
+            "clearing the INT8 split-K sums");
   if ((s = ensure_maps(&pl, args)) != EG_OK) return s;
   const eg::KParams kp = make_params(&pl, args, p.act, epi_flags(p.flags), args->Y, args->ldy);
   return launch_fused(&pl, kp, st);

@@ -102,9 +102,20 @@ struct Cfg {
   static constexpr uint32_t kQBytes = uint32_t(BN) * 128u * kAtoms;
   static constexpr uint32_t kP8Bytes = kConvert ? 128u * 128u : 0u;  // int8 staging
   static constexpr uint32_t kQ8Bytes = kConvert ? uint32_t(BN) * 128u : 0u;
-  static constexpr uint32_t kStageBytes = kPBytes + kQBytes + kP8Bytes + kQ8Bytes;
+  // TMA ring stage: the UMMA operands, or (INT8) the int8 staging tiles; the
+  // converted fp16 operands then live in their own 2-slot ring, so the int8
+  // ring can be deep (bytes in flight) while the fp16 ring stays small.
+  static constexpr uint32_t kStageBytes = kConvert ? kP8Bytes + kQ8Bytes : kPBytes + kQBytes;
+  static constexpr int kOpSlots = 2;
+  static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * (kPBytes + kQBytes) : 0u;
   static constexpr uint32_t kTxBytes = (128u + BN) * 128u;  // bytes one stage's TMA delivers
-  static constexpr int kThreads = kConvert ? 320 : 192;
+  // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for block-scale
+  // promotion of wide tiles (two column halves per quarter, so each thread
+  // keeps BN/2 running sums and the promotion keeps up with UMMA).
+  static constexpr int kEpiWarps = (kPromote && !kConvert && BN >= 64) ? 8 : 4;
+  static constexpr int kEpiThreads = kEpiWarps * 32;
+  static constexpr int kColsPerThread = BN / (kEpiWarps / 4);
+  static constexpr int kThreads = 64 + kEpiThreads + (kConvert ? 128 : 0);
   // Small tiles (decode) are meant to run two CTAs per SM; cap registers so
   // two fit.  Promotion with wide tiles keeps BN accumulators per thread.
   // Decode tiles (BN 16) keep a third slot per SM free so that the next
@@ -112,10 +123,20 @@ struct Cfg {
   // still runs.
   static constexpr int kMinBlocks =
       kConvert ? (BN <= 16 ? 2 : 1)
-               : ((kPromote && BN >= 64) || BN >= 128) ? 1 : (BN <= 16 ? 3 : 2);
+               : ((kPromote && BN >= 64) || BN >= 128) ? 1 : (BN <= 32 ? 3 : 2);
+  // Register cap per thread for that residency.  The SM's 64K registers are
+  // split over its 4 sub-partitions (16K each) and warps are spread over
+  // them, so the busiest sub-partition holds ceil(warps / 4) warps of
+  // 32 threads: at most 512 / ceil(warps / 4) registers per thread
+  // (allocated in units of 8).
+  static constexpr int kWarpsPerSmsp = (kMinBlocks * (kThreads / 32) + 3) / 4;
+  static constexpr int kMaxRegs =
+      (512 / kWarpsPerSmsp) / 8 * 8 > 255 ? 255 : (512 / kWarpsPerSmsp) / 8 * 8;
   static constexpr int kCW = BN < 32 ? BN : 32;            // TMEM load chunk (columns)
-  // two accumulator buffers (per unit, or per K block when promoting)
-  static constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN;
+  // TMEM accumulator buffers: 2 (one unit drains while the next fills), or
+  // 4 when promoting K blocks so UMMA runs further ahead of the epilogue
+  static constexpr int kAccBufs = (kPromote && 4 * BN <= 512) ? 4 : 2;
+  static constexpr uint32_t kTmemCols = kAccBufs * BN <= 32 ? 32 : kAccBufs * BN;
   static constexpr uint32_t kIdesc =
       (IN == IN_BF16) ? idesc_f32acc(1, 1, 128, BN)
                       : idesc_f32acc(0, 0, 128, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
@@ -126,7 +147,7 @@ struct Cfg {
 template <int IN, int SC, bool SWAP, int BN>
 constexpr uint32_t smem_bytes_for(int stages) {
   using C = Cfg<IN, SC, SWAP, BN>;
-  return 1024u + uint32_t(stages) * C::kStageBytes + 512u;
+  return 1024u + uint32_t(stages) * C::kStageBytes + C::kOpBytes + 512u;
 }
 
 // ------------------------------------------------------------- helpers ----
@@ -135,8 +156,9 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ void epi_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Named barrier 1 among the epilogue warps only.
+__device__ __forceinline__ void epi_bar_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ float tanh_fast(float x) {
@@ -254,44 +276,53 @@ __device__ __forceinline__ uint16_t epi_int8(int32_t acc, float sa, float sw, fl
 template <int CW>
 struct SwapIn {
   float b, sw;
-  float sa[CW], r[CW];
 };
 
 template <int SC, int CW>
 __device__ __forceinline__ void load_swap_inputs(const KParams& p, int n, int col0, SwapIn<CW>& in) {
   const bool nv = n < p.N;
   const bool has_bias = (p.flags & F_BIAS) != 0;
-  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
   in.b = (has_bias && nv) ? __bfloat162float(p.bias[n]) : 0.0f;
   in.sw = (SC == SC_TC && nv) ? __ldg(p.s_w + n) : 1.0f;
-#pragma unroll
-  for (int j = 0; j < CW; ++j) {
-    const int m = col0 + j;
-    const bool ok = nv && m < p.M;
-    in.sa[j] = (SC == SC_TC && ok) ? __ldg(p.s_a + m) : 1.0f;
-    in.r[j] = (has_res && ok) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+  if constexpr (SC == SC_TC) {
+    // the token scales are the same for every lane: touch them now so the
+    // epilogue finds them in L1
+    if (nv && (threadIdx.x & 31) == 0 && col0 < p.M) (void)__ldg(p.s_a + col0);
   }
 }
 
 // Swap-AB epilogue compute and store: lanes of a warp hold consecutive n, so
-// each token's stores of Y are coalesced across the warp.
+// each token's residual loads and Y stores are coalesced across the warp.
 template <int IN, int SC, int CW>
 __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
                                            const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
   if (n >= p.N) return;
+  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
   __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y);
+  // groups of 8 tokens: the group's loads first, then its arithmetic
+  constexpr int G = CW < 8 ? CW : 8;
 #pragma unroll
-  for (int j = 0; j < CW; ++j) {
-    const int m = col0 + j;
-    if (m < p.M) {
-      uint16_t o;
-      if (IN == IN_INT8)
-        o = epi_int8(static_cast<int32_t>(vals[j]), in.sa[j], in.sw, in.b, in.r[j], p.act, p.flags);
-      else
-        o = __bfloat16_as_ushort(__float2bfloat16_rn(
-            epi_value(__uint_as_float(vals[j]), (SC == SC_TC) ? in.sa[j] * in.sw : 1.0f, in.b,
-                      in.r[j], p.act, p.flags)));
-      Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
+  for (int g = 0; g < CW; g += G) {
+    float r[G], sa[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int m = col0 + g + j;
+      r[j] = (has_res && m < p.M) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+      sa[j] = (SC == SC_TC && m < p.M) ? __ldg(p.s_a + m) : 1.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int m = col0 + g + j;
+      if (m < p.M) {
+        uint16_t o;
+        if (IN == IN_INT8)
+          o = epi_int8(static_cast<int32_t>(vals[g + j]), sa[j], in.sw, in.b, r[j], p.act, p.flags);
+        else
+          o = __bfloat16_as_ushort(__float2bfloat16_rn(
+              epi_value(__uint_as_float(vals[g + j]), (SC == SC_TC) ? sa[j] * in.sw : 1.0f, in.b,
+                        r[j], p.act, p.flags)));
+        Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
+      }
     }
   }
 }
@@ -398,6 +429,15 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
 }
 
 template <int CW>
+__device__ __forceinline__ void tmem_load_chunk_p(uint32_t taddr, uint32_t* r) {
+  if constexpr (CW == 32) {
+    tmem_ld32p(taddr, r);
+  } else {
+    tmem_ld16(taddr, r);
+  }
+}
+
+template <int CW>
 __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[CW]) {
   if constexpr (CW == 32) {
     tmem_ld32(taddr, r);
@@ -421,17 +461,30 @@ __device__ __forceinline__ uint32_t* ws_slot(const KParams& p, int split, int ti
 // INT8 prologue transform of one ring stage: the int8 staging tiles (TMA,
 // 128-byte swizzled rows of 128 codes) become fp16 tiles in the UMMA layout
 // (two 128-byte K atoms per tile).  Exact: every int8 value is an fp16 value.
-template <int BN, class C>
-__device__ __forceinline__ void convert_stage(uint8_t* base, int ct) {
-#pragma unroll 1
-  for (int q = ct; q < (128 + BN) * 8; q += 128) {
-    const bool isP = q < 128 * 8;
-    const int rr = isP ? (q >> 3) : ((q - 1024) >> 3);
-    const int j = q & 7;
-    const uint8_t* src = base + C::kPBytes + C::kQBytes + (isP ? 0u : C::kP8Bytes) + rr * 128 +
-                         ((j ^ (rr & 7)) << 4);
-    const uint4 v = *reinterpret_cast<const uint4*>(src);
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+// Convert the int8 tile of `rows` rows (128 codes each) at src to fp16 at dst.
+// The 128 transform threads own 16-byte chunks q = ct + 128 k: one chunk
+// column j = ct % 8 and rows ct/8 + 16 k, so the swizzle phase (row % 8) is
+// the same for all of a thread's chunks.  All loads are issued first, then
+// the arithmetic, then the stores.
+template <int NCH>
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int rows, int ct) {
+  const int j = ct & 7;
+  const int r0 = ct >> 3;
+  const int sw = r0 & 7;                  // == (r0 + 16 k) & 7
+  const uint32_t src_off = static_cast<uint32_t>(r0) * 128u + (static_cast<uint32_t>(j ^ sw) << 4);
+  uint4 v[NCH];
+#pragma unroll
+  for (int k = 0; k < NCH; ++k)
+    v[k] = *reinterpret_cast<const uint4*>(src + src_off + static_cast<uint32_t>(k) * 16u * 128u);
+  // 16 fp16 values = two 16-byte chunks of fp16 atom j/4: chunks 2(j%4), +1
+  uint8_t* atom = dst + static_cast<uint32_t>(j >> 2) * static_cast<uint32_t>(rows) * 128u;
+  const int c0 = 2 * (j & 3);
+  const uint32_t d0 = static_cast<uint32_t>(r0) * 128u + (static_cast<uint32_t>(c0 ^ sw) << 4);
+  const uint32_t d1 = static_cast<uint32_t>(r0) * 128u + (static_cast<uint32_t>((c0 + 1) ^ sw) << 4);
+  const __half2 bias2 = __floats2half2_rn(1152.0f, 1152.0f);
+#pragma unroll
+  for (int k = 0; k < NCH; ++k) {
+    const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
     uint32_t h[8];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -440,21 +493,22 @@ __device__ __forceinline__ void convert_stage(uint8_t* base, int ct) {
       asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
       asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
       // fp16 0x64XX = 1024 + XX; subtracting 1152 = 1024 + 128 gives b exactly
-      const __half2 c = __floats2half2_rn(1152.0f, 1152.0f);
-      __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), c);
-      __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), c);
+      __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), bias2);
+      __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), bias2);
       h[2 * t] = *reinterpret_cast<uint32_t*>(&l2);
       h[2 * t + 1] = *reinterpret_cast<uint32_t*>(&h2);
     }
-    // 16 fp16 values = two 16-byte chunks: atom j/4, chunks 2*(j%4) and +1
-    uint8_t* atom = base + (isP ? 0u : C::kPBytes) +
-                    static_cast<uint32_t>(j >> 2) * (isP ? 128u : static_cast<uint32_t>(BN)) * 128u;
-    const int c0 = 2 * (j & 3);
-    *reinterpret_cast<uint4*>(atom + rr * 128 + ((c0 ^ (rr & 7)) << 4)) =
-        make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(atom + rr * 128 + (((c0 + 1) ^ (rr & 7)) << 4)) =
-        make_uint4(h[4], h[5], h[6], h[7]);
+    const uint32_t rk = static_cast<uint32_t>(k) * 16u * 128u;
+    *reinterpret_cast<uint4*>(atom + d0 + rk) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(atom + d1 + rk) = make_uint4(h[4], h[5], h[6], h[7]);
   }
+}
+
+template <int BN, class C>
+__device__ __forceinline__ void convert_stage(const uint8_t* src8, uint8_t* dst16, int ct) {
+  static_assert(BN % 16 == 0, "Q tile rows come in groups of 16");
+  convert_tile<8>(src8, dst16, 128, ct);                                  // P: 128 rows
+  convert_tile<BN / 16>(src8 + C::kP8Bytes, dst16 + C::kPBytes, BN, ct);  // Q: BN rows
 }
 
 // One work unit = one 128 x BN output tile and one K split.
@@ -532,6 +586,10 @@ __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it
 // thread's release-acquire increment at GPU scope; the last CTA's acquire,
 // followed by the barrier, orders its reads of the other partials after
 // them (the semaphore pattern of split-K GEMMs).
+__device__ __forceinline__ void red_add_s32(int* addr, int v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
   int old;
   asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;"
@@ -542,18 +600,55 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
 }
 
 __device__ __forceinline__ bool split_arrive_last(const KParams& p, int tile, int contrib, int ept,
-                                                  int* last_flag) {
-  epi_bar_sync();
+                                                  int nthreads, int* last_flag) {
+  epi_bar_sync(nthreads);
   if (ept == 0) {
     const int prev = atom_add_acq_rel_gpu(p.counters + tile, 1);
     const int last = (prev == contrib - 1);
     if (last) p.counters[tile] = 0;  // ready for the next call (stream-ordered)
     *last_flag = last;
   }
-  epi_bar_sync();
+  epi_bar_sync(nthreads);
   const bool last = *last_flag != 0;
-  epi_bar_sync();  // the flag is rewritten by the next unit
+  epi_bar_sync(nthreads);  // the flag is rewritten by the next unit
   return last;
+}
+
+// The last CTA of a tile sums the tile's partials (its own one included, read
+// back from the workspace) for NV consecutive columns starting at col_first,
+// in contributor order 0..contrib-1, so the result is the same whichever CTA
+// arrives last.  G contributors' loads are issued per round, so the latency
+// is paid once per G contributors, not once per contributor.
+template <int IN, int BN, int NV>
+__device__ __forceinline__ void reduce_partials(const KParams& p, int tile, int contrib,
+                                                int col_first, int lane_row, bool row_valid,
+                                                int cols_left, uint32_t (&acc)[NV]) {
+  constexpr int G = (32 / NV) < 1 ? 1 : ((32 / NV) > 8 ? 8 : (32 / NV));
+  for (int s0 = 0; s0 < contrib; s0 += G) {
+    uint32_t v[G][NV];
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      const bool su = s0 + u < contrib;
+      const uint32_t* wsb = ws_slot<BN>(p, su ? s0 + u : 0, tile, col_first, lane_row);
+#pragma unroll
+      for (int c = 0; c < NV; ++c)
+        v[u][c] = (su && row_valid && c < cols_left) ? __ldcg(wsb + c * 128) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      if (s0 + u < contrib) {
+#pragma unroll
+        for (int c = 0; c < NV; ++c) {
+          if (s0 + u == 0)
+            acc[c] = v[u][c];
+          else if (IN == IN_INT8)
+            acc[c] = static_cast<uint32_t>(static_cast<int32_t>(acc[c]) + static_cast<int32_t>(v[u][c]));
+          else
+            acc[c] = __float_as_uint(__fadd_rn(__uint_as_float(acc[c]), __uint_as_float(v[u][c])));
+        }
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- kernel ---
@@ -563,8 +658,8 @@ __device__ __forceinline__ bool split_arrive_last(const KParams& p, int tile, in
 // units, so the epilogue of one unit overlaps the UMMA mainloop of the next.
 
 template <int IN, int SC, bool SWAP, int BN>
-__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
-                                  Cfg<IN, SC, SWAP, BN>::kMinBlocks)
+__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
+    __maxnreg__((Cfg<IN, SC, SWAP, BN>::kMaxRegs))
     fused_linear_kernel(const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmQ, const KParams p) {
   using C = Cfg<IN, SC, SWAP, BN>;
@@ -573,18 +668,30 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  // ring layout: per stage [P | Q | P8 | Q8], each part a multiple of 1 KB
+  // Shared memory: [TMA ring: S stages of (P | Q), or (P8 | Q8) for INT8]
+  // [INT8: 2 fp16 operand slots of (P | Q)] [barriers, 512 B] [block scales].
+  // Every tile part is a multiple of 1 KB, so 1024-byte alignment holds.
   auto stage_base = [&](int s) { return smem + static_cast<uint32_t>(s) * C::kStageBytes; };
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<uint32_t>(S) * C::kStageBytes);
+  uint8_t* op_area = smem + static_cast<uint32_t>(S) * C::kStageBytes;
+  // UMMA operands of ring iteration g: the ring stage itself, or (INT8) the
+  // fp16 slot the transform warps wrote
+  auto op_base = [&](uint32_t g) {
+    return C::kConvert ? op_area + (g % C::kOpSlots) * (C::kPBytes + C::kQBytes)
+                       : stage_base(static_cast<int>(g % S));
+  };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(op_area + C::kOpBytes);
   uint64_t* full = bars;              // TMA landed (expect_tx)
-  uint64_t* empty = bars + S;         // slot free (UMMA commit, or converter)
-  uint64_t* bfull = bars + 2 * S;     // converted operands ready (INT8)
-  uint64_t* bempty = bars + 3 * S;    // converted operands consumed (INT8)
-  uint64_t* tfull = bars + 4 * S;     // [2] TMEM buffer holds a finished K block / tile
-  uint64_t* tempty = tfull + 2;       // [2] TMEM buffer drained by the epilogue
-  uint64_t* mma_done = tempty + 2;
+  uint64_t* empty = bars + S;         // ring stage free (UMMA commit, or converter)
+  uint64_t* bfull = bars + 2 * S;     // [2] fp16 operands ready (INT8)
+  uint64_t* bempty = bars + 3 * S;    // [2] fp16 operands consumed (INT8)
+  constexpr int NB = C::kAccBufs;
+  uint64_t* tfull = bars + 4 * S;     // [NB] TMEM buffer holds a finished K block / tile
+  uint64_t* tempty = tfull + NB;      // [NB] TMEM buffer drained by the epilogue
+  uint64_t* mma_done = tempty + NB;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  // block scales of the current unit (block scaling only; sized by the host)
+  float* scale_smem = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512u);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -603,9 +710,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
       mbar_init(&bfull[s], 128);
       mbar_init(&bempty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], C::kEpiThreads);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -630,9 +737,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
       auto load_op = [&](bool weight, const Unit& w, int i, int s) {
         uint8_t* base = stage_base(s);
         const bool isP = (weight == SWAP);
-        uint8_t* dst = C::kConvert
-                           ? base + C::kPBytes + C::kQBytes + (isP ? 0u : C::kP8Bytes)
-                           : base + (isP ? 0u : C::kPBytes);
+        uint8_t* dst = base + (isP ? 0u : (C::kConvert ? C::kP8Bytes : C::kPBytes));
         const int kx = (w.kt0 + i) * C::kElemsPerStage;
         const CUtensorMap* map = isP ? &tmP : &tmQ;
         const int y = isP ? w.row0 : w.col0;
@@ -695,8 +800,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
       while (ok && work_next(p, BN, it, w)) {
         if (!C::kPromote) {
           // one TMEM buffer per unit; wait until the epilogue drained it
-          const int b = blk & 1;
-          if (!mbar_wait(&tempty[b], ((blk >> 1) & 1u) ^ 1u, lim)) {
+          const int b = blk % NB;
+          if (!mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
             record_status(p.status, ST_TIMEOUT_MMA);
             ok = false;
             break;
@@ -705,13 +810,16 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
         for (int i = 0; i < w.nk; ++i, ++g) {
           const int s = static_cast<int>(g % S);
           const uint32_t ph = (g / S) & 1u;
-          const int b = blk & 1;
-          if (C::kPromote && !mbar_wait(&tempty[b], ((blk >> 1) & 1u) ^ 1u, lim)) {
+          const int b = blk % NB;
+          if (C::kPromote && !mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
             record_status(p.status, ST_TIMEOUT_MMA);
             ok = false;
             break;
           }
-          if (!mbar_wait(C::kConvert ? &bfull[s] : &full[s], ph, lim)) {
+          // INT8: fp16 operand slot g%2 (its own phase); else the ring stage
+          const int os = static_cast<int>(g % C::kOpSlots);
+          const uint32_t oph = (g / C::kOpSlots) & 1u;
+          if (!mbar_wait(C::kConvert ? &bfull[os] : &full[s], C::kConvert ? oph : ph, lim)) {
             record_status(p.status, ST_TIMEOUT_MMA);
             ok = false;
             break;
@@ -719,7 +827,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
           tc_fence_after();
           if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
           const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
-          const uint32_t pa = smem_u32(stage_base(s));
+          const uint32_t pa = smem_u32(op_base(g));
           const uint32_t qa = pa + C::kPBytes;
 #pragma unroll
           for (int a = 0; a < C::kAtoms; ++a) {
@@ -734,21 +842,21 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
                 umma_f16(d, ad, bd, C::kIdesc, accum);
             }
           }
-          umma_commit(C::kConvert ? &bempty[s] : &empty[s]);
+          umma_commit(C::kConvert ? &bempty[os] : &empty[s]);
           if (C::kPromote) {
             umma_commit(&tfull[b]);
             ++blk;
           }
         }
         if (!C::kPromote && ok) {
-          if (w.nk > 0) umma_commit(&tfull[blk & 1]);
+          if (w.nk > 0) umma_commit(&tfull[blk % NB]);
           ++blk;
         }
       }
       trace_point(p, TR_LAST_COMMIT);
       umma_commit(mma_done);
     }
-  } else if (warp >= 6) {
+  } else if (C::kConvert && warp >= 6) {
     // ---------------------------------- INT8 -> fp16 prologue transform ----
     if constexpr (C::kConvert) {
       const int ct = threadIdx.x - 192;  // 0..127
@@ -758,17 +866,19 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
       Unit w;
       while (ok && work_next(p, BN, it, w)) {
         for (int i = 0; i < w.nk; ++i, ++g) {
-          const int s = static_cast<int>(g % S);
+          const int s = static_cast<int>(g % S);           // int8 ring stage
           const uint32_t ph = (g / S) & 1u;
-          if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[s], ph ^ 1u, lim)) {
+          const int os = static_cast<int>(g % C::kOpSlots);  // fp16 operand slot
+          const uint32_t oph = (g / C::kOpSlots) & 1u;
+          if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[os], oph ^ 1u, lim)) {
             record_status(p.status, ST_TIMEOUT_CONVERT);
             ok = false;
             break;
           }
-          convert_stage<BN, C>(stage_base(s), ct);
+          convert_stage<BN, C>(stage_base(s), op_base(g), ct);
           fence_proxy_async_smem();
           mbar_arrive(&empty[s]);
-          mbar_arrive(&bfull[s]);
+          mbar_arrive(&bfull[os]);
         }
       }
     }
@@ -776,8 +886,13 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
     // ----------------------------------------------------- epilogue ----
     const int quarter = warp & 3;
     const int lane_row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int ept = threadIdx.x - 64;  // 0..127
+    constexpr int CPT = C::kColsPerThread;
+    static_assert(C::kPromote || CPT == BN, "the TMEM-resident path uses 4 epilogue warps");
+    // this thread's first column in the tile
+    const int cbeg = (C::kEpiWarps == 4) ? 0 : ((warp - 2) >> 2) * CPT;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                            static_cast<uint32_t>(cbeg);
+    const int ept = threadIdx.x - 64;  // 0 .. kEpiThreads-1
     griddep_wait();
     uint32_t blk = 0;
     bool ok = true;
@@ -787,26 +902,38 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
       const int row = w.row0 + lane_row;
       if constexpr (C::kPromote) {
         // ---- promotion: per 128-K block, TMEM buffer -> registers ----
-        uint32_t acc[BN];
+        uint32_t acc[CPT];
 #pragma unroll
-        for (int c = 0; c < BN; ++c) acc[c] = 0u;  // +0.0f or int 0
-        auto row_scale = [&](int kb) -> float {
-          if constexpr (SC == SC_BLOCK) {
-            if (!SWAP) {
-              const float sw = __ldg(p.s_w + (w.col0 / 128) * p.kb_count + kb);
-              return (row < p.M) ? __ldg(p.s_a + static_cast<int64_t>(row) * p.kb_count + kb) * sw
-                                 : 0.0f;
-            }
-            return __ldg(p.s_w + w.tile_r * p.kb_count + kb);
+        for (int c = 0; c < CPT; ++c) acc[c] = 0u;  // +0.0f or int 0
+        // Block scales of this unit's K range, staged in shared memory once
+        // per unit (one K block of UMMA is shorter than a global load's
+        // latency): sc_a[t][i] = s_a of tile row/column t at K block kt0+i,
+        // row stride nk+1 (no bank conflicts), then sc_w[i].
+        float* sc_a = scale_smem;
+        float* sc_w = scale_smem + (SWAP ? BN : 128) * (w.nk + 1);
+        if constexpr (SC == SC_BLOCK) {
+          const int T = SWAP ? BN : 128;
+          const int base = SWAP ? w.col0 : w.row0;
+          const int lim_t = SWAP ? p.M : p.M;  // s_a rows are tokens in both layouts
+          epi_bar_sync(C::kEpiThreads);        // the previous unit's reads are done
+          for (int idx = ept; idx < T * w.nk; idx += C::kEpiThreads) {
+            const int t = idx / w.nk, i = idx - t * w.nk;
+            const int m = base + t;
+            sc_a[t * (w.nk + 1) + i] =
+                (m < lim_t) ? __ldg(p.s_a + static_cast<int64_t>(m) * p.kb_count + w.kt0 + i) : 0.0f;
           }
-          return 1.0f;
-        };
-        float srow_next = (w.nk > 0) ? row_scale(w.kt0) : 1.0f;
+          const int wrow = SWAP ? w.tile_r : (w.col0 / 128);
+          for (int i = ept; i < w.nk; i += C::kEpiThreads)
+            sc_w[i] = __ldg(p.s_w + static_cast<int64_t>(wrow) * p.kb_count + w.kt0 + i);
+          epi_bar_sync(C::kEpiThreads);
+        }
         for (int i = 0; i < w.nk; ++i, ++blk) {
-          const int b = blk & 1;
-          const uint32_t bph = (blk >> 1) & 1u;
-          const float srow = srow_next;  // loaded one block ahead
-          if (i + 1 < w.nk) srow_next = row_scale(w.kt0 + i + 1);
+          const int b = blk % NB;
+          const uint32_t bph = (blk / NB) & 1u;
+          float srow = 1.0f;  // scale shared by the thread's row (block scaling)
+          if constexpr (SC == SC_BLOCK) {
+            srow = SWAP ? sc_w[i] : sc_a[lane_row * (w.nk + 1) + i] * sc_w[i];
+          }
           if (!mbar_wait(&tfull[b], bph, lim)) {
             record_status(p.status, ST_TIMEOUT_EPILOGUE);
             ok = false;
@@ -814,73 +941,73 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
           }
           tc_fence_after();
           if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
+          // all of this thread's columns of the block, then one wait
+          uint32_t r[CPT];
 #pragma unroll
-          for (int c = 0; c < BN; c += CW) {
-            uint32_t r[CW];
-            tmem_load_chunk<CW>(t_lane + static_cast<uint32_t>(b * BN + c), r);
-            tmem_ld_wait();
+          for (int c = 0; c < CPT; c += CW)
+            tmem_load_chunk_p<CW>(t_lane + static_cast<uint32_t>(b * BN + c), r + c);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&tempty[b]);  // the buffer is free once the values are in registers
 #pragma unroll
-            for (int j = 0; j < CW; ++j) {
-              if constexpr (SC == SC_BLOCK) {
-                float s = srow;
-                if (SWAP) {
-                  const int m = w.col0 + c + j;
-                  s = (m < p.M)
-                          ? srow * __ldg(p.s_a + static_cast<int64_t>(m) * p.kb_count + w.kt0 + i)
-                          : 0.0f;
-                }
-                acc[c + j] = __float_as_uint(
-                    __fmaf_rn(s, __uint_as_float(r[j]), __uint_as_float(acc[c + j])));
-              } else {
-                acc[c + j] = static_cast<uint32_t>(static_cast<int32_t>(acc[c + j]) +
-                                                   __float2int_rn(__uint_as_float(r[j])));
-              }
+          for (int c = 0; c < CPT; ++c) {
+            if constexpr (SC == SC_BLOCK) {
+              float s = srow;
+              if (SWAP) s = srow * sc_a[(cbeg + c) * (w.nk + 1) + i];  // 0 beyond M
+              acc[c] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[c]), __uint_as_float(acc[c])));
+            } else {
+              acc[c] = static_cast<uint32_t>(static_cast<int32_t>(acc[c]) +
+                                             __float2int_rn(__uint_as_float(r[c])));
             }
           }
-          tc_fence_before();
-          mbar_arrive(&tempty[b]);
         }
         if (!ok) break;
         bool do_epi = true;
         if (w.contrib > 1) {
+          if constexpr (IN == IN_INT8) {
+            // int32 sums are exact in any order: every contributor adds its
+            // partial into the tile's slot 0 (kept at zero between calls);
+            // the last one reads the total in one round and re-zeroes it
+            uint32_t* wsb = ws_slot<BN>(p, 0, w.tile, cbeg, lane_row);  // column stride 128
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (row < p.rows && w.col0 + c < p.cols)
-              __stcg(ws_slot<BN>(p, w.j, w.tile, c, lane_row), acc[c]);
-          do_epi = split_arrive_last(p, w.tile, w.contrib, ept, last_flag);
-          if (do_epi) {
-            // partials in split order 0..S-1 (this CTA's own one is read back
-            // from the workspace too); per split, independent loads
-            const bool rv = row < p.rows;
-            for (int s2 = 0; s2 < w.contrib; ++s2) {
+            for (int c = 0; c < CPT; ++c)
+              if (row < p.rows && w.col0 + cbeg + c < p.cols)
+                red_add_s32(reinterpret_cast<int*>(wsb + c * 128), static_cast<int32_t>(acc[c]));
+            do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
+            if (do_epi) {
 #pragma unroll
-              for (int c = 0; c < BN; ++c) {
-                const bool okc = rv && w.col0 + c < p.cols;
-                const uint32_t v = okc ? __ldcg(ws_slot<BN>(p, s2, w.tile, c, lane_row)) : 0u;
-                if (IN == IN_INT8)
-                  acc[c] = (s2 == 0) ? v
-                                     : static_cast<uint32_t>(static_cast<int32_t>(acc[c]) +
-                                                             static_cast<int32_t>(v));
-                else
-                  acc[c] = (s2 == 0) ? v
-                                     : __float_as_uint(__fadd_rn(__uint_as_float(acc[c]),
-                                                                 __uint_as_float(v)));
+              for (int c = 0; c < CPT; ++c) {
+                const bool okc = row < p.rows && w.col0 + cbeg + c < p.cols;
+                acc[c] = okc ? __ldcg(wsb + c * 128) : 0u;
               }
+#pragma unroll
+              for (int c = 0; c < CPT; ++c)
+                if (row < p.rows && w.col0 + cbeg + c < p.cols) __stcg(wsb + c * 128, 0u);
+            }
+          } else {
+            uint32_t* wsb = ws_slot<BN>(p, w.j, w.tile, cbeg, lane_row);  // column stride 128
+#pragma unroll
+            for (int c = 0; c < CPT; ++c)
+              if (row < p.rows && w.col0 + cbeg + c < p.cols) __stcg(wsb + c * 128, acc[c]);
+            do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
+            if (do_epi) {
+              reduce_partials<IN, BN, CPT>(p, w.tile, w.contrib, cbeg, lane_row, row < p.rows,
+                                           p.cols - (w.col0 + cbeg), acc);
             }
           }
         }
         if (do_epi) {
 #pragma unroll
-          for (int c = 0; c < BN; c += CW) {
+          for (int c = 0; c < CPT; c += CW) {
             uint32_t r[CW];
 #pragma unroll
             for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
-            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + c, r);
+            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + cbeg + c, r);
           }
         }
       } else {
         // ---- accumulator in TMEM buffer blk&1 until the unit is done ----
-        const int b = blk & 1;
+        const int b = blk % NB;
         const uint32_t tb = t_lane + static_cast<uint32_t>(b * BN);
         // swap-AB with one chunk (decode): epilogue inputs load while the
         // mainloop runs
@@ -890,7 +1017,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
           if (!(p.flags & F_DEBUG)) load_swap_inputs<SC, CW>(p, row, w.col0, pre);
         }
         if (w.nk > 0) {
-          if (!mbar_wait(&tfull[b], (blk >> 1) & 1u, lim)) {
+          if (!mbar_wait(&tfull[b], (blk / NB) & 1u, lim)) {
             record_status(p.status, ST_TIMEOUT_EPILOGUE);
             ok = false;
             break;
@@ -905,12 +1032,12 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
             uint32_t r[CW];
             tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
             tmem_ld_wait();
+            uint32_t* wsb = ws_slot<BN>(p, w.j, w.tile, c, lane_row);  // column stride 128
 #pragma unroll
             for (int j = 0; j < CW; ++j)
-              if (row < p.rows && w.col0 + c + j < p.cols)
-                __stcg(ws_slot<BN>(p, w.j, w.tile, c + j, lane_row), r[j]);
+              if (row < p.rows && w.col0 + c + j < p.cols) __stcg(wsb + j * 128, r[j]);
           }
-          do_epi = split_arrive_last(p, w.tile, w.contrib, ept, last_flag);
+          do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
         }
         if (do_epi) {
 #pragma unroll 1
@@ -924,25 +1051,11 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads,
               for (int j = 0; j < CW; ++j) r[j] = 0u;
             }
             if (w.contrib > 1) {
-              // partials summed in split order 0..S-1 (deterministic); per
-              // split, the chunk's loads are independent and overlap
-              float tot[CW];
-              const bool rv = row < p.rows;
-              for (int s2 = 0; s2 < w.contrib; ++s2) {
-                float v[CW];
-#pragma unroll
-                for (int j = 0; j < CW; ++j) {
-                  const bool okc = rv && w.col0 + c + j < p.cols;
-                  v[j] = (s2 == w.j)
-                             ? __uint_as_float(r[j])
-                             : (okc ? __uint_as_float(__ldcg(ws_slot<BN>(p, s2, w.tile, c + j, lane_row)))
-                                    : 0.0f);
-                }
-#pragma unroll
-                for (int j = 0; j < CW; ++j) tot[j] = (s2 == 0) ? v[j] : __fadd_rn(tot[j], v[j]);
-              }
-#pragma unroll
-              for (int j = 0; j < CW; ++j) r[j] = __float_as_uint(tot[j]);
+              // partials summed in split order 0..S-1 (deterministic; this
+              // CTA's own one is read back too); per split, the chunk's loads
+              // are independent and overlap
+              reduce_partials<IN, BN, CW>(p, w.tile, w.contrib, c, lane_row, row < p.rows,
+                                          p.cols - (w.col0 + c), r);
             }
             if constexpr (kPre) {
               if (!(p.flags & F_DEBUG)) {

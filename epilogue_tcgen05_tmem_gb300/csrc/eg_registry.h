@@ -34,7 +34,7 @@ EG_DECLARE_LOOKUP(lookup_int8_tc)
     using C_ = ::eg::Cfg<IN, SC, SWAP, BN>;                                            \
     out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN>); \
     out->stage_bytes = C_::kStageBytes;                                                \
-    out->fixed_bytes = 1024u + 512u;                                                   \
+    out->fixed_bytes = 1024u + 512u + C_::kOpBytes;                                    \
     out->threads = C_::kThreads;                                                       \
     out->elems_per_stage = C_::kElemsPerStage;                                         \
     out->tmem_cols = static_cast<int>(C_::kTmemCols);                                  \

@@ -44,7 +44,8 @@ bool tuning_default(const eg_problem& p, int sms, eg_tuning* out) {
     // decode: rows over N (swap-AB), columns over the few tokens
     t.swap_ab = 1;
     t.tile_n = p.M <= 16 ? 16 : (p.M <= 32 ? 32 : 64);
-    t.stages = (p.dtype == EG_IN_INT8) ? 3 : 4;
+    // INT8: a deep int8 staging ring (the fp16 operand ring is separate)
+    t.stages = (p.dtype == EG_IN_INT8) ? 8 : 4;
   } else {
     t.swap_ab = 0;
     const int max_bn = p.dtype == EG_IN_INT8 ? 64 : (promote ? 128 : 256);
@@ -55,9 +56,11 @@ bool tuning_default(const eg_problem& p, int sms, eg_tuning* out) {
   }
   KernelEntry ke;
   if (!entry_for(p, t.swap_ab, t.tile_n, &ke)) return false;
-  while (t.stages > 2 && ke.fixed_bytes + uint32_t(t.stages) * ke.stage_bytes > kSmemPerBlock)
+  const uint32_t extra = static_cast<uint32_t>(
+      block_scale_smem_bytes(p, t.swap_ab, t.tile_n, ke.elems_per_stage));
+  while (t.stages > 2 && ke.fixed_bytes + uint32_t(t.stages) * ke.stage_bytes + extra > kSmemPerBlock)
     --t.stages;
-  const uint32_t smem = ke.fixed_bytes + uint32_t(t.stages) * ke.stage_bytes;
+  const uint32_t smem = ke.fixed_bytes + uint32_t(t.stages) * ke.stage_bytes + extra;
   int per_sm = static_cast<int>(kSmemPerSm / (smem + 1024));
   if (per_sm < 1) per_sm = 1;
   if (per_sm > 2) per_sm = 2;
