@@ -291,7 +291,7 @@ def run_native(args):
         "per_m": per_m,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": None, "peak_source": peaks["source"],
+                     "traffic": measured_traffic("fp8_dynamic_decode"), "peak_source": peaks["source"],
                      "kernel": "fused_linear_kernel<e4m3, token_channel, swap_ab>"},
         "e2e": e2e, "gpu_launches": args.steps * calls_per_step, "clocks": clocks,
     }
@@ -303,6 +303,31 @@ def run_native(args):
         print(json.dumps(out), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def kernel_source_sha256():
+    """Hash of the fused kernel's device sources: a stored ncu traffic figure
+    holds only for the kernel it was captured on."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("eg_kernel.cuh", "eg_ptx.cuh"):
+        with open(os.path.join(ROOT, "epilogue_tcgen05_tmem_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(key):
+    """DRAM bytes (read + write) per launch from the committed ncu summary of
+    this kernel, or None when there is none or the kernel has changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh).get(key)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_source_sha256") != kernel_source_sha256():
+        return None
+    return rec["dram_bytes_per_launch"]
 
 
 def run_e2e(args, torch, eg, plans, acts, Wd, tokens, bytes_per_step, stream):

@@ -513,8 +513,11 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
     eg_plan_destroy(pl);
     return st;
   };
+  // The attribute belongs to the kernel function, which plans with other
+  // ring depths share: allow the device maximum (each launch still passes
+  // its own size), so that a later plan cannot shrink an earlier one's limit.
   cudaError_t e = cudaFuncSetAttribute(ke.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+                                       static_cast<int>(kMaxSmem));
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaFuncSetAttribute"));
   // operands arrive through TMA into shared memory: prefer the largest
   // shared-memory carveout so that several CTAs can be resident per SM
@@ -891,7 +894,7 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   pl.ws = static_cast<unsigned char*>(scratch) + kScratchCounterBytes;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   EG_CUDA(cudaFuncSetAttribute(pl.ke.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)),
+                               static_cast<int>(kMaxSmem)),
           "cudaFuncSetAttribute");
   // the arrival counters and the status word start every call at zero (the
   // array keeps whatever the previous call left)

@@ -350,3 +350,17 @@ def test_balanced_split_k_int8_exact(sk):
     assert np.array_equal(yacc.numpy().astype(np.int64), acc64)
     y, _ = run(p, t)
     assert ulp_dist(bits(y), oracle.linear(p)).max() <= 1
+
+
+def test_plans_sharing_a_kernel_with_other_ring_depths():
+    """Two plans of the same kernel instantiation with different stage
+    counts: creating the shallower one must not break the deeper one."""
+    p = inputs.make_problem(4, 512, 1024, "e4m3", "token_channel", act="silu", bias=True, seed=2)
+    deep = make_plan(p, dict(tile_n=16, stages=6, split_k=2, swap_ab=1))
+    shallow = make_plan(p, dict(tile_n=16, stages=2, split_k=2, swap_ab=1))
+    ref = oracle.linear(p)
+    for plan in (deep, shallow, deep):
+        y, _ = run(p, plan=plan)
+        assert_close_rms(bits(y), ref)
+    deep.close()
+    shallow.close()
