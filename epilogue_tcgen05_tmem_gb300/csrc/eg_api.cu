@@ -171,6 +171,13 @@ bool lookup_kernel(const eg_problem& p, int swap, int bn, eg::KernelEntry* ke) {
 
 constexpr uint32_t kMaxSmem = 232448;  // opt-in dynamic shared memory per block on sm_100/103
 
+// Cluster split-K exchange buffer: [split][128 / split rows][tile_n + 4]
+// fp32 words, i.e. 128 padded rows whatever the split.  The kernel lays it
+// over its operand ring (TMA stages and, for INT8, the fp16 operand slots).
+uint64_t red_buffer_bytes(const eg_tuning& t) {
+  return t.cluster_reduce ? uint64_t(t.tile_n + 4) * 128u * 4u : 0u;
+}
+
 eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEntry* ke,
                           uint32_t* smem, int* k_tiles) {
   if (t.swap_ab != 0 && t.swap_ab != 1)
@@ -180,6 +187,19 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
                 t.tile_n, t.swap_ab);
   if (t.stages < 2 || t.stages > 8)
     return fail(EG_ERR_UNSUPPORTED, "stages must be in 2..8 (got %d)", t.stages);
+  if (t.cluster_reduce != 0 && t.cluster_reduce != 1)
+    return fail(EG_ERR_INVALID_ARG, "cluster_reduce must be 0 or 1");
+  if (t.cluster_reduce) {
+    if (t.split_k != 2 && t.split_k != 4 && t.split_k != 8)
+      return fail(EG_ERR_UNSUPPORTED, "cluster_reduce needs split_k in {2, 4, 8} (got %d)", t.split_k);
+    if (t.stream_k != 0)
+      return fail(EG_ERR_INVALID_ARG, "cluster_reduce and balanced split-K exclude each other");
+  }
+  const uint64_t ring = uint64_t(t.stages) * ke->stage_bytes + ke->op_bytes;
+  if (red_buffer_bytes(t) > ring)
+    return fail(EG_ERR_UNSUPPORTED,
+                "cluster_reduce with tile_n=%d needs %llu bytes of operand ring; %d stages give %llu",
+                t.tile_n, (unsigned long long)red_buffer_bytes(t), t.stages, (unsigned long long)ring);
   const uint64_t s = ke->fixed_bytes + uint64_t(t.stages) * ke->stage_bytes +
                      eg::block_scale_smem_bytes(p, t.swap_ab, t.tile_n, ke->elems_per_stage);
   if (s > kMaxSmem)
@@ -206,6 +226,70 @@ int sm_count_of(int dev) {
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     n = 148;
   return n;
+}
+
+// CTAs of the plan's kernel that fit on one SM: shared memory (with the
+// per-block reservation), registers (allocated per warp in units of 256 and
+// spread over the SM's 4 sub-partitions), threads, blocks, and the 512 TMEM
+// columns.  Also records the kernel's registers per thread.
+eg_status residency(eg_plan* pl, int dev, int* per_sm_out) {
+  cudaFuncAttributes fa{};
+  EG_CUDA(cudaFuncGetAttributes(&fa, pl->ke.fn), "cudaFuncGetAttributes");
+  pl->regs = fa.numRegs;
+  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0, sm_blocks = 0;
+  EG_CUDA(cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev), "device limits");
+  EG_CUDA(cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev), "device limits");
+  const int warps = (pl->ke.threads + 31) / 32;
+  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+  const int warps_per_smsp = (sm_regs / 4) / std::max(1, regs_warp);
+  int per_sm = sm_smem / static_cast<int>(pl->smem + reserved);
+  per_sm = std::min(per_sm, (4 * warps_per_smsp) / warps);
+  per_sm = std::min(per_sm, sm_threads / pl->ke.threads);
+  per_sm = std::min(per_sm, sm_blocks);
+  per_sm = std::min(per_sm, 512 / pl->ke.tmem_cols);
+  if (per_sm < 1) return fail(EG_ERR_UNSUPPORTED, "the kernel does not fit on an SM");
+  *per_sm_out = per_sm;
+  return EG_OK;
+}
+
+// Launch grid, work units and partial-sum slots per tile of the plan's
+// tuning, for `per_sm` resident CTAs on each of `sms` SMs.
+void plan_grid(eg_plan* pl, int sms, int per_sm) {
+  const eg_tuning& t = pl->tune;
+  const long long tiles = static_cast<long long>(pl->tiles_rows) * pl->tiles_cols;
+  const long long units = tiles * t.split_k;
+  pl->blocks_per_sm = per_sm;
+  pl->max_contrib = t.split_k;
+  if (t.stream_k > 0) {
+    // balanced split-K: G CTAs share I = tiles x K-tiles iterations; CTA c
+    // owns [floor(c I/G), floor((c+1) I/G)); a tile has as many partial sums
+    // as CTAs whose ranges overlap it
+    const long long iters = tiles * pl->k_tiles;
+    long long G = static_cast<long long>(sms) * std::min(per_sm, t.stream_k);
+    if (G > iters) G = iters;
+    pl->grid = static_cast<int>(G);
+    pl->units = static_cast<int>(std::min<long long>(iters, INT32_MAX));
+    int mc = 1;
+    for (long long tile = 0; tile < tiles && G > 0; ++tile) {
+      const long long b = tile * pl->k_tiles, e2 = b + pl->k_tiles;
+      const long long first = ((b + 1) * G - 1) / iters, last = (e2 * G - 1) / iters;
+      mc = std::max(mc, static_cast<int>(last - first + 1));
+    }
+    pl->max_contrib = mc;
+  } else if (t.cluster_reduce) {
+    // one unit per CTA; the split_k CTAs of a tile form one cluster and the
+    // partial sums never leave shared memory
+    pl->grid = static_cast<int>(units);
+    pl->units = static_cast<int>(units);
+    pl->max_contrib = 1;
+  } else {
+    const long long slots = static_cast<long long>(sms) * per_sm;
+    pl->grid = static_cast<int>(units < slots ? units : slots);
+    pl->units = static_cast<int>(units);
+  }
 }
 
 eg_status encode_map(CUtensorMap* m, const void* base, int dtype, int64_t rows, int64_t K,
@@ -339,6 +423,7 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.l2_prefetch = pl->l2_prefetch;
   k.trace = pl->trace;
   k.trace_ctas = pl->trace_ctas;
+  k.cluster_reduce = pl->tune.cluster_reduce;
   // streamed weights: hint L2 to evict them first when the grid reads each
   // weight tile once (one tile column / row over the tokens)
   const bool w_once = pl->tune.swap_ab ? (pl->tiles_cols == 1) : (pl->tiles_rows == 1);
@@ -362,11 +447,23 @@ eg_status launch_fused(eg_plan* pl, const eg::KParams& kp, cudaStream_t st) {
   cfg.blockDim = dim3(pl->ke.threads);
   cfg.dynamicSmemBytes = pl->smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (kp.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (kp.cluster_reduce) {
+    // the split_k CTAs of a tile (consecutive blocks) form one cluster
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(kp.split_k);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = kp.pdl ? 1 : 0;
+  cfg.numAttrs = n;
   void* args[3] = {const_cast<CUtensorMap*>(&pl->tmP), const_cast<CUtensorMap*>(&pl->tmQ),
                    const_cast<eg::KParams*>(&kp)};
   EG_CUDA(cudaLaunchKernelExC(&cfg, pl->ke.fn, args), "launching the fused kernel");
@@ -506,7 +603,6 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   pl->cols = static_cast<int>(swap ? p.M : p.N);
   pl->tiles_rows = (pl->rows + 127) / 128;
   pl->tiles_cols = (pl->cols + t.tile_n - 1) / t.tile_n;
-  const int units = pl->tiles_rows * pl->tiles_cols * t.split_k;
   pl->wait_limit_ns = default_wait_limit_ns();
   if (const char* e2 = getenv("EG_PDL_L2_PREFETCH")) pl->l2_prefetch = atoi(e2) != 0;
   auto cleanup = [&](eg_status st) {
@@ -524,56 +620,10 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   e = cudaFuncSetAttribute(ke.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "setting the shared-memory carveout"));
-  cudaFuncAttributes fa{};
-  if ((e = cudaFuncGetAttributes(&fa, ke.fn)) != cudaSuccess)
-    return cleanup(cuda_fail(e, "cudaFuncGetAttributes"));
-  pl->regs = fa.numRegs;
-  // persistent grid: every resident CTA slot, at most one per work unit.
-  // Residency from the SM's limits: shared memory (with the per-block
-  // reservation), registers (allocated per warp in units of 256), threads,
-  // blocks, and the 512 TMEM columns.
-  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0, sm_blocks = 0;
-  if ((e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev)) != cudaSuccess)
-    return cleanup(cuda_fail(e, "device limits"));
-  const int warps = (ke.threads + 31) / 32;
-  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
-  // registers: 4 sub-partitions of sm_regs/4 each; the warps of all
-  // resident CTAs spread over them
-  const int warps_per_smsp = (sm_regs / 4) / std::max(1, regs_warp);
-  int per_sm = sm_smem / static_cast<int>(smem + reserved);
-  per_sm = std::min(per_sm, (4 * warps_per_smsp) / warps);
-  per_sm = std::min(per_sm, sm_threads / ke.threads);
-  per_sm = std::min(per_sm, sm_blocks);
-  per_sm = std::min(per_sm, 512 / ke.tmem_cols);
-  if (per_sm < 1) return cleanup(fail(EG_ERR_UNSUPPORTED, "the kernel does not fit on an SM"));
+  int per_sm = 0;
+  if ((s = residency(pl, dev, &per_sm)) != EG_OK) return cleanup(s);
+  plan_grid(pl, sm_count_of(dev), per_sm);
   const size_t tiles = size_t(pl->tiles_rows) * pl->tiles_cols;
-  pl->blocks_per_sm = per_sm;
-  pl->max_contrib = t.split_k;
-  if (t.stream_k > 0) {
-    // balanced split-K: G CTAs share I = tiles x K-tiles iterations; CTA c
-    // owns [floor(c I/G), floor((c+1) I/G)); a tile has as many partial sums
-    // as CTAs whose ranges overlap it
-    const long long iters = static_cast<long long>(tiles) * k_tiles;
-    long long G = static_cast<long long>(sm_count_of(dev)) * std::min(per_sm, t.stream_k);
-    if (G > iters) G = iters;
-    pl->grid = static_cast<int>(G);
-    pl->units = static_cast<int>(std::min<long long>(iters, INT32_MAX));
-    int mc = 1;
-    for (size_t tile = 0; tile < tiles && G > 0; ++tile) {
-      const long long b = static_cast<long long>(tile) * k_tiles, e2 = b + k_tiles;
-      const long long first = ((b + 1) * G - 1) / iters, last = (e2 * G - 1) / iters;
-      mc = std::max(mc, static_cast<int>(last - first + 1));
-    }
-    pl->max_contrib = mc;
-  } else {
-    const long long slots = static_cast<long long>(sm_count_of(dev)) * per_sm;
-    pl->grid = static_cast<int>(units < slots ? units : slots);
-    pl->units = units;
-  }
   if (pl->max_contrib > 1 && tiles > 0) {
     pl->ws_bytes = size_t(pl->max_contrib) * tiles * size_t(t.tile_n) * 128 * 4;
     if ((e = cudaMalloc(&pl->ws, pl->ws_bytes)) != cudaSuccess)
@@ -845,40 +895,9 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
 
   // work decomposition and scratch needs
   const size_t tiles = size_t(pl.tiles_rows) * pl.tiles_cols;
-  cudaFuncAttributes fa{};
-  EG_CUDA(cudaFuncGetAttributes(&fa, pl.ke.fn), "cudaFuncGetAttributes");
-  int sm_smem = 0, reserved = 0, sm_regs = 0, sm_threads = 0, sm_blocks = 0;
-  EG_CUDA(cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev), "device limits");
-  EG_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev), "device limits");
-  EG_CUDA(cudaDeviceGetAttribute(&sm_regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev), "device limits");
-  EG_CUDA(cudaDeviceGetAttribute(&sm_threads, cudaDevAttrMaxThreadsPerMultiProcessor, dev), "device limits");
-  EG_CUDA(cudaDeviceGetAttribute(&sm_blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev), "device limits");
-  const int warps = (pl.ke.threads + 31) / 32;
-  const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
-  const int warps_per_smsp = (sm_regs / 4) / std::max(1, regs_warp);
-  int per_sm = sm_smem / static_cast<int>(smem + reserved);
-  per_sm = std::min(per_sm, (4 * warps_per_smsp) / warps);
-  per_sm = std::min(per_sm, sm_threads / pl.ke.threads);
-  per_sm = std::min(per_sm, sm_blocks);
-  per_sm = std::min(per_sm, 512 / pl.ke.tmem_cols);
-  if (per_sm < 1) return fail(EG_ERR_UNSUPPORTED, "the kernel does not fit on an SM");
-  pl.max_contrib = t.split_k;
-  if (t.stream_k > 0) {
-    const long long iters = static_cast<long long>(tiles) * k_tiles;
-    long long G = static_cast<long long>(sm_count_of(dev)) * std::min(per_sm, t.stream_k);
-    if (G > iters) G = iters;
-    pl.grid = static_cast<int>(G);
-    int mc = 1;
-    for (size_t tile = 0; tile < tiles && G > 0; ++tile) {
-      const long long b = static_cast<long long>(tile) * k_tiles, e2 = b + k_tiles;
-      mc = std::max(mc, static_cast<int>((e2 * G - 1) / iters - ((b + 1) * G - 1) / iters + 1));
-    }
-    pl.max_contrib = mc;
-  } else {
-    const long long units = static_cast<long long>(tiles) * t.split_k;
-    const long long slots = static_cast<long long>(sm_count_of(dev)) * per_sm;
-    pl.grid = static_cast<int>(units < slots ? units : slots);
-  }
+  int per_sm = 0;
+  if ((s = residency(&pl, dev, &per_sm)) != EG_OK) return s;
+  plan_grid(&pl, sm_count_of(dev), per_sm);
   const size_t ws_need = pl.max_contrib > 1 ? size_t(pl.max_contrib) * tiles * size_t(t.tile_n) * 128 * 4 : 0;
   if (tiles > kScratchCounters || ws_need > kScratchWorkspaceBytes)
     return fail(EG_ERR_UNSUPPORTED,

@@ -81,6 +81,7 @@ struct KParams {
   int32_t trace_ctas;             // CTAs the trace buffer holds
   int32_t stream_k;               // balanced split-K over the grid (else split_k)
   int32_t max_contrib;            // workspace slots per tile
+  int32_t cluster_reduce;         // split-K through distributed shared memory
 };
 
 constexpr int kTracePoints = 8;
@@ -651,6 +652,180 @@ __device__ __forceinline__ void reduce_partials(const KParams& p, int tile, int 
   }
 }
 
+// Block scales of one unit into a shared-memory buffer, with asynchronous
+// copies (the caller commits and waits): sc_a[t][i] = s_a of tile row (or,
+// with swap-AB, column) t at K block kt0 + i, row stride nk + 1 (no bank
+// conflicts), zero beyond M; then sc_w[i] of the tile's weight block row.
+template <bool SWAP, int BN, int NT>
+__device__ __forceinline__ void stage_block_scales(const KParams& p, const Unit& w, float* buf,
+                                                   int ept) {
+  const int T = SWAP ? BN : 128;
+  const int base = SWAP ? w.col0 : w.row0;
+  float* sc_a = buf;
+  float* sc_w = buf + T * (w.nk + 1);
+  for (int idx = ept; idx < T * w.nk; idx += NT) {
+    const int t = idx / w.nk, i = idx - t * w.nk;
+    const int m = base + t;
+    const bool ok = m < p.M;
+    const float* src = p.s_a + (ok ? static_cast<int64_t>(m) * p.kb_count + w.kt0 + i : 0);
+    cp_async_4(sc_a + t * (w.nk + 1) + i, src, ok ? 4u : 0u);
+  }
+  const int wrow = SWAP ? w.tile_r : (w.col0 / 128);
+  for (int i = ept; i < w.nk; i += NT)
+    cp_async_4(sc_w + i, p.s_w + static_cast<int64_t>(wrow) * p.kb_count + w.kt0 + i, 4u);
+}
+
+// ------------------------------------------- split-K inside a cluster ----
+//
+// The S = split_k CTAs of a tile form one thread-block cluster (cluster rank
+// = split index j).  Rank o owns the tile's rows [o R, (o+1) R), R = 128 / S.
+// The exchange buffer of a CTA, [j][row - o R][BN + 4] fp32 words (rows
+// padded so that 16-byte reads of consecutive rows hit distinct banks), lies
+// over its operand ring, which is idle once the CTA's last UMMA completed.
+// All traffic is asynchronous remote stores that complete transaction bytes
+// on the receiving CTA's mbarrier, so no fences are needed:
+//   1. once its accumulator is final, CTA o writes one word into every CTA
+//      of the cluster (red_ready of each expects 4 S bytes): "my buffer is
+//      free";
+//   2. when red_ready completes, each epilogue thread sends the BN partial
+//      sums of its row to the row's owner (red_full of the owner expects
+//      S x its valid rows x BN x 4 bytes);
+//   3. the owner sums the S partials of each of its elements in split order
+//      j = 0..S-1 (the workspace path's order, so the results are the same)
+//      and runs the epilogue.
+
+__host__ __device__ constexpr int red_row_words(int bn) { return bn + 4; }
+
+// Bytes CTA `rank` of the cluster of unit w receives in step 2.
+__device__ __forceinline__ uint32_t cluster_bytes_expected(const KParams& p, int row0, int rank,
+                                                           int bn) {
+  const int R = 128 / p.split_k;
+  int rows = p.rows - (row0 + rank * R);
+  rows = rows < 0 ? 0 : (rows > R ? R : rows);
+  return static_cast<uint32_t>(p.split_k * rows * bn * 4);
+}
+
+// Step 1: thread o < S of the epilogue writes CTA o's flag word.
+__device__ __forceinline__ void cluster_signal_ready(const KParams& p, uint64_t* red_ready,
+                                                     uint32_t* flags, int ept) {
+  if (ept < p.split_k) {
+    const uint32_t o = static_cast<uint32_t>(ept);
+    const uint32_t me = cluster_ctarank();
+    st_async_u32(cluster_map(smem_u32(flags + me), o), me, cluster_map(smem_u32(red_ready), o));
+  }
+}
+
+// Step 2 for NV consecutive columns starting at col_first of this thread's
+// row (NV a multiple of 4).
+template <int BN, int NV>
+__device__ __forceinline__ void cluster_send(const KParams& p, uint32_t red_base, uint64_t* red_full,
+                                             const Unit& w, int lane_row, int col_first,
+                                             const uint32_t* vals) {
+  static_assert(NV % 4 == 0, "16-byte pieces");
+  const int R = 128 / p.split_k;
+  if (w.row0 + lane_row >= p.rows) return;
+  const uint32_t owner = static_cast<uint32_t>(lane_row / R);
+  const int lr = lane_row - static_cast<int>(owner) * R;
+  const uint32_t dst = cluster_map(red_base, owner) +
+                       static_cast<uint32_t>(((w.j * R + lr) * red_row_words(BN) + col_first) * 4);
+  const uint32_t bar = cluster_map(smem_u32(red_full), owner);
+#pragma unroll
+  for (int c = 0; c < NV; c += 4)
+    st_async_v4(dst + static_cast<uint32_t>(c * 4), vals[c], vals[c + 1], vals[c + 2], vals[c + 3], bar);
+}
+
+// Epilogue inputs that depend only on an owner thread's row (it keeps one
+// row): bias and weight scale (rows over N) or token scale (rows over M).
+// Loaded before the thread waits for the partial sums.
+struct RowIn {
+  float b, s;
+};
+
+template <int SC, bool SWAP>
+__device__ __forceinline__ RowIn cluster_row_inputs(const KParams& p, int row) {
+  RowIn in{0.0f, 1.0f};
+  if (row >= p.rows || (p.flags & F_DEBUG)) return in;
+  if (SWAP) {
+    if (p.flags & F_BIAS) in.b = __bfloat162float(p.bias[row]);
+    if (SC == SC_TC) in.s = __ldg(p.s_w + row);
+  } else {
+    if (SC == SC_TC) in.s = __ldg(p.s_a + row);
+  }
+  return in;
+}
+
+// Step 3.  Thread e keeps row e % R of the owned slice and handles the
+// 4-column groups e / R, + T / R, ... (T = epilogue threads, a multiple of
+// R): the group's global loads and S 16-byte partial reads first, then its
+// arithmetic and stores.  False on timeout.
+template <int IN, int SC, bool SWAP, int BN, int T>
+__device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uint32_t* red,
+                                                     uint64_t* red_full, const Unit& w, int ept,
+                                                     const RowIn& in) {
+  const int S = p.split_k;
+  const int R = 128 / S;
+  if (!mbar_wait_cluster(red_full, 0, p.wait_limit_ns)) return false;
+  const int rr = ept % R;
+  const int row = w.row0 + static_cast<int>(cluster_ctarank()) * R + rr;
+  if (row >= p.rows) return true;
+  const int cv = min(BN, p.cols - w.col0);
+  const int step = 4 * (T / R);
+  const bool debug = (p.flags & F_DEBUG) != 0;
+  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
+  const bool has_bias = (p.flags & F_BIAS) != 0;
+  constexpr int W = red_row_words(BN);
+  for (int c0 = 4 * (ept / R); c0 < cv; c0 += step) {
+    float rv[4], cs[4], cb[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const bool ok = c0 + g < cv && !debug;
+      const int col = w.col0 + c0 + g;
+      const int m = SWAP ? col : row, n = SWAP ? row : col;
+      rv[g] = (ok && has_res) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+      cs[g] = (ok && SC == SC_TC) ? __ldg(SWAP ? p.s_a + col : p.s_w + col) : 1.0f;
+      cb[g] = (ok && !SWAP && has_bias) ? __bfloat162float(p.bias[col]) : 0.0f;
+    }
+    uint4 v = *reinterpret_cast<const uint4*>(red + rr * W + c0);
+    for (int j = 1; j < S; ++j) {
+      const uint4 x = *reinterpret_cast<const uint4*>(red + (j * R + rr) * W + c0);
+      if (IN == IN_INT8) {
+        v.x = static_cast<uint32_t>(static_cast<int32_t>(v.x) + static_cast<int32_t>(x.x));
+        v.y = static_cast<uint32_t>(static_cast<int32_t>(v.y) + static_cast<int32_t>(x.y));
+        v.z = static_cast<uint32_t>(static_cast<int32_t>(v.z) + static_cast<int32_t>(x.z));
+        v.w = static_cast<uint32_t>(static_cast<int32_t>(v.w) + static_cast<int32_t>(x.w));
+      } else {
+        v.x = __float_as_uint(__fadd_rn(__uint_as_float(v.x), __uint_as_float(x.x)));
+        v.y = __float_as_uint(__fadd_rn(__uint_as_float(v.y), __uint_as_float(x.y)));
+        v.z = __float_as_uint(__fadd_rn(__uint_as_float(v.z), __uint_as_float(x.z)));
+        v.w = __float_as_uint(__fadd_rn(__uint_as_float(v.w), __uint_as_float(x.w)));
+      }
+    }
+    const uint32_t acc[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (c0 + g >= cv) break;
+      const int col = w.col0 + c0 + g;
+      const int m = SWAP ? col : row, n = SWAP ? row : col;
+      const int64_t at = static_cast<int64_t>(m) * p.ldy + n;
+      if (debug) {
+        reinterpret_cast<uint32_t*>(p.Y)[at] = acc[g];
+        continue;
+      }
+      // the scale is s_a[m] * s_w[n] in that order, as in the other paths
+      const float sa = SWAP ? cs[g] : in.s, sw = SWAP ? in.s : cs[g];
+      const float bias = SWAP ? in.b : cb[g];
+      uint16_t o;
+      if (IN == IN_INT8)
+        o = epi_int8(static_cast<int32_t>(acc[g]), sa, sw, bias, rv[g], p.act, p.flags);
+      else
+        o = __bfloat16_as_ushort(__float2bfloat16_rn(epi_value(
+            __uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f, bias, rv[g], p.act, p.flags)));
+      reinterpret_cast<__nv_bfloat16*>(p.Y)[at] = __ushort_as_bfloat16(o);
+    }
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- kernel ---
 //
 // Persistent: CTA b handles work units b, b + gridDim.x, ...  Ring stages,
@@ -688,10 +863,16 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
   uint64_t* tfull = bars + 4 * S;     // [NB] TMEM buffer holds a finished K block / tile
   uint64_t* tempty = tfull + NB;      // [NB] TMEM buffer drained by the epilogue
   uint64_t* mma_done = tempty + NB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* red_full = mma_done + 1;  // cluster split-K: this CTA's rows have all partials
+  uint64_t* red_ready = red_full + 1; // cluster split-K: every CTA's exchange buffer is free
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_ready + 1);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint32_t* red_flags = reinterpret_cast<uint32_t*>(last_flag + 1);  // [split_k] words
   // block scales of the current unit (block scaling only; sized by the host)
   float* scale_smem = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512u);
+  // cluster split-K exchange buffer [split][128 / split][BN + 4]: over the
+  // operand ring, once the ring is idle (the host checks that it fits)
+  uint32_t* red_buf = reinterpret_cast<uint32_t*>(smem);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -715,7 +896,18 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
       mbar_init(&tempty[b], C::kEpiThreads);
     }
     mbar_init(mma_done, 1);
+    mbar_init(red_full, 1);
+    mbar_init(red_ready, 1);
     fence_mbar_init();
+    if (p.cluster_reduce) {
+      // one unit per CTA: what this CTA will receive is known now, before
+      // any CTA of the cluster can send (they all pass the cluster barrier
+      // below first)
+      mbar_arrive_expect_tx(red_ready, 4u * static_cast<uint32_t>(p.split_k));
+      const int tile = static_cast<int>(blockIdx.x) / p.split_k;
+      mbar_arrive_expect_tx(red_full, cluster_bytes_expected(p, (tile % p.tiles_rows) * 128,
+                                                             static_cast<int>(cluster_ctarank()), BN));
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -724,6 +916,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // cluster split-K: every CTA's barriers are initialised before any remote
+  // arrival
+  if (p.cluster_reduce) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
   if (p.pdl && threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) trace_point(p, TR_SETUP);
@@ -898,33 +1093,48 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
     bool ok = true;
     WorkIter it = work_begin(p);
     Unit w;
+    // Block scales: without swap-AB (large M, many units per CTA) they are
+    // staged one unit ahead, into the other of two buffers, so their global
+    // latency overlaps the current unit; with swap-AB (decode, about one unit
+    // per CTA) each unit stages its own, all copies in flight at once.
+    constexpr int kScaleRows = SWAP ? BN : 128;
+    constexpr bool kAhead = (SC == SC_BLOCK) && !SWAP;
+    const int scale_buf_floats = (kScaleRows + 1) * (p.k_tiles + 1);
+    WorkIter it_pf = it;
+    uint32_t su = 0;
+    if constexpr (kAhead) {
+      Unit w0;
+      if (work_next(p, BN, it_pf, w0))
+        stage_block_scales<SWAP, BN, C::kEpiThreads>(p, w0, scale_smem, ept);
+      cp_async_commit();
+    }
     while (ok && work_next(p, BN, it, w)) {
       const int row = w.row0 + lane_row;
+      const uint32_t cur = su++;
       if constexpr (C::kPromote) {
         // ---- promotion: per 128-K block, TMEM buffer -> registers ----
         uint32_t acc[CPT];
 #pragma unroll
         for (int c = 0; c < CPT; ++c) acc[c] = 0u;  // +0.0f or int 0
-        // Block scales of this unit's K range, staged in shared memory once
-        // per unit (one K block of UMMA is shorter than a global load's
-        // latency): sc_a[t][i] = s_a of tile row/column t at K block kt0+i,
-        // row stride nk+1 (no bank conflicts), then sc_w[i].
-        float* sc_a = scale_smem;
-        float* sc_w = scale_smem + (SWAP ? BN : 128) * (w.nk + 1);
-        if constexpr (SC == SC_BLOCK) {
-          const int T = SWAP ? BN : 128;
-          const int base = SWAP ? w.col0 : w.row0;
-          const int lim_t = SWAP ? p.M : p.M;  // s_a rows are tokens in both layouts
-          epi_bar_sync(C::kEpiThreads);        // the previous unit's reads are done
-          for (int idx = ept; idx < T * w.nk; idx += C::kEpiThreads) {
-            const int t = idx / w.nk, i = idx - t * w.nk;
-            const int m = base + t;
-            sc_a[t * (w.nk + 1) + i] =
-                (m < lim_t) ? __ldg(p.s_a + static_cast<int64_t>(m) * p.kb_count + w.kt0 + i) : 0.0f;
-          }
-          const int wrow = SWAP ? w.tile_r : (w.col0 / 128);
-          for (int i = ept; i < w.nk; i += C::kEpiThreads)
-            sc_w[i] = __ldg(p.s_w + static_cast<int64_t>(wrow) * p.kb_count + w.kt0 + i);
+        // this unit's block scales (staged one unit ahead; layout in
+        // stage_block_scales)
+        float* sc_a = scale_smem + (kAhead ? (cur & 1u) * scale_buf_floats : 0);
+        float* sc_w = sc_a + kScaleRows * (w.nk + 1);
+        if constexpr (kAhead) {
+          // every thread is done with the other buffer (the previous unit's)
+          epi_bar_sync(C::kEpiThreads);
+          Unit wn;
+          if (work_next(p, BN, it_pf, wn))
+            stage_block_scales<SWAP, BN, C::kEpiThreads>(
+                p, wn, scale_smem + ((cur + 1u) & 1u) * scale_buf_floats, ept);
+          cp_async_commit();
+          cp_async_wait<1>();            // this thread's copies for this unit landed
+          epi_bar_sync(C::kEpiThreads);  // ... and every thread's
+        } else if constexpr (SC == SC_BLOCK) {
+          epi_bar_sync(C::kEpiThreads);  // the previous unit's reads of this buffer are done
+          stage_block_scales<SWAP, BN, C::kEpiThreads>(p, w, sc_a, ept);
+          cp_async_commit();
+          cp_async_wait<0>();
           epi_bar_sync(C::kEpiThreads);
         }
         for (int i = 0; i < w.nk; ++i, ++blk) {
@@ -962,6 +1172,27 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           }
         }
         if (!ok) break;
+        if (p.cluster_reduce) {
+          // every UMMA of the unit has completed (its last buffer was full),
+          // so this CTA's operand ring is idle
+          cluster_signal_ready(p, red_ready, red_flags, ept);
+          const RowIn rin = cluster_row_inputs<SC, SWAP>(
+              p, w.row0 + static_cast<int>(cluster_ctarank()) * (128 / p.split_k) + ept % (128 / p.split_k));
+          if (!mbar_wait_cluster(red_ready, 0, lim)) {
+            record_status(p.status, ST_TIMEOUT_EPILOGUE);
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int c = 0; c < CPT; c += CW)
+            cluster_send<BN, CW>(p, smem_u32(red_buf), red_full, w, lane_row, cbeg + c, acc + c);
+          if (!cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads>(p, red_buf, red_full, w, ept, rin)) {
+            record_status(p.status, ST_TIMEOUT_EPILOGUE);
+            ok = false;
+            break;
+          }
+          continue;
+        }
         bool do_epi = true;
         if (w.contrib > 1) {
           if constexpr (IN == IN_INT8) {
@@ -1014,7 +1245,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
         constexpr bool kPre = SWAP && BN == CW;
         SwapIn<CW> pre;
         if constexpr (kPre) {
-          if (!(p.flags & F_DEBUG)) load_swap_inputs<SC, CW>(p, row, w.col0, pre);
+          if (!(p.flags & F_DEBUG) && !p.cluster_reduce) load_swap_inputs<SC, CW>(p, row, w.col0, pre);
         }
         if (w.nk > 0) {
           if (!mbar_wait(&tfull[b], (blk / NB) & 1u, lim)) {
@@ -1024,6 +1255,35 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           }
           tc_fence_after();
           if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
+        }
+        if (p.cluster_reduce) {
+          // the accumulator is final, so every UMMA has completed and this
+          // CTA's operand ring is idle
+          cluster_signal_ready(p, red_ready, red_flags, ept);
+          const RowIn rin = cluster_row_inputs<SC, SWAP>(
+              p, w.row0 + static_cast<int>(cluster_ctarank()) * (128 / p.split_k) + ept % (128 / p.split_k));
+          if (!mbar_wait_cluster(red_ready, 0, lim)) {
+            record_status(p.status, ST_TIMEOUT_EPILOGUE);
+            ok = false;
+            break;
+          }
+          // this row's partial sums go to the CTA of the cluster owning it
+#pragma unroll 1
+          for (int c = 0; c < BN; c += CW) {
+            uint32_t r[CW];
+            tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
+            tmem_ld_wait();
+            cluster_send<BN, CW>(p, smem_u32(red_buf), red_full, w, lane_row, c, r);
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[b]);
+          ++blk;
+          if (!cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads>(p, red_buf, red_full, w, ept, rin)) {
+            record_status(p.status, ST_TIMEOUT_EPILOGUE);
+            ok = false;
+            break;
+          }
+          continue;
         }
         bool do_epi = true;
         if (w.contrib > 1) {
@@ -1078,6 +1338,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
   // ------------------------------------------------------------ teardown ---
   tc_fence_before();
   __syncthreads();
+  // no CTA of a cluster leaves while another may still write its buffer
+  if (p.cluster_reduce) cluster_sync_all();
   if (threadIdx.x == 0) trace_point(p, TR_END);
   if (warp == 1) {
     tc_fence_after();

@@ -7,7 +7,8 @@ namespace eg {
 struct KernelEntry {
   const void* fn = nullptr;      // __global__ function
   uint32_t stage_bytes = 0;      // shared memory per ring stage
-  uint32_t fixed_bytes = 0;      // alignment slack + barriers
+  uint32_t fixed_bytes = 0;      // alignment slack + barriers + op_bytes
+  uint32_t op_bytes = 0;         // INT8 fp16 operand slots (follow the ring)
   int threads = 0;
   int elems_per_stage = 0;       // K elements one stage covers
   int tmem_cols = 0;             // TMEM columns one CTA allocates
@@ -35,6 +36,7 @@ EG_DECLARE_LOOKUP(lookup_int8_tc)
     out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN>); \
     out->stage_bytes = C_::kStageBytes;                                                \
     out->fixed_bytes = 1024u + 512u + C_::kOpBytes;                                    \
+    out->op_bytes = C_::kOpBytes;                                                      \
     out->threads = C_::kThreads;                                                       \
     out->elems_per_stage = C_::kElemsPerStage;                                         \
     out->tmem_cols = static_cast<int>(C_::kTmemCols);                                  \

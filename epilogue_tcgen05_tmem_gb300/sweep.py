@@ -52,10 +52,16 @@ def candidates(p, swaps=(0, 1)):
                 for s in SPLITS:
                     if s > k_tiles or (s > 1 and k_tiles // s < 2):
                         continue
-                    yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0)
+                    yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0,
+                               cluster_reduce=0)
+                    # the same split reduced inside a cluster (2, 4 or 8 CTAs)
+                    if s in (2, 4, 8):
+                        yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0,
+                                   cluster_reduce=1)
                 # balanced split-K with 1 or 2 CTAs per SM
                 for sk in (1, 2):
-                    yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=swap, stream_k=sk)
+                    yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=swap, stream_k=sk,
+                               cluster_reduce=0)
 
 
 def time_config(eg, torch, p, d, Ws, tuning, reps=3, calls=None):
@@ -100,8 +106,8 @@ def time_config(eg, torch, p, d, Ws, tuning, reps=3, calls=None):
 def pick(results):
     best = min(t for _, t in results)
     near = [(c, t) for c, t in results if t <= best * 1.01]
-    near.sort(key=lambda ct: (ct[0]["stream_k"], ct[0]["split_k"], ct[0]["swap_ab"],
-                              ct[0]["stages"], ct[1]))
+    near.sort(key=lambda ct: (ct[0]["stream_k"], ct[0]["cluster_reduce"], ct[0]["split_k"],
+                              ct[0]["swap_ab"], ct[0]["stages"], ct[1]))
     return near[0]
 
 
@@ -138,7 +144,7 @@ def sweep(workload, tokens, swaps=(0, 1), verbose=True):
         c, t = pick(results)
         bucket = M if M <= 32 else 0
         row = (eg.DTYPES[p.dtype], eg.SCALES[p.scale], p.N, p.K, bucket, c["tile_n"],
-               c["stages"], c["split_k"], c["swap_ab"], c["stream_k"])
+               c["stages"], c["split_k"], c["swap_ab"], c["stream_k"], c["cluster_reduce"])
         rows.append(row)
         if verbose:
             top = sorted(results, key=lambda ct: ct[1])[:6]
@@ -159,7 +165,7 @@ def format_rows(rows, comment=""):
     if comment:
         out.append(f"// {comment}")
     for r in rows:
-        out.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % r)
+        out.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % r)
     return "\n".join(out) + "\n"
 
 

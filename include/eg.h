@@ -145,6 +145,15 @@ typedef struct {
                        tiles x K-tiles iteration space in equal contiguous
                        ranges (split_k must be 1); a tile's partial sums
                        reduce through the same workspace, in CTA order */
+  int32_t cluster_reduce; /* 0: split-K partial sums go through the plan's
+                       global workspace and the last CTA of a tile to
+                       arrive reduces them.  1: the split_k CTAs of a tile
+                       (split_k in {2, 4, 8}, stream_k 0) run as one thread-
+                       block cluster and exchange their partial sums through
+                       distributed shared memory; each CTA reduces 128 /
+                       split_k of the tile's rows (in split order, so the
+                       result is the same) and runs their epilogue.  No
+                       workspace or arrival counters are used. */
 } eg_tuning;
 
 typedef struct {

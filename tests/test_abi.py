@@ -82,3 +82,57 @@ def test_valid_problem_without_device_reports_cuda_error(L):
 def test_plan_class_raises_loudly(L):
     with pytest.raises(eg.EgError):
         eg.Plan(-1, 8, 64)
+
+
+def _c_struct_fields(name):
+    """Field names of a typedef struct in include/eg.h, in order."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "eg.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\}\s*" + name + ";", src).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            fields += [f.strip().lstrip("*") for f in decl.split(None, 1)[1].split(",")]
+    return fields
+
+
+@pytest.mark.parametrize("name,cls", [("eg_tuning", eg.eg_tuning), ("eg_problem", eg.eg_problem)])
+def test_binding_structs_match_header(name, cls):
+    assert [f for f, _ in cls._fields_] == _c_struct_fields(name)
+
+
+def test_tuning_table_rows_are_valid():
+    """Every swept row has the 11 fields of the table, and uses the cluster
+    reduction only with a split of 2, 4 or 8 and without balanced split-K."""
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "epilogue_tcgen05_tmem_gb300", "csrc", "eg_tuning_table.inc")
+    rows = [tuple(int(x) for x in m.split(","))
+            for m in re.findall(r"^\s*\{([-\d, ]+)\},", open(path).read(), flags=re.M)]
+    assert rows
+    for r in rows:
+        assert len(r) == 11, r
+        dtype, scale, N, K, bucket, tn, stages, split, swap, sk, cl = r
+        assert bucket in (0, 1, 2, 4, 8, 16, 24, 32) and tn in (16, 32, 64, 128, 256)
+        assert 2 <= stages <= 8 and swap in (0, 1) and cl in (0, 1)
+        if cl:
+            assert split in (2, 4, 8) and sk == 0, r
+        if sk:
+            assert split == 1, r
+
+
+def test_sweep_candidates_and_rows():
+    from epilogue_tcgen05_tmem_gb300 import inputs, sweep
+    p = inputs.make_problem(16, 1024, 4096, "e4m3", "token_channel", seed=0)
+    cands = list(sweep.candidates(p, swaps=(1,)))
+    assert all(set(c) == {"tile_n", "stages", "split_k", "swap_ab", "stream_k", "cluster_reduce"}
+               for c in cands)
+    cl = [c for c in cands if c["cluster_reduce"]]
+    assert cl and all(c["split_k"] in (2, 4, 8) and c["stream_k"] == 0 for c in cl)
+    text = sweep.format_rows([(1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1)])
+    assert text.strip() == "{1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1},"

@@ -364,3 +364,90 @@ def test_plans_sharing_a_kernel_with_other_ring_depths():
         assert_close_rms(bits(y), ref)
     deep.close()
     shallow.close()
+
+
+# ------------------------------------------ split-K inside a cluster ----
+
+CLUSTER_CASES = [
+    # dtype, scale, M, N, K, tile_n, swap, split
+    ("e4m3", "token_channel", 1, 1536, 2048, 16, 1, 4),
+    ("e4m3", "token_channel", 5, 1000, 1024, 16, 1, 2),     # ragged N: partial last row tile
+    ("e4m3", "token_channel", 16, 2048, 4096, 16, 1, 8),
+    ("e4m3", "token_channel", 27, 1536, 2048, 32, 1, 4),    # ragged columns inside the tile
+    ("e4m3", "token_channel", 40, 1024, 2048, 32, 1, 4),    # two column tiles, the last ragged
+    ("bf16", "none", 200, 136, 512, 32, 0, 2),              # rows over M, ragged both ways
+    ("e4m3", "block", 8, 1024, 1024, 16, 1, 4),
+    ("e4m3", "block", 130, 384, 1024, 64, 0, 2),            # 8 epilogue warps
+]
+
+
+@pytest.mark.parametrize("dtype,scale,M,N,K,tn,swap,S", CLUSTER_CASES)
+def test_cluster_split_k_matches_workspace_path(dtype, scale, M, N, K, tn, swap, S):
+    """Partial sums exchanged through distributed shared memory give the
+    same bits as the workspace path with the same split, and meet the bound
+    against the oracle."""
+    p = inputs.make_problem(M, N, K, dtype, scale, act="silu", bias=True, residual=True, seed=31)
+    base = dict(tile_n=tn, stages=4, split_k=S, swap_ab=swap)
+    pc = make_plan(p, dict(base, cluster_reduce=1))
+    li = pc.launch_info
+    assert pc.workspace_bytes == 0
+    assert li["grid"] == li["units"]
+    assert li["grid"] % S == 0
+    yc, _ = run(p, plan=pc)
+    yc2, _ = run(p, plan=pc)
+    pc.close()
+    yw, _ = run(p, dict(base, cluster_reduce=0))
+    assert torch.equal(yc.view(torch.int16), yc2.view(torch.int16)), "not deterministic"
+    assert torch.equal(yc.view(torch.int16), yw.view(torch.int16)), "differs from the workspace path"
+    assert_close_rms(bits(yc), oracle.linear(p))
+
+
+@pytest.mark.parametrize("M,S", [(1, 4), (16, 8), (29, 2)])
+def test_cluster_split_k_int8_exact(M, S):
+    p = inputs.make_problem(M, 1000, 4096, "int8", "token_channel", residual=True, seed=33)
+    t = dict(tile_n=16 if M <= 16 else 32, stages=4, split_k=S, swap_ab=1, cluster_reduce=1)
+    yacc, _ = run(p, t, debug=True)
+    _, _, acc64 = oracle.linear(p, want_acc=True)
+    assert np.array_equal(yacc.numpy().astype(np.int64), acc64), "int32 accumulator not exact"
+    y, _ = run(p, t)
+    assert ulp_dist(bits(y), oracle.linear(p)).max() <= 1
+
+
+def test_cluster_split_k_debug_float_accumulators():
+    p = inputs.make_problem(12, 640, 2048, "e4m3", "token_channel", seed=35)
+    t = dict(tile_n=16, stages=4, split_k=4, swap_ab=1)
+    ya, _ = run(p, dict(t, cluster_reduce=1), debug=True)
+    yb, _ = run(p, dict(t, cluster_reduce=0), debug=True)
+    assert torch.equal(ya.view(torch.int32), yb.view(torch.int32))
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    err = np.abs(ya.numpy().astype(np.float64) - acc)
+    assert err.max() <= 1e-4 * np.sqrt(np.mean(acc * acc))
+
+
+def test_cluster_split_k_full_size_decode():
+    """The decode linear (K=4096, N=12288) with the cluster reduction, sampled
+    outputs against the oracle, through graph replay with PDL."""
+    for M in (1, 16, 32):
+        p = inputs.workload("fp8_dynamic", M)
+        plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=True, graph=True, pdl=True,
+                       tuning=dict(tile_n=16 if M <= 16 else 32, stages=4, split_k=4, swap_ab=1,
+                                   cluster_reduce=1))
+        d = to_device(p)
+        for _ in range(3):
+            y, _ = run(p, plan=plan, d=d)
+        plan.close()
+        _sampled(p, y)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(split_k=3), eg.EG_ERR_UNSUPPORTED),
+    (dict(split_k=16), eg.EG_ERR_UNSUPPORTED),
+    (dict(split_k=1, stream_k=1), eg.EG_ERR_UNSUPPORTED),
+    (dict(stream_k=1), eg.EG_ERR_INVALID_ARG),
+    (dict(tile_n=256, stages=2, split_k=2), eg.EG_ERR_UNSUPPORTED),   # buffer > operand ring
+])
+def test_cluster_split_k_rejected_tunings(bad, status):
+    t = dict(dict(tile_n=16, stages=4, split_k=4, swap_ab=1, cluster_reduce=1), **bad)
+    with pytest.raises(eg.EgError) as ei:
+        eg.Plan(4, 1024, 4096, "e4m3", "token_channel", "silu", bias=True, tuning=t)
+    assert ei.value.status == status
