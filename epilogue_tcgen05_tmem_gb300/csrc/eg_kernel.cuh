@@ -181,6 +181,49 @@ __device__ __forceinline__ float act_apply(int act, float v) {
   }
 }
 
+// The activation as a compile-time choice.  The epilogue code is
+// instantiated per activation and selected once per chunk (EG_ACT_DISPATCH):
+// a runtime switch inside the per-element code would be repeated for every
+// unrolled element, spreading the path actually taken over a large stretch
+// of code that the instruction cache cannot hold.
+template <int ACT>
+__device__ __forceinline__ float act_c(float v) {
+  if constexpr (ACT == ACT_RELU) return fmaxf(v, 0.0f);
+  if constexpr (ACT == ACT_GELU_ERF) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+  if constexpr (ACT == ACT_GELU_TANH) {
+    const float u = 0.7978845608028654f * (v + 0.044715f * v * v * v);
+    return 0.5f * v * (1.0f + tanh_fast(u));
+  }
+  if constexpr (ACT == ACT_SILU) return __fdividef(v, 1.0f + __expf(-v));
+  return v;
+}
+
+// Runs CALL (an expression that names the activation as A_) with A_ bound to
+// the compile-time value of `act`.
+#define EG_ACT_DISPATCH(act, CALL)                                   \
+  switch (act) {                                                     \
+    case ACT_RELU: {                                                 \
+      constexpr int A_ = ACT_RELU;                                   \
+      CALL;                                                          \
+    } break;                                                         \
+    case ACT_GELU_ERF: {                                             \
+      constexpr int A_ = ACT_GELU_ERF;                               \
+      CALL;                                                          \
+    } break;                                                         \
+    case ACT_GELU_TANH: {                                            \
+      constexpr int A_ = ACT_GELU_TANH;                              \
+      CALL;                                                          \
+    } break;                                                         \
+    case ACT_SILU: {                                                 \
+      constexpr int A_ = ACT_SILU;                                   \
+      CALL;                                                          \
+    } break;                                                         \
+    default: {                                                       \
+      constexpr int A_ = ACT_NONE;                                   \
+      CALL;                                                          \
+    } break;                                                         \
+  }
+
 // Float pair (hi + lo) arithmetic for the INT8 epilogue, so that
 // acc * s_a * s_w + R is formed to ~2^-44 relative before the single bf16
 // rounding (the oracle forms it in float64).
@@ -239,30 +282,32 @@ __device__ __forceinline__ float bf16_to_f(uint16_t b) {
 
 // One output element of the epilogue (float path).  `bias` and `r` are the
 // bf16 inputs already widened; unused ones are ignored by the flags.
-__device__ __forceinline__ float epi_value(float v, float scale, float bias, float r, int act,
+template <int ACT>
+__device__ __forceinline__ float epi_value(float v, float scale, float bias, float r,
                                            uint32_t flags) {
   v = v * scale;
   if (flags & F_BIAS) v += bias;
   if (flags & F_RES_PRE) {
     v += r;
-    v = act_apply(act, v);
+    v = act_c<ACT>(v);
   } else {
-    v = act_apply(act, v);
+    v = act_c<ACT>(v);
     if (flags & F_RES) v += r;
   }
   return v;
 }
 
 // INT8 epilogue element: exact int32 accumulator -> bf16 bits.
+template <int ACT>
 __device__ __forceinline__ uint16_t epi_int8(int32_t acc, float sa, float sw, float bias, float r,
-                                             int act, uint32_t flags) {
+                                             uint32_t flags) {
   DF v = df_scale_int(acc, sa, sw);
   if (flags & F_BIAS) v = df_add(v, bias);
   if (flags & F_RES_PRE) {
     v = df_add(v, r);
-    if (act != ACT_NONE) v = DF{act_apply(act, __fadd_rn(v.hi, v.lo)), 0.0f};
+    if (ACT != ACT_NONE) v = DF{act_c<ACT>(__fadd_rn(v.hi, v.lo)), 0.0f};
   } else {
-    if (act != ACT_NONE) v = DF{act_apply(act, __fadd_rn(v.hi, v.lo)), 0.0f};
+    if (ACT != ACT_NONE) v = DF{act_c<ACT>(__fadd_rn(v.hi, v.lo)), 0.0f};
     if (flags & F_RES) v = df_add(v, r);
   }
   return bf16_bits_from_df(v);
@@ -294,7 +339,7 @@ __device__ __forceinline__ void load_swap_inputs(const KParams& p, int n, int co
 
 // Swap-AB epilogue compute and store: lanes of a warp hold consecutive n, so
 // each token's residual loads and Y stores are coalesced across the warp.
-template <int IN, int SC, int CW>
+template <int IN, int SC, int CW, int ACT>
 __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
                                            const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
   if (n >= p.N) return;
@@ -317,11 +362,11 @@ __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
       if (m < p.M) {
         uint16_t o;
         if (IN == IN_INT8)
-          o = epi_int8(static_cast<int32_t>(vals[g + j]), sa[j], in.sw, in.b, r[j], p.act, p.flags);
+          o = epi_int8<ACT>(static_cast<int32_t>(vals[g + j]), sa[j], in.sw, in.b, r[j], p.flags);
         else
           o = __bfloat16_as_ushort(__float2bfloat16_rn(
-              epi_value(__uint_as_float(vals[g + j]), (SC == SC_TC) ? sa[j] * in.sw : 1.0f, in.b,
-                        r[j], p.act, p.flags)));
+              epi_value<ACT>(__uint_as_float(vals[g + j]), (SC == SC_TC) ? sa[j] * in.sw : 1.0f,
+                             in.b, r[j], p.flags)));
         Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
       }
     }
@@ -331,9 +376,9 @@ __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
 // Apply the epilogue to CW consecutive accumulator columns of one TMEM lane
 // (= one UMMA row) and store them.  `vals` holds fp32 bits, or int32 for
 // INT8.  row = tile row index + lane row; c0 = first column of the chunk.
-template <int IN, int SC, bool SWAP, int CW>
-__device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int col0,
-                                               const uint32_t (&vals)[CW]) {
+template <int IN, int SC, bool SWAP, int CW, int ACT>
+__device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int col0,
+                                                 const uint32_t (&vals)[CW]) {
   const bool debug = (p.flags & F_DEBUG) != 0;
   const bool has_bias = (p.flags & F_BIAS) != 0;
   const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
@@ -376,12 +421,11 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
             const float b = bf16_to_f(static_cast<uint16_t>(bw[h] >> (16 * e)));
             const float r = bf16_to_f(static_cast<uint16_t>(rw[h] >> (16 * e)));
             if (IN == IN_INT8) {
-              o[e] = epi_int8(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.act,
-                              p.flags);
+              o[e] = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.flags);
             } else {
               const float s = (SC == SC_TC) ? sa * sws[h * 2 + e] : 1.0f;
               o[e] = __bfloat16_as_ushort(__float2bfloat16_rn(
-                  epi_value(__uint_as_float(vals[j]), s, b, r, p.act, p.flags)));
+                  epi_value<ACT>(__uint_as_float(vals[j]), s, b, r, p.flags)));
             }
           }
           out[g * 4 + h] = static_cast<uint32_t>(o[0]) | (static_cast<uint32_t>(o[1]) << 16);
@@ -401,11 +445,11 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
         const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
         uint16_t o;
         if (IN == IN_INT8)
-          o = epi_int8(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.act, p.flags);
+          o = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.flags);
         else
           o = __bfloat16_as_ushort(__float2bfloat16_rn(
-              epi_value(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r, p.act,
-                        p.flags)));
+              epi_value<ACT>(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r,
+                             p.flags)));
         yrow[n] = __ushort_as_bfloat16(o);
       }
     }
@@ -425,8 +469,14 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
     }
     SwapIn<CW> in;
     load_swap_inputs<SC, CW>(p, n, col0, in);
-    store_swap<IN, SC, CW>(p, n, col0, vals, in);
+    store_swap<IN, SC, CW, ACT>(p, n, col0, vals, in);
   }
+}
+
+template <int IN, int SC, bool SWAP, int CW>
+__device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int col0,
+                                               const uint32_t (&vals)[CW]) {
+  EG_ACT_DISPATCH(p.act, (epilogue_chunk_a<IN, SC, SWAP, CW, A_>(p, row, col0, vals)))
 }
 
 template <int CW>
@@ -652,23 +702,40 @@ __device__ __forceinline__ void reduce_partials(const KParams& p, int tile, int 
   }
 }
 
+// Row stride (floats) of a unit's staged block scales: nk rounded up to a
+// multiple of 4, plus 4 (16-byte aligned rows for vector copies).
+__host__ __device__ constexpr int scale_row_stride(int nk) { return (nk + 3) / 4 * 4 + 4; }
+
 // Block scales of one unit into a shared-memory buffer, with asynchronous
 // copies (the caller commits and waits): sc_a[t][i] = s_a of tile row (or,
-// with swap-AB, column) t at K block kt0 + i, row stride nk + 1 (no bank
-// conflicts), zero beyond M; then sc_w[i] of the tile's weight block row.
+// with swap-AB, column) t at K block kt0 + i, row stride
+// scale_row_stride(nk), zero beyond M; then sc_w[i] of the tile's weight
+// block row.  16-byte copies when the rows' pieces are 16-byte aligned.
 template <bool SWAP, int BN, int NT>
 __device__ __forceinline__ void stage_block_scales(const KParams& p, const Unit& w, float* buf,
                                                    int ept) {
   const int T = SWAP ? BN : 128;
   const int base = SWAP ? w.col0 : w.row0;
+  const int ss = scale_row_stride(w.nk);
   float* sc_a = buf;
-  float* sc_w = buf + T * (w.nk + 1);
-  for (int idx = ept; idx < T * w.nk; idx += NT) {
-    const int t = idx / w.nk, i = idx - t * w.nk;
-    const int m = base + t;
-    const bool ok = m < p.M;
-    const float* src = p.s_a + (ok ? static_cast<int64_t>(m) * p.kb_count + w.kt0 + i : 0);
-    cp_async_4(sc_a + t * (w.nk + 1) + i, src, ok ? 4u : 0u);
+  float* sc_w = buf + T * ss;
+  if ((p.kb_count & 3) == 0 && (w.kt0 & 3) == 0 && (w.nk & 3) == 0) {
+    const int q = w.nk >> 2;
+    for (int idx = ept; idx < T * q; idx += NT) {
+      const int t = idx / q, c = idx - t * q;
+      const int m = base + t;
+      const bool ok = m < p.M;
+      const float* src = p.s_a + (ok ? static_cast<int64_t>(m) * p.kb_count + w.kt0 + 4 * c : 0);
+      cp_async_16(sc_a + t * ss + 4 * c, src, ok ? 16u : 0u);
+    }
+  } else {
+    for (int idx = ept; idx < T * w.nk; idx += NT) {
+      const int t = idx / w.nk, i = idx - t * w.nk;
+      const int m = base + t;
+      const bool ok = m < p.M;
+      const float* src = p.s_a + (ok ? static_cast<int64_t>(m) * p.kb_count + w.kt0 + i : 0);
+      cp_async_4(sc_a + t * ss + i, src, ok ? 4u : 0u);
+    }
   }
   const int wrow = SWAP ? w.tile_r : (w.col0 / 128);
   for (int i = ept; i < w.nk; i += NT)
@@ -758,7 +825,7 @@ __device__ __forceinline__ RowIn cluster_row_inputs(const KParams& p, int row) {
 // 4-column groups e / R, + T / R, ... (T = epilogue threads, a multiple of
 // R): the group's global loads and S 16-byte partial reads first, then its
 // arithmetic and stores.  False on timeout.
-template <int IN, int SC, bool SWAP, int BN, int T>
+template <int IN, int SC, bool SWAP, int BN, int T, int ACT>
 __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uint32_t* red,
                                                      uint64_t* red_full, const Unit& w, int ept,
                                                      const RowIn& in) {
@@ -816,10 +883,10 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
       const float bias = SWAP ? in.b : cb[g];
       uint16_t o;
       if (IN == IN_INT8)
-        o = epi_int8(static_cast<int32_t>(acc[g]), sa, sw, bias, rv[g], p.act, p.flags);
+        o = epi_int8<ACT>(static_cast<int32_t>(acc[g]), sa, sw, bias, rv[g], p.flags);
       else
-        o = __bfloat16_as_ushort(__float2bfloat16_rn(epi_value(
-            __uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f, bias, rv[g], p.act, p.flags)));
+        o = __bfloat16_as_ushort(__float2bfloat16_rn(epi_value<ACT>(
+            __uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f, bias, rv[g], p.flags)));
       reinterpret_cast<__nv_bfloat16*>(p.Y)[at] = __ushort_as_bfloat16(o);
     }
   }
@@ -1099,7 +1166,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
     // per CTA) each unit stages its own, all copies in flight at once.
     constexpr int kScaleRows = SWAP ? BN : 128;
     constexpr bool kAhead = (SC == SC_BLOCK) && !SWAP;
-    const int scale_buf_floats = (kScaleRows + 1) * (p.k_tiles + 1);
+    const int scale_buf_floats = (kScaleRows + 1) * scale_row_stride(p.k_tiles);
     WorkIter it_pf = it;
     uint32_t su = 0;
     if constexpr (kAhead) {
@@ -1119,7 +1186,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
         // this unit's block scales (staged one unit ahead; layout in
         // stage_block_scales)
         float* sc_a = scale_smem + (kAhead ? (cur & 1u) * scale_buf_floats : 0);
-        float* sc_w = sc_a + kScaleRows * (w.nk + 1);
+        const int ss = scale_row_stride(w.nk);
+        float* sc_w = sc_a + kScaleRows * ss;
         if constexpr (kAhead) {
           // every thread is done with the other buffer (the previous unit's)
           epi_bar_sync(C::kEpiThreads);
@@ -1142,7 +1210,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           const uint32_t bph = (blk / NB) & 1u;
           float srow = 1.0f;  // scale shared by the thread's row (block scaling)
           if constexpr (SC == SC_BLOCK) {
-            srow = SWAP ? sc_w[i] : sc_a[lane_row * (w.nk + 1) + i] * sc_w[i];
+            srow = SWAP ? sc_w[i] : sc_a[lane_row * ss + i] * sc_w[i];
           }
           if (!mbar_wait(&tfull[b], bph, lim)) {
             record_status(p.status, ST_TIMEOUT_EPILOGUE);
@@ -1163,7 +1231,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           for (int c = 0; c < CPT; ++c) {
             if constexpr (SC == SC_BLOCK) {
               float s = srow;
-              if (SWAP) s = srow * sc_a[(cbeg + c) * (w.nk + 1) + i];  // 0 beyond M
+              if (SWAP) s = srow * sc_a[(cbeg + c) * ss + i];  // 0 beyond M
               acc[c] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[c]), __uint_as_float(acc[c])));
             } else {
               acc[c] = static_cast<uint32_t>(static_cast<int32_t>(acc[c]) +
@@ -1186,7 +1254,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
 #pragma unroll
           for (int c = 0; c < CPT; c += CW)
             cluster_send<BN, CW>(p, smem_u32(red_buf), red_full, w, lane_row, cbeg + c, acc + c);
-          if (!cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads>(p, red_buf, red_full, w, ept, rin)) {
+          bool red_ok = false;
+          EG_ACT_DISPATCH(p.act, (red_ok = cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads, A_>(
+                                      p, red_buf, red_full, w, ept, rin)))
+          if (!red_ok) {
             record_status(p.status, ST_TIMEOUT_EPILOGUE);
             ok = false;
             break;
@@ -1278,7 +1349,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           tc_fence_before();
           mbar_arrive(&tempty[b]);
           ++blk;
-          if (!cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads>(p, red_buf, red_full, w, ept, rin)) {
+          bool red_ok = false;
+          EG_ACT_DISPATCH(p.act, (red_ok = cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads, A_>(
+                                      p, red_buf, red_full, w, ept, rin)))
+          if (!red_ok) {
             record_status(p.status, ST_TIMEOUT_EPILOGUE);
             ok = false;
             break;
@@ -1319,7 +1393,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
             }
             if constexpr (kPre) {
               if (!(p.flags & F_DEBUG)) {
-                store_swap<IN, SC, CW>(p, row, w.col0, r, pre);
+                EG_ACT_DISPATCH(p.act, (store_swap<IN, SC, CW, A_>(p, row, w.col0, r, pre)))
                 continue;
               }
             }

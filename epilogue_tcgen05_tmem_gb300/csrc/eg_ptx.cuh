@@ -134,6 +134,14 @@ __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc, uin
                : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both addresses 16-byte
+// aligned); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
