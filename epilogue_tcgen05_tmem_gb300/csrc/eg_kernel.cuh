@@ -23,8 +23,9 @@
 //               bf16 rounding and the single store; split-K partials go
 //               through an fp32 workspace, the last CTA of a tile to arrive
 //               reduces them in split order and runs the epilogue.
-//   warps 6..9  (INT8 only) prologue transform: int8 tiles -> fp16 tiles
-//               (exact) in the UMMA layout.
+//   warps 6..9  (INT8 only) prologue transform, exact: the int8 P tile ->
+//               fp16 in tensor memory (the UMMA reads its A operand there),
+//               the int8 Q tile -> fp16 in shared memory (UMMA layout).
 // Rows of the UMMA are M (P = A, Q = W) or, with swap-AB, N (P = W, Q = A),
 // so TMEM lane = row and column = the other dimension.
 //
@@ -103,12 +104,14 @@ struct Cfg {
   static constexpr uint32_t kQBytes = uint32_t(BN) * 128u * kAtoms;
   static constexpr uint32_t kP8Bytes = kConvert ? 128u * 128u : 0u;  // int8 staging
   static constexpr uint32_t kQ8Bytes = kConvert ? uint32_t(BN) * 128u : 0u;
-  // TMA ring stage: the UMMA operands, or (INT8) the int8 staging tiles; the
-  // converted fp16 operands then live in their own 2-slot ring, so the int8
-  // ring can be deep (bytes in flight) while the fp16 ring stays small.
+  // TMA ring stage: the UMMA operands, or (INT8) the int8 staging tiles.
+  // INT8 converts P (128 rows) into fp16 in tensor memory (the UMMA's A
+  // operand, two buffers of 64 columns) and Q into fp16 in a 2-slot shared
+  // ring, so the int8 ring can be deep while the fp16 operands stay small
+  // and shared memory carries the conversion's traffic for Q only.
   static constexpr uint32_t kStageBytes = kConvert ? kP8Bytes + kQ8Bytes : kPBytes + kQBytes;
   static constexpr int kOpSlots = 2;
-  static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * (kPBytes + kQBytes) : 0u;
+  static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * kQBytes : 0u;
   static constexpr uint32_t kTxBytes = (128u + BN) * 128u;  // bytes one stage's TMA delivers
   // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for block-scale
   // promotion of wide tiles (two column halves per quarter, so each thread
@@ -137,12 +140,17 @@ struct Cfg {
   // TMEM accumulator buffers: 2 (one unit drains while the next fills), or
   // 4 when promoting K blocks so UMMA runs further ahead of the epilogue
   static constexpr int kAccBufs = (kPromote && 4 * BN <= 512) ? 4 : 2;
-  static constexpr uint32_t kTmemCols = kAccBufs * BN <= 32 ? 32 : kAccBufs * BN;
+  static constexpr uint32_t kAccCols = kAccBufs * BN;
+  static constexpr uint32_t kTmemACols = kConvert ? kOpSlots * 64u : 0u;  // fp16 P, 128 K each
+  static constexpr uint32_t kTmemUsed = kAccCols + kTmemACols;
+  static constexpr uint32_t kTmemCols =
+      kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
   static constexpr uint32_t kIdesc =
       (IN == IN_BF16) ? idesc_f32acc(1, 1, 128, BN)
                       : idesc_f32acc(0, 0, 128, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(!kPromote || BN <= 128, "promotion keeps BN fp32 values per thread");
+  static_assert(kTmemUsed <= 512, "tensor memory holds 512 columns");
 };
 
 template <int IN, int SC, bool SWAP, int BN>
@@ -555,11 +563,37 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
   }
 }
 
-template <int BN, class C>
-__device__ __forceinline__ void convert_stage(const uint8_t* src8, uint8_t* dst16, int ct) {
-  static_assert(BN % 16 == 0, "Q tile rows come in groups of 16");
-  convert_tile<8>(src8, dst16, 128, ct);                                  // P: 128 rows
-  convert_tile<BN / 16>(src8 + C::kP8Bytes, dst16 + C::kPBytes, BN, ct);  // Q: BN rows
+// INT8 prologue transform of P, one row per thread: row r (TMEM lane r) of
+// the int8 staging tile (128 codes, 128-byte swizzled) becomes 64 columns of
+// fp16 pairs in tensor memory at t_row (the warp's lane quarter and the
+// buffer's first column), in K order, with two 32-column stores.
+__device__ __forceinline__ void convert_row_to_tmem(const uint8_t* src, uint32_t t_row, int r) {
+  const int sw = r & 7;
+  const uint8_t* row = src + r * 128;
+  const __half2 bias2 = __floats2half2_rn(1152.0f, 1152.0f);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t h[32];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = half * 4 + jj;  // 16-byte chunk: codes 16 j .. 16 j + 15
+      const uint4 v = *reinterpret_cast<const uint4*>(row + ((j ^ sw) << 4));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t x = w4[t] ^ 0x80808080u;  // byte b -> b + 128 (unsigned)
+        uint32_t lo, hi;
+        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+        // fp16 0x64XX = 1024 + XX; subtracting 1152 = 1024 + 128 gives b exactly
+        __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), bias2);
+        __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), bias2);
+        h[jj * 8 + 2 * t] = *reinterpret_cast<uint32_t*>(&l2);
+        h[jj * 8 + 2 * t + 1] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+    }
+    tmem_st32(t_row + static_cast<uint32_t>(half * 32), h);
+  }
 }
 
 // One work unit = one 128 x BN output tile and one K split.
@@ -918,7 +952,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
   // UMMA operands of ring iteration g: the ring stage itself, or (INT8) the
   // fp16 slot the transform warps wrote
   auto op_base = [&](uint32_t g) {
-    return C::kConvert ? op_area + (g % C::kOpSlots) * (C::kPBytes + C::kQBytes)
+    return C::kConvert ? op_area + (g % C::kOpSlots) * C::kQBytes
                        : stage_base(static_cast<int>(g % S));
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(op_area + C::kOpBytes);
@@ -1090,18 +1124,24 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
           const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
           const uint32_t pa = smem_u32(op_base(g));
-          const uint32_t qa = pa + C::kPBytes;
+          const uint32_t qa = C::kConvert ? pa : pa + C::kPBytes;
+          // INT8: P is in tensor memory, buffer os, 8 columns per K step of 16
+          const uint32_t pt = tmem_base + C::kAccCols + static_cast<uint32_t>(os) * 64u;
 #pragma unroll
           for (int a = 0; a < C::kAtoms; ++a) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = sdesc_k_sw128(pa + static_cast<uint32_t>(a) * 128u * 128u + 32u * k);
               const uint64_t bd = sdesc_k_sw128(qa + static_cast<uint32_t>(a) * BN * 128u + 32u * k);
               const uint32_t accum = C::kPromote ? ((a | k) != 0) : ((i | a | k) != 0);
-              if (IN == IN_E4M3)
-                umma_f8(d, ad, bd, C::kIdesc, accum);
-              else
-                umma_f16(d, ad, bd, C::kIdesc, accum);
+              if constexpr (C::kConvert) {
+                umma_f16_ts(d, pt + static_cast<uint32_t>(a * 4 + k) * 8u, bd, C::kIdesc, accum);
+              } else {
+                const uint64_t ad = sdesc_k_sw128(pa + static_cast<uint32_t>(a) * 128u * 128u + 32u * k);
+                if (IN == IN_E4M3)
+                  umma_f8(d, ad, bd, C::kIdesc, accum);
+                else
+                  umma_f16(d, ad, bd, C::kIdesc, accum);
+              }
             }
           }
           umma_commit(C::kConvert ? &bempty[os] : &empty[s]);
@@ -1122,6 +1162,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
     // ---------------------------------- INT8 -> fp16 prologue transform ----
     if constexpr (C::kConvert) {
       const int ct = threadIdx.x - 192;  // 0..127
+      // the row this thread converts into tensor memory: its warp's lane
+      // quarter (warp % 4) and its lane
+      const int conv_row = (warp & 3) * 32 + lane;
+      const uint32_t t_conv = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kAccCols;
       uint32_t g = 0;
       bool ok = true;
       WorkIter it = work_begin(p);
@@ -1137,7 +1181,13 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
             ok = false;
             break;
           }
-          convert_stage<BN, C>(stage_base(s), op_base(g), ct);
+          tc_fence_after();  // the UMMAs that read buffer os have completed
+          // P row -> tensor memory (buffer os); Q -> fp16 shared slot os
+          convert_row_to_tmem(stage_base(s), t_conv + static_cast<uint32_t>(os) * 64u, conv_row);
+          static_assert(BN % 16 == 0, "Q tile rows come in groups of 16");
+          convert_tile<BN / 16>(stage_base(s) + C::kP8Bytes, op_base(g), BN, ct);
+          tmem_st_wait();
+          tc_fence_before();
           fence_proxy_async_smem();
           mbar_arrive(&empty[s]);
           mbar_arrive(&bfull[os]);
