@@ -76,6 +76,11 @@ def lib():
             L.orc_accum_splitk.argtypes = [P, vp, vp, vp, vp, ctypes.c_int64,
                                            ctypes.c_int64, vp, vp]
             L.orc_default_threads.argtypes = []
+            L.orc_quant_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int32, vp, ctypes.c_int64, vp]
+            L.orc_quant_rows.restype = ctypes.c_int
+            L.orc_e4m3_from_float.argtypes = [ctypes.c_float]
+            L.orc_e4m3_from_float.restype = ctypes.c_uint8
             for f in ("orc_linear", "orc_linear_naive", "orc_linear_points",
                       "orc_accum_splitk", "orc_default_threads"):
                 getattr(L, f).restype = ctypes.c_int
@@ -182,3 +187,21 @@ def act(name: str, v: float) -> float:
 
 def default_threads() -> int:
     return lib().orc_default_threads()
+
+
+def quant_rows(x_bits, dtype: str):
+    """Per-token dynamic quantisation of bf16 activations (bits [M, K]):
+    (codes uint8 [M, K] -- E4M3 codes or int8 two's complement -- and
+    float32 scales [M])."""
+    x = np.ascontiguousarray(x_bits, np.uint16)
+    M, K = x.shape
+    q = np.zeros((M, K), np.uint8)
+    sc = np.zeros(M, np.float32)
+    rc = lib().orc_quant_rows(_ptr(x), M, K, K, DTYPES[dtype], _ptr(q), K, _ptr(sc))
+    if rc:
+        raise ValueError("oracle rejected the quantisation")
+    return q, sc
+
+
+def e4m3_from_float(v: float) -> int:
+    return lib().orc_e4m3_from_float(v)

@@ -372,3 +372,64 @@ int orc_accum_splitk(const orc_problem* p, const void* A, const void* W,
   }
   return 0;
 }
+
+
+/* ---------------------------------------------------------------------- */
+/* Per-token dynamic quantisation.                                         */
+
+/* E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent field 0 holds
+ * the subnormals m * 2^-9; the all-ones pattern S.1111.111 is NaN, so the
+ * largest finite magnitude is 1.75 * 2^8 = 448.  The magnitude is rounded
+ * on the grid of its binade (the subnormal grid 2^-9 below 2^-6), ties to
+ * even; a result past 448 saturates. */
+uint8_t orc_e4m3_from_float(float v) {
+  const uint8_t sign = signbit(v) ? 0x80 : 0;
+  if (isnan(v)) return sign | 0x7F;
+  const double a = fabs((double)v);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1) */
+  int lead = e - 1;      /* a in [2^lead, 2^(lead+1)) */
+  if (lead < -6) lead = -6;                 /* subnormals share the 2^-9 grid */
+  const double quantum = ldexp(1.0, lead - 3);
+  const double n = nearbyint(a / quantum);  /* exact quotient; ties to even */
+  const double r = n * quantum;             /* the rounded magnitude */
+  if (r >= 448.0) return sign | 0x7E;       /* 448 or beyond: saturate */
+  if (r < 0x1p-6) return sign | (uint8_t)nearbyint(r / 0x1p-9);  /* subnormal (or 0) */
+  int er;
+  const double fr = frexp(r, &er);          /* r = fr * 2^er, fr in [0.5, 1) */
+  const int exp_field = er - 1 + 7;
+  const int mant = (int)((fr * 2.0 - 1.0) * 8.0);  /* exact: r is on the grid */
+  return sign | (uint8_t)((exp_field << 3) | mant);
+}
+
+int orc_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int32_t dtype,
+                   uint8_t* q, int64_t ldq, float* s) {
+  if (M < 0 || K < 0 || (M > 0 && (!s || (K > 0 && (!x || !q)))) || ldx < K || ldq < K) return -1;
+  if (dtype != ORC_IN_E4M3 && dtype != ORC_IN_INT8) return -1;
+  const float qmax = dtype == ORC_IN_E4M3 ? 448.0f : 127.0f;
+  for (int64_t m = 0; m < M; ++m) {
+    const uint16_t* row = x + m * ldx;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = fabsf((float)orc_bf16_to_double(row[k]));  /* exact */
+      if (v > amax) amax = v;
+    }
+    const float sm = amax > 0.0f ? amax / qmax : 1.0f;
+    s[m] = sm;
+    for (int64_t k = 0; k < K; ++k) {
+      const float t = (float)orc_bf16_to_double(row[k]) / sm;   /* float32 division */
+      uint8_t code;
+      if (dtype == ORC_IN_E4M3) {
+        code = orc_e4m3_from_float(t);
+      } else {
+        float r = nearbyintf(t);  /* ties to even */
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        code = (uint8_t)(int8_t)r;
+      }
+      q[m * ldq + k] = code;
+    }
+  }
+  return 0;
+}

@@ -100,6 +100,26 @@ int orc_accum_splitk(const orc_problem* p, const void* A, const void* W,
 /* Number of worker threads orc_linear uses for nthreads <= 0. */
 int orc_default_threads(void);
 
+/* Dynamic per-token quantisation of activations (the prologue transform
+ * that precedes the FP8_Dynamic and W8A8_INT8 layers; "Helion linear backend
+ * in vLLM", section "One kernel instead of three", scale formats, and
+ * "Helion + TorchInductor co-operation: operator fusion", section on
+ * prologue fusion).  For each row m of the bf16 matrix x [M][ldx]:
+ *   amax = max_k |x[m][k]|                           (float32, exact)
+ *   s[m] = amax / 448 (E4M3) or amax / 127 (INT8)    (float32 division)
+ *          and s[m] = 1 when amax = 0
+ *   E4M3: q = E4M3 code of (x / s[m]) rounded to nearest even, saturated
+ *         to +-448 (float32 division)
+ *   INT8: q = clamp(round-half-even(x / s[m]), -127, 127)
+ * q is written to q[M][ldq] (bytes).  dtype is ORC_IN_E4M3 or ORC_IN_INT8.
+ * Returns 0, or -1 for bad arguments. */
+int orc_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int32_t dtype,
+                   uint8_t* q, int64_t ldq, float* s);
+
+/* OCP FP8 E4M3 code of a float: round to nearest, ties to even, finite
+ * values saturate to +-448, NaN -> 0x7F (sign kept). */
+uint8_t orc_e4m3_from_float(float v);
+
 #ifdef __cplusplus
 }
 #endif

@@ -360,3 +360,97 @@ def test_oracle_rejects_bad_arguments():
     p = _small("e4m3", "block", 2, 130, 200)   # K % 128 != 0 for block scaling
     with pytest.raises(ValueError):
         oracle.linear(p)
+
+
+# --------------------------------------- per-token dynamic quantisation ---
+
+def _finite_e4m3_codes():
+    return [c for c in range(256) if (c & 0x7F) != 0x7F]
+
+
+def test_e4m3_encoder_inverts_the_table():
+    """Every finite code survives decode -> encode (the decoder is pinned to
+    the OCP table above)."""
+    for c in _finite_e4m3_codes():
+        v = oracle.e4m3_to_double(c)
+        assert oracle.e4m3_from_float(v) == c, hex(c)
+
+
+def test_e4m3_encoder_ties_to_even_and_saturates():
+    """Between consecutive finite magnitudes the midpoint goes to the code
+    with an even mantissa, anything off the midpoint to the nearer code;
+    magnitudes at or past 448 saturate; NaN stays NaN."""
+    mags = sorted({oracle.e4m3_to_double(c) for c in range(0x7F)})
+    for lo, hi in zip(mags, mags[1:]):
+        c_lo, c_hi = oracle.e4m3_from_float(lo), oracle.e4m3_from_float(hi)
+        mid = (lo + hi) / 2  # exact in float32 (a few significant bits)
+        even = c_lo if (c_lo & 1) == 0 else c_hi
+        assert oracle.e4m3_from_float(mid) == even
+        assert oracle.e4m3_from_float(-mid) == (even | 0x80)
+        assert oracle.e4m3_from_float(np.nextafter(np.float32(mid), np.float32(0))) == c_lo
+        assert oracle.e4m3_from_float(np.nextafter(np.float32(mid), np.float32(1e9))) == c_hi
+    for v in (448.0, 449.0, 464.0, 1e30, float("inf")):
+        assert oracle.e4m3_from_float(v) == 0x7E and oracle.e4m3_from_float(-v) == 0xFE
+    assert oracle.e4m3_from_float(float("nan")) & 0x7F == 0x7F
+
+
+def test_e4m3_encoder_matches_torch_on_a_dense_sweep():
+    """Library cross-check: torch's float -> float8_e4m3fn conversion (round
+    to nearest even) on values inside the finite range."""
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.normal(0, 1, 20000),
+                        rng.normal(0, 0.01, 20000), np.ldexp(rng.uniform(-1, 1, 5000), -7)])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_from_float(float(v)) for v in x], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def _bf16_bits(a):
+    return (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_quant_rows_closed_forms():
+    # row 0: amax 2 -> s = 2/448; x/s = 224, -448, 112, 0 (exact E4M3 values)
+    # row 1: zero row -> s = 1, codes 0
+    # row 2: a constant row -> every code is +448
+    x = _bf16_bits([[1.0, -2.0, 0.5, 0.0], [0.0, 0.0, 0.0, 0.0], [0.25, 0.25, 0.25, 0.25]])
+    q, s = oracle.quant_rows(x, "e4m3")
+    assert s[0] == np.float32(2.0) / np.float32(448.0) and s[1] == 1.0
+    assert s[2] == np.float32(0.25) / np.float32(448.0)
+    assert list(q[0]) == [0x76, 0xFE, 0x6E, 0x00] and list(q[1]) == [0, 0, 0, 0]
+    assert list(q[2]) == [0x7E] * 4
+    qi, si = oracle.quant_rows(x, "int8")
+    assert si[0] == np.float32(2.0) / np.float32(127.0)
+    # 1 / (2/127) = 63.5 in float32 -> ties to even -> 64
+    assert list(qi[0].view(np.int8)) == [64, -127, 32, 0] and list(qi[1]) == [0, 0, 0, 0]
+
+
+def test_quant_rows_int8_ties_to_even():
+    """amax 127 gives s = 1, so x/s = x and the rounding of exact halves shows."""
+    x = _bf16_bits([[127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 126.5, -126.5]])
+    q, s = oracle.quant_rows(x, "int8")
+    assert s[0] == 1.0
+    assert list(q[0].view(np.int8)) == [127, 0, 2, 2, 0, -2, 126, -126]
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "int8"])
+def test_quant_rows_error_bound_and_range(dtype):
+    """Each dequantised code is within half a step of its input (E4M3: half a
+    unit of the third mantissa bit, relative; int8: s/2), up to the float32
+    rounding of x / s; the row's amax element maps to the largest code."""
+    rng = np.random.default_rng(9)
+    xf = (rng.normal(0, 1, (6, 700)) * np.array([1, 10, 0.01, 1e-3, 100, 3])[:, None]).astype(np.float32)
+    x = _bf16_bits(xf)
+    xv = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    q, s = oracle.quant_rows(x, dtype)
+    for m in range(x.shape[0]):
+        if dtype == "e4m3":
+            deq = np.array([oracle.e4m3_to_double(int(c)) for c in q[m]]) * s[m]
+            assert np.all(np.abs(deq - xv[m]) <= np.abs(xv[m]) * 2.0 ** -4 + s[m] * 2.0 ** -10 + 1e-30)
+            assert np.max(np.abs(deq)) == pytest.approx(448.0 * s[m], rel=1e-6)
+        else:
+            deq = q[m].view(np.int8).astype(np.float64) * s[m]
+            # half a step, plus the float32 rounding of x / s (|x/s| <= 127)
+            assert np.all(np.abs(deq - xv[m]) <= s[m] * (0.5 + 127 * 2.0 ** -23))
+            assert np.max(np.abs(q[m].view(np.int8).astype(int))) == 127
