@@ -17,8 +17,9 @@ here).  Per-bucket microseconds per call are reported beside it.
 ``--impl reference`` times the CPU oracle (plain C, float64) on a bounded
 sample of the same workload instead.
 ``--config NAME`` measures another workload (bf16_small, fp8_calls,
-w8a8_int8, block_fp8, prefill_bf16, prefill_unfused; ``--m`` picks token
-counts) and prints its own line.
+w8a8_int8, block_fp8, prefill_bf16, prefill_unfused, and fp8_quant_calls /
+int8_quant_calls: bf16 activations quantised per token in the same plan run;
+``--m`` picks token counts) and prints its own line.
 """
 from __future__ import annotations
 
@@ -453,7 +454,11 @@ def run_config(args):
     peaks = measured_peaks()
     name = args.config
     unfused = name == "prefill_unfused"
-    wl = "prefill_bf16" if unfused else name
+    # quantisation prologue: bf16 activations in, per-token quantisation
+    # and the GEMM in one plan run
+    quant = name in ("fp8_quant_calls", "int8_quant_calls")
+    wl = {"prefill_unfused": "prefill_bf16", "fp8_quant_calls": "fp8_calls",
+          "int8_quant_calls": "w8a8_int8"}.get(name, name)
     Ms = [None]
     if wl in ("w8a8_int8", "fp8_calls"):
         Ms = list(inputs.DECODE_TOKENS)
@@ -469,9 +474,15 @@ def run_config(args):
         d = device_problem(p, torch)
         plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
                        residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
-                       pdl=not unfused,
+                       pdl=not unfused, quant_a=quant,
                        tuning=json.loads(args.tuning) if args.tuning else None)
         nb = traffic.problem_bytes(p)
+        if quant:
+            # the layer reads bf16 activations instead of codes and scales
+            X = torch.from_numpy(inputs.activations_bf16(p.M, p.K, outlier_frac=0.01)).view(
+                torch.bfloat16).cuda()
+            nb += p.M * p.K * 2 - p.M * p.K - p.M * 4
+            d["A"], d["s_a"] = X, None
         fl = traffic.flops(p.M, p.N, p.K)
         # rotate weight copies so repeated calls do not hit L2
         nw = max(1, math.ceil(2 * 129e6 / max(p.W.nbytes, 1)) + 1)

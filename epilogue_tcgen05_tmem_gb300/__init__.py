@@ -27,13 +27,13 @@ DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2}
 SCALES = {"none": 0, "token_channel": 1, "block": 2}
 ACTS = {"none": 0, "relu": 1, "gelu_erf": 2, "gelu_tanh": 3, "silu": 4}
 EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RUN_GRAPH, \
-    EG_RUN_PDL = 1, 2, 4, 8, 16, 32
+    EG_RUN_PDL, EG_RUN_QUANT_A = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "eg_plan_run",
             "eg_plan_run_unfused", "eg_plan_device_status", "eg_plan_destroy",
             "eg_plan_last_launch_count", "eg_plan_set_test_stall", "eg_plan_get_launch",
             "eg_plan_set_trace", "eg_status_string", "eg_last_error_detail",
-            "eg_linear_noalloc")
+            "eg_linear_noalloc", "eg_quantize_rows")
 EG_TRACE_POINTS = 8
 TRACE_POINT_NAMES = ("start", "setup", "first_tma", "first_operands", "last_commit",
                      "first_acc", "epilogue_done", "end")
@@ -109,6 +109,9 @@ def lib() -> ctypes.CDLL:
             L.eg_linear_noalloc.argtypes = [ctypes.POINTER(eg_problem), ctypes.POINTER(eg_tuning),
                                             ctypes.POINTER(eg_args), vp]
             L.eg_linear_noalloc.restype = ctypes.c_int
+            L.eg_quantize_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int32, vp, ctypes.c_int64, vp, vp]
+            L.eg_quantize_rows.restype = ctypes.c_int
             for f in ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning",
                       "eg_plan_run", "eg_plan_run_unfused", "eg_plan_device_status",
                       "eg_plan_destroy", "eg_plan_set_test_stall", "eg_plan_get_launch",
@@ -171,6 +174,23 @@ def eg_linear_noalloc(problem: eg_problem, tuning: eg_tuning | None, args: eg_ar
                                    ctypes.byref(args), stream)
 
 
+def eg_quantize_rows(x: int, M: int, K: int, ldx: int, dtype: int, q: int, ldq: int, s: int,
+                     stream: int | None) -> int:
+    return lib().eg_quantize_rows(x, M, K, ldx, dtype, q, ldq, s, stream)
+
+
+def quantize_rows(x, dtype: str, stream=None):
+    """Per-token quantisation of bf16 activations x [M, K] (torch CUDA
+    tensor): returns (codes [M, K] uint8 for E4M3 / int8, scales [M] float32)."""
+    import torch
+    M, K = x.shape
+    q = torch.empty(M, K, dtype=torch.uint8 if dtype == "e4m3" else torch.int8, device=x.device)
+    sc = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(eg_quantize_rows(x.data_ptr(), M, K, x.stride(0), DTYPES[dtype], q.data_ptr(), K,
+                            sc.data_ptr(), Plan._stream(stream)))
+    return q, sc
+
+
 def eg_plan_destroy(plan) -> int:
     return lib().eg_plan_destroy(plan)
 
@@ -210,12 +230,13 @@ class Plan:
 
     A [M,K] and W [N,K] hold the input codes (torch.bfloat16, torch.uint8 for
     e4m3 codes or torch.int8), s_a/s_w float32, bias [N] and residual [M,N]
-    bf16, Y [M,N] bf16 (float32/int32 in debug mode).
+    bf16, Y [M,N] bf16 (float32/int32 in debug mode).  With ``quant_a`` A is
+    bf16 and each run quantises it per token first (s_a is not used).
     """
 
     def __init__(self, M, N, K, dtype="bf16", scale="none", act="none", bias=False,
                  residual=False, residual_pre_act=False, debug_accum=False, graph=False,
-                 pdl=False, tuning: dict | None = None):
+                 pdl=False, tuning: dict | None = None, quant_a=False):
         flags = 0
         if bias:
             flags |= EG_EPI_BIAS
@@ -227,6 +248,8 @@ class Plan:
             flags |= EG_RUN_GRAPH
         if pdl:
             flags |= EG_RUN_PDL
+        if quant_a:
+            flags |= EG_RUN_QUANT_A
         self.problem = make_problem(M, N, K, dtype, scale, act, flags)
         t = make_tuning(**tuning) if tuning is not None else None
         s, h = eg_plan_create(self.problem, t)

@@ -16,6 +16,7 @@
 #include "../../include/eg.h"
 #include "eg_kernel.cuh"
 #include "eg_registry.h"
+#include "eg_quant.h"
 #include "eg_tuning.h"
 
 namespace {
@@ -94,6 +95,10 @@ struct eg_plan {
   int kb_count = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  // EG_RUN_QUANT_A: the per-token codes [M][ldq] and scales [M] of A
+  void* qa = nullptr;
+  float* qs = nullptr;
+  int64_t ldq = 0;
   int* counters = nullptr;
   int* status = nullptr;
   uint64_t wait_limit_ns = 0;
@@ -147,8 +152,11 @@ eg_status validate_problem(const eg_problem* p) {
     return fail(EG_ERR_INVALID_ARG, "unknown activation %d", p->act);
   const uint32_t known =
       EG_EPI_BIAS | EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH |
-      EG_RUN_PDL;
+      EG_RUN_PDL | EG_RUN_QUANT_A;
   if (p->flags & ~known) return fail(EG_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  if ((p->flags & EG_RUN_QUANT_A) &&
+      !((p->dtype == EG_IN_E4M3 || p->dtype == EG_IN_INT8) && p->scale == EG_SCALE_TOKEN_CHANNEL))
+    return fail(EG_ERR_INVALID_ARG, "EG_RUN_QUANT_A needs E4M3 or INT8 inputs with per-token scales");
   if ((p->flags & EG_EPI_RESIDUAL) && (p->flags & EG_EPI_RESIDUAL_PRE_ACT))
     return fail(EG_ERR_INVALID_ARG, "EG_EPI_RESIDUAL and EG_EPI_RESIDUAL_PRE_ACT exclude each other");
   if ((p->K * elt_bytes(p->dtype)) % 16)
@@ -325,17 +333,20 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
   const int eb = elt_bytes(p.dtype);
   if (!a->Y) return fail(EG_ERR_INVALID_ARG, "Y is NULL");
   if (p.K > 0 && (!a->A || !a->W)) return fail(EG_ERR_INVALID_ARG, "A or W is NULL");
+  const bool quant_a = (p.flags & EG_RUN_QUANT_A) != 0;  // A holds bf16 activations
   if (p.K > 0) {
-    if (!aligned16(a->A) || !aligned16(a->W))
+    if (!aligned16(a->W) || (!quant_a && !aligned16(a->A)))
       return fail(EG_ERR_INVALID_ARG, "A and W must be 16-byte aligned");
+    if (quant_a && (reinterpret_cast<uintptr_t>(a->A) & 1u))
+      return fail(EG_ERR_INVALID_ARG, "bf16 A must be 2-byte aligned");
     if (a->lda < p.K || a->ldw < p.K)
       return fail(EG_ERR_INVALID_ARG, "lda/ldw must be >= K");
-    if ((a->lda * eb) % 16 || (a->ldw * eb) % 16)
+    if ((!quant_a && (a->lda * eb) % 16) || (a->ldw * eb) % 16)
       return fail(EG_ERR_INVALID_ARG, "lda and ldw must be multiples of 16 bytes");
   }
   if (p.scale != EG_SCALE_NONE) {
-    if (!a->s_a || !a->s_w) return fail(EG_ERR_INVALID_ARG, "scaled modes need s_a and s_w");
-    if (!aligned16(a->s_a) || !aligned16(a->s_w))
+    if ((!quant_a && !a->s_a) || !a->s_w) return fail(EG_ERR_INVALID_ARG, "scaled modes need s_a and s_w");
+    if ((!quant_a && !aligned16(a->s_a)) || !aligned16(a->s_w))
       return fail(EG_ERR_INVALID_ARG, "s_a and s_w must be 16-byte aligned");
   }
   const int esz = debug_out ? 4 : 2;
@@ -354,7 +365,8 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
     if (a->ldr < p.N) return fail(EG_ERR_INVALID_ARG, "ldr must be >= N");
   }
   const size_t ybytes = size_t(p.M - 1) * size_t(a->ldy) * esz + size_t(p.N) * esz;
-  if (overlaps(a->Y, ybytes, a->A, size_t(p.M - 1) * a->lda * eb + size_t(p.K) * eb) ||
+  const int ab = quant_a ? 2 : eb;
+  if (overlaps(a->Y, ybytes, a->A, size_t(p.M - 1) * a->lda * ab + size_t(p.K) * ab) ||
       overlaps(a->Y, ybytes, a->W, size_t(p.N - 1) * a->ldw * eb + size_t(p.K) * eb) ||
       (res && !debug_out &&
        overlaps(a->Y, ybytes, a->residual, size_t(p.M - 1) * a->ldr * 2 + size_t(p.N) * 2)))
@@ -561,6 +573,23 @@ const char* eg_status_string(eg_status s) {
 
 const char* eg_last_error_detail(void) { return g_detail.c_str(); }
 
+eg_status eg_quantize_rows(const void* x, int64_t M, int64_t K, int64_t ldx, int32_t dtype,
+                           void* q, int64_t ldq, float* s, void* stream) {
+  if (M < 0 || K < 0 || M > INT32_MAX || K > INT32_MAX)
+    return fail(EG_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld", (long long)M, (long long)K);
+  if (dtype != EG_IN_E4M3 && dtype != EG_IN_INT8)
+    return fail(EG_ERR_INVALID_ARG, "eg_quantize_rows quantises to E4M3 or INT8 (dtype %d)", dtype);
+  if (M == 0) return EG_OK;
+  if (!s || (K > 0 && (!x || !q)))
+    return fail(EG_ERR_INVALID_ARG, "x, q and s must be non-NULL");
+  if (ldx < K || ldq < K) return fail(EG_ERR_INVALID_ARG, "ldx and ldq must be >= K");
+  if (reinterpret_cast<uintptr_t>(x) & 1u) return fail(EG_ERR_INVALID_ARG, "x must be 2-byte aligned");
+  EG_CUDA(eg::launch_quant_rows(x, M, K, ldx, dtype == EG_IN_E4M3, q, ldq, s,
+                                static_cast<cudaStream_t>(stream), false),
+          "launching the quantisation kernel");
+  return EG_OK;
+}
+
 eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_plan** out) {
   if (!out) return fail(EG_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
@@ -633,6 +662,12 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
     if ((e = cudaMemset(pl->ws, 0, pl->ws_bytes)) != cudaSuccess)
       return cleanup(cuda_fail(e, "zeroing the split-K workspace"));
   }
+  if ((p.flags & EG_RUN_QUANT_A) && p.M > 0) {
+    pl->ldq = (p.K + 15) / 16 * 16;  // 16-byte rows for the TMA loads
+    if ((e = cudaMalloc(&pl->qa, size_t(p.M) * size_t(pl->ldq > 0 ? pl->ldq : 16))) != cudaSuccess ||
+        (e = cudaMalloc(reinterpret_cast<void**>(&pl->qs), size_t(p.M) * sizeof(float))) != cudaSuccess)
+      return cleanup(cuda_fail(e, "allocating the quantised activations"));
+  }
   if ((e = cudaMalloc(reinterpret_cast<void**>(&pl->counters), (tiles + 1) * sizeof(int))) !=
           cudaSuccess ||
       (e = cudaMalloc(reinterpret_cast<void**>(&pl->status), sizeof(int))) != cudaSuccess)
@@ -691,9 +726,23 @@ eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns, int32_t 
 
 static eg_status run_direct(eg_plan* pl, const eg_args* a, cudaStream_t st) {
   const eg_problem& p = pl->prob;
+  eg_args q;
+  if (p.flags & EG_RUN_QUANT_A) {
+    // prologue: per-token codes and scales of the bf16 activations, then
+    // the GEMM on them (its programmatic dependent)
+    EG_CUDA(eg::launch_quant_rows(a->A, p.M, p.K, a->lda, p.dtype == EG_IN_E4M3, pl->qa, pl->ldq,
+                                  pl->qs, st, (p.flags & EG_RUN_PDL) != 0),
+            "launching the quantisation kernel");
+    q = *a;
+    q.A = pl->qa;
+    q.lda = pl->ldq;
+    q.s_a = pl->qs;
+    a = &q;
+  }
   eg_status s = ensure_maps(pl, a);
   if (s != EG_OK) return s;
-  const eg::KParams kp = make_params(pl, a, p.act, epi_flags(p.flags), a->Y, a->ldy);
+  eg::KParams kp = make_params(pl, a, p.act, epi_flags(p.flags), a->Y, a->ldy);
+  if (p.flags & EG_RUN_QUANT_A) kp.pdl = 1;
   return launch_fused(pl, kp, st);
 }
 
@@ -705,16 +754,17 @@ eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream) {
   plan->last_launches = 0;
   if (p.M == 0 || p.N == 0) return EG_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int launches = (p.flags & EG_RUN_QUANT_A) ? 2 : 1;
   if (!(p.flags & EG_RUN_GRAPH)) {
     if ((s = run_direct(plan, args, st)) != EG_OK) return s;
-    plan->last_launches = 1;
+    plan->last_launches = launches;
     return EG_OK;
   }
   // graph mode: one captured graph per distinct argument set
   for (auto& g : plan->graphs) {
     if (memcmp(&g.args, args, sizeof(eg_args)) == 0) {
       EG_CUDA(cudaGraphLaunch(g.exec, st), "cudaGraphLaunch");
-      plan->last_launches = 1;
+      plan->last_launches = launches;
       return EG_OK;
     }
   }
@@ -735,7 +785,7 @@ eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
   plan->graphs.push_back(GraphEntry{*args, exec});
   EG_CUDA(cudaGraphLaunch(exec, st), "cudaGraphLaunch");
-  plan->last_launches = 1;
+  plan->last_launches = launches;
   return EG_OK;
 }
 
@@ -745,6 +795,8 @@ eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1, void
   const eg_problem& p = plan->prob;
   if (p.flags & EG_OUT_DEBUG_ACCUM)
     return fail(EG_ERR_INVALID_ARG, "the unfused path has no debug output mode");
+  if (p.flags & EG_RUN_QUANT_A)
+    return fail(EG_ERR_UNSUPPORTED, "the unfused path takes quantised A (no EG_RUN_QUANT_A)");
   eg_status s = validate_args(plan, args, false);
   if (s != EG_OK) return s;
   plan->last_launches = 0;
@@ -799,6 +851,8 @@ eg_status eg_plan_destroy(eg_plan* plan) {
   for (auto& g : plan->graphs) cudaGraphExecDestroy(g.exec);
   if (plan->cap_stream) cudaStreamDestroy(plan->cap_stream);
   if (plan->ws) cudaFree(plan->ws);
+  if (plan->qa) cudaFree(plan->qa);
+  if (plan->qs) cudaFree(plan->qs);
   if (plan->counters) cudaFree(plan->counters);
   if (plan->status) cudaFree(plan->status);
   delete plan;
@@ -858,6 +912,9 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   const eg_problem& p = *problem;
   if (p.flags & EG_RUN_GRAPH)
     return fail(EG_ERR_INVALID_ARG, "eg_linear_noalloc keeps no captured graphs (drop EG_RUN_GRAPH)");
+  if (p.flags & EG_RUN_QUANT_A)
+    return fail(EG_ERR_UNSUPPORTED, "eg_linear_noalloc has no buffers for quantised activations "
+                                    "(quantise with eg_quantize_rows first)");
   int dev = -1;
   EG_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
   int major = 0, minor = 0;

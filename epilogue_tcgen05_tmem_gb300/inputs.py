@@ -256,3 +256,16 @@ def workload(name: str, M: int | None = None, seed: int = 0) -> Problem:
                             residual=True, residual_pre_act=True, seed=seed,
                             name=name)
     raise KeyError(name)
+
+
+def activations_bf16(M: int, K: int, seed: int = 0, outlier_frac: float = 0.0,
+                     outlier_mult: float = 10.0) -> np.ndarray:
+    """bf16 bit patterns [M, K] of the activations make_problem draws (the
+    same seed streams and outlier columns), before any quantisation: the
+    input of the per-token quantisation prologue."""
+    a = normal(seed, STREAM_A, (M, K), 1.0)
+    if outlier_frac > 0 and K > 0:
+        nout = int(round(outlier_frac * K))
+        cols = np.sort(permutation(seed, STREAM_OUTLIER, K)[:nout])
+        a[:, cols] *= outlier_mult
+    return to_bf16_bits(a)

@@ -116,13 +116,21 @@ enum {
   EG_EPI_RESIDUAL_PRE_ACT = 4,  /* v = act(v + R)  (excludes EG_EPI_RESIDUAL) */
   EG_OUT_DEBUG_ACCUM = 8,       /* write the raw reduced accumulator */
   EG_RUN_GRAPH = 16,            /* eg_plan_run replays a captured CUDA graph */
-  EG_RUN_PDL = 32               /* launch as a programmatic dependent of the
+  EG_RUN_PDL = 32,              /* launch as a programmatic dependent of the
                                    previous kernel on the stream: the kernel
                                    starts streaming W before that kernel has
                                    finished, and waits for it before reading
                                    A, s_a, R, bias or s_w and before writing.
                                    Requires that the previous kernel does not
                                    write W. */
+  EG_RUN_QUANT_A = 64           /* E4M3 / INT8 with per-token scales only:
+                                   eg_args.A holds bf16 activations [M][lda]
+                                   (lda in elements); each run first
+                                   quantises them per token as
+                                   eg_quantize_rows does, into codes and
+                                   scales the plan owns (eg_args.s_a is not
+                                   read), then runs the GEMM on them as its
+                                   programmatic dependent. */
 };
 
 typedef struct {
@@ -130,7 +138,7 @@ typedef struct {
   int32_t dtype;  /* eg_in_dtype */
   int32_t scale;  /* eg_scale_mode */
   int32_t act;    /* eg_act */
-  uint32_t flags; /* EG_EPI_* | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH */
+  uint32_t flags; /* EG_EPI_* | EG_OUT_DEBUG_ACCUM | EG_RUN_* */
 } eg_problem;
 
 /* One point of the kernel's tuning space.  The UMMA tile is 128 rows by
@@ -260,6 +268,22 @@ EG_API eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace
  * eg_last_error_detail().  Device-side wait timeouts are not reported. */
 EG_API eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
                                    const eg_args* args, void* stream);
+
+/* Dynamic per-token quantisation of activations, the prologue transform in
+ * front of the FP8_Dynamic and W8A8_INT8 layers ("Helion linear backend in
+ * vLLM", section "One kernel instead of three": per-token activation
+ * scales; "Helion + TorchInductor co-operation: operator fusion", section
+ * on prologue fusion).  For each row m of x (bf16 [M][ldx], device):
+ *   s[m] = amax_k |x[m][k]| / 448 (dtype EG_IN_E4M3) or / 127 (EG_IN_INT8),
+ *          float32 division; s[m] = 1 when the row is all zero;
+ *   q[m][k] = round-to-nearest-even(x[m][k] / s[m]) (float32 division),
+ *          saturated to +-448 (E4M3 code) or +-127 (int8).
+ * q: device bytes [M][ldq], ldq >= K; s: device float [M].  Enqueued on
+ * `stream` (a cudaStream_t, NULL for the default stream); nothing is
+ * allocated.  EG_ERR_INVALID_ARG for bad sizes, NULL pointers or another
+ * dtype; EG_ERR_CUDA if the launch fails. */
+EG_API eg_status eg_quantize_rows(const void* x, int64_t M, int64_t K, int64_t ldx, int32_t dtype,
+                                  void* q, int64_t ldq, float* s, void* stream);
 
 EG_API const char* eg_status_string(eg_status s);
 EG_API const char* eg_last_error_detail(void);
