@@ -185,6 +185,8 @@ class Problem:
     residual_pre_act: bool = False
     name: str = ""
     meta: dict = field(default_factory=dict)
+    out: str = "bf16"     # output format: "bf16" | "f16" | "e4m3" (codes of Y / s_y)
+    s_y: float = 1.0      # per-tensor output scale (E4M3 output only)
 
 
 def make_problem(M, N, K, dtype="bf16", scale=None, act="none", bias=False,
@@ -229,7 +231,7 @@ def take_tokens(p: Problem, m: int) -> Problem:
     r = None if p.residual is None else np.ascontiguousarray(p.residual[:m])
     return Problem(m, p.N, p.K, p.dtype, p.scale, p.act, p.bias, r,
                    np.ascontiguousarray(p.A[:m]), p.W, s_a, p.s_w,
-                   p.residual_pre_act, p.name, dict(p.meta))
+                   p.residual_pre_act, p.name, dict(p.meta), p.out, p.s_y)
 
 
 # Workloads of the pages, restated as seeded synthetic problems.
@@ -241,12 +243,12 @@ def workload(name: str, M: int | None = None, seed: int = 0) -> Problem:
         return make_problem(64, 256, 512, "bf16", act="gelu_erf", bias=True,
                             seed=seed, name=name)
     if name == "fp8_dynamic":           # K=4096 N=12288, +bias, SiLU
-        p = make_problem(32, 12288, 4096, "e4m3", "token_channel", act="silu",
+        p = make_problem(max(32, M or 32), 12288, 4096, "e4m3", "token_channel", act="silu",
                          bias=True, outlier_frac=0.01, seed=seed, name=name)
         return take_tokens(p, M or 32)
     if name == "w8a8_int8":             # K=12288 N=4096, + residual
-        p = make_problem(32, 4096, 12288, "int8", "token_channel", residual=True,
-                         seed=seed, name=name)
+        p = make_problem(max(32, M or 32), 4096, 12288, "int8", "token_channel",
+                         residual=True, seed=seed, name=name)
         return take_tokens(p, M or 32)
     if name == "block_fp8":             # K=5120 N=25600
         return make_problem(M or 32, 25600, 5120, "e4m3", "block", seed=seed,

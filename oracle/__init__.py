@@ -30,13 +30,13 @@ _lib = None
 DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2}
 SCALES = {"none": 0, "token_channel": 1, "block": 2}
 ACTS = {"none": 0, "relu": 1, "gelu_erf": 2, "gelu_tanh": 3, "silu": 4}
-BIAS, RESIDUAL, RESIDUAL_PRE_ACT = 1, 2, 4
+BIAS, RESIDUAL, RESIDUAL_PRE_ACT, OUT_F16, OUT_E4M3 = 1, 2, 4, 8, 16
 
 
 class _Problem(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("dtype", ctypes.c_int32), ("scale", ctypes.c_int32),
-                ("act", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("act", ctypes.c_int32), ("flags", ctypes.c_uint32), ("s_y", ctypes.c_float)]
 
 
 def build(force: bool = False) -> str:
@@ -81,6 +81,12 @@ def lib():
             L.orc_quant_rows.restype = ctypes.c_int
             L.orc_e4m3_from_float.argtypes = [ctypes.c_float]
             L.orc_e4m3_from_float.restype = ctypes.c_uint8
+            L.orc_e4m3_from_double.argtypes = [ctypes.c_double]
+            L.orc_e4m3_from_double.restype = ctypes.c_uint8
+            L.orc_f16_to_double.argtypes = [ctypes.c_uint16]
+            L.orc_f16_to_double.restype = ctypes.c_double
+            L.orc_f16_from_double.argtypes = [ctypes.c_double]
+            L.orc_f16_from_double.restype = ctypes.c_uint16
             for f in ("orc_linear", "orc_linear_naive", "orc_linear_points",
                       "orc_accum_splitk", "orc_default_threads"):
                 getattr(L, f).restype = ctypes.c_int
@@ -97,7 +103,8 @@ def _c(a, dt):
 
 
 def _problem(p, flags):
-    return _Problem(p.M, p.N, p.K, DTYPES[p.dtype], SCALES[p.scale], ACTS[p.act], flags)
+    return _Problem(p.M, p.N, p.K, DTYPES[p.dtype], SCALES[p.scale], ACTS[p.act], flags,
+                    float(getattr(p, "s_y", 1.0)))
 
 
 def _flags(p):
@@ -106,6 +113,11 @@ def _flags(p):
         f |= BIAS
     if p.residual is not None:
         f |= RESIDUAL_PRE_ACT if p.residual_pre_act else RESIDUAL
+    out = getattr(p, "out", "bf16")
+    if out == "f16":
+        f |= OUT_F16
+    elif out == "e4m3":
+        f |= OUT_E4M3
     return f
 
 
@@ -119,8 +131,9 @@ def _arrays(p):
 
 
 def linear(p, nthreads: int = 0, want_acc: bool = False, naive: bool = False):
-    """Y (bf16 bits [M,N]); with want_acc also the float64 accumulator and, for
-    INT8, the exact int64 accumulator.  ``p`` is any object with the fields
+    """Y (bf16 bits [M,N]: fp16 bits, or E4M3 codes as uint8, when ``p.out``
+    says so); with want_acc also the float64 accumulator and, for INT8, the
+    exact int64 accumulator.  ``p`` is any object with the fields
     of a problem (M, N, K, dtype, scale, act, A, W, s_a, s_w, bias, residual,
     residual_pre_act)."""
     A, W, sa, sw, b, r = _arrays(p)
@@ -136,6 +149,8 @@ def linear(p, nthreads: int = 0, want_acc: bool = False, naive: bool = False):
                               _ptr(b), _ptr(r), _ptr(Y), _ptr(acc), _ptr(acc64), nthreads)
     if rc:
         raise ValueError("oracle rejected the problem")
+    if getattr(p, "out", "bf16") == "e4m3":
+        Y = Y.astype(np.uint8)
     if want_acc:
         return Y, acc, acc64
     return Y
@@ -154,6 +169,8 @@ def linear_points(p, ms, ns, nthreads: int = 0):
                                  _ptr(Y), _ptr(acc), nthreads)
     if rc:
         raise ValueError("oracle rejected the points")
+    if getattr(p, "out", "bf16") == "e4m3":
+        Y = Y.astype(np.uint8)
     return Y, acc
 
 
@@ -205,3 +222,15 @@ def quant_rows(x_bits, dtype: str):
 
 def e4m3_from_float(v: float) -> int:
     return lib().orc_e4m3_from_float(v)
+
+
+def e4m3_from_double(v: float) -> int:
+    return lib().orc_e4m3_from_double(v)
+
+
+def f16_to_double(bits: int) -> float:
+    return lib().orc_f16_to_double(bits)
+
+
+def f16_from_double(v: float) -> int:
+    return lib().orc_f16_from_double(v)

@@ -109,6 +109,8 @@ static int check(const orc_problem* p, const void* A, const void* W,
   if ((p->flags & ORC_BIAS) && !bias) return -1;
   if ((p->flags & (ORC_RESIDUAL | ORC_RESIDUAL_PRE_ACT)) && !R) return -1;
   if (p->act < ORC_ACT_NONE || p->act > ORC_ACT_SILU) return -1;
+  if ((p->flags & ORC_OUT_F16) && (p->flags & ORC_OUT_E4M3)) return -1;
+  if ((p->flags & ORC_OUT_E4M3) && !(p->s_y > 0.0f && isfinite(p->s_y))) return -1;
   return 0;
 }
 
@@ -126,6 +128,8 @@ static uint16_t epilogue(const orc_problem* p, int64_t m, int64_t n, double acc,
     v = orc_act(p->act, v);
     if (p->flags & ORC_RESIDUAL) v = v + orc_bf16_to_double(R[m * p->N + n]);
   }
+  if (p->flags & ORC_OUT_F16) return orc_f16_from_double(v);
+  if (p->flags & ORC_OUT_E4M3) return orc_e4m3_from_double(v / (double)p->s_y);
   return orc_bf16_from_double(v);
 }
 
@@ -382,10 +386,12 @@ int orc_accum_splitk(const orc_problem* p, const void* A, const void* W,
  * largest finite magnitude is 1.75 * 2^8 = 448.  The magnitude is rounded
  * on the grid of its binade (the subnormal grid 2^-9 below 2^-6), ties to
  * even; a result past 448 saturates. */
-uint8_t orc_e4m3_from_float(float v) {
+uint8_t orc_e4m3_from_float(float v) { return orc_e4m3_from_double((double)v); }
+
+uint8_t orc_e4m3_from_double(double v) {
   const uint8_t sign = signbit(v) ? 0x80 : 0;
   if (isnan(v)) return sign | 0x7F;
-  const double a = fabs((double)v);
+  const double a = fabs(v);
   if (a == 0.0) return sign;
   int e;
   frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1) */
@@ -432,4 +438,41 @@ int orc_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int32_t
     }
   }
   return 0;
+}
+
+
+/* ---------------------------------------------------------------------- */
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 mantissa bits; exponent
+ * field 0 holds the subnormals m * 2^-24; field 31 is infinity / NaN. */
+double orc_f16_to_double(uint16_t bits) {
+  const int sign = bits >> 15;
+  const int e = (bits >> 10) & 0x1F;
+  const int m = bits & 0x3FF;
+  double mag;
+  if (e == 31) mag = m ? NAN : INFINITY;
+  else if (e == 0) mag = ldexp((double)m, -24);
+  else mag = ldexp(1.0 + (double)m / 1024.0, e - 15);
+  return sign ? -mag : mag;
+}
+
+uint16_t orc_f16_from_double(double v) {
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  if (isnan(v)) return 0x7E00;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7C00;
+  int e;
+  frexp(a, &e);
+  int lead = e - 1;
+  if (lead < -14) lead = -14;                /* subnormals share the 2^-24 grid */
+  const double quantum = ldexp(1.0, lead - 10);
+  const double n = nearbyint(a / quantum);   /* exact quotient; ties to even */
+  const double r = n * quantum;
+  if (r >= 65536.0) return sign | 0x7C00;    /* past the largest finite: infinity */
+  if (r < 0x1p-14) return sign | (uint16_t)nearbyint(r / 0x1p-24);
+  int er;
+  const double fr = frexp(r, &er);
+  const int exp_field = er - 1 + 15;
+  const int mant = (int)((fr * 2.0 - 1.0) * 1024.0);
+  return sign | (uint16_t)((exp_field << 10) | mant);
 }

@@ -14,7 +14,9 @@
  *   v += bias[n]                                        (if BIAS)
  *   default order:  v = act(v); v += R[m][n]            (if RESIDUAL)
  *   pre-act order:  v += R[m][n]; v = act(v)            (if RESIDUAL_PRE_ACT)
- *   Y[m][n] = bf16 round-to-nearest-even of v, rounded directly from float64.
+ *   Y[m][n] = bf16 round-to-nearest-even of v, rounded directly from float64
+ *   (or fp16, or the E4M3 code of v / s_y: ORC_OUT_F16, ORC_OUT_E4M3; the
+ *   uint16 output then holds the fp16 bits or the code in its low byte).
  *
  * Sources: "Helion + TorchInductor co-operation: operator fusion", section
  * "Designing extensible epilogues in Helion" (bias broadcast over rows, ReLU,
@@ -53,11 +55,19 @@ extern "C" {
 #define ORC_BIAS 1u
 #define ORC_RESIDUAL 2u
 #define ORC_RESIDUAL_PRE_ACT 4u
+/* Output narrowing ("Helion + TorchInductor co-operation: operator fusion":
+ * the FP32 -> narrow conversion right before the store, fp16 on that page's
+ * own kernel): without these flags Y is bf16; ORC_OUT_F16 rounds v to IEEE
+ * binary16 (nearest even, overflow to infinity); ORC_OUT_E4M3 writes the
+ * E4M3 code of v / s_y (float64 division, nearest even, saturating). */
+#define ORC_OUT_F16 8u
+#define ORC_OUT_E4M3 16u
 
 typedef struct {
   int64_t M, N, K;
   int32_t dtype, scale, act;
   uint32_t flags;
+  float s_y; /* output scale, ORC_OUT_E4M3 only */
 } orc_problem;
 
 /* Element codecs. */
@@ -119,6 +129,13 @@ int orc_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int32_t
 /* OCP FP8 E4M3 code of a float: round to nearest, ties to even, finite
  * values saturate to +-448, NaN -> 0x7F (sign kept). */
 uint8_t orc_e4m3_from_float(float v);
+uint8_t orc_e4m3_from_double(double v);
+
+/* IEEE binary16: decode, and round a float64 to nearest even in one step
+ * (subnormals on the 2^-24 grid; magnitudes that round past 65504 become
+ * infinity). */
+double orc_f16_to_double(uint16_t bits);
+uint16_t orc_f16_from_double(double v);
 
 #ifdef __cplusplus
 }

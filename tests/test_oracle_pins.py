@@ -454,3 +454,86 @@ def test_quant_rows_error_bound_and_range(dtype):
             # half a step, plus the float32 rounding of x / s (|x/s| <= 127)
             assert np.all(np.abs(deq - xv[m]) <= s[m] * (0.5 + 127 * 2.0 ** -23))
             assert np.max(np.abs(q[m].view(np.int8).astype(int))) == 127
+
+
+# --------------------------------------------------- output narrowing ---
+
+def test_f16_decode_all_patterns_match_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_double(int(b)) for b in bits])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.all(np.isnan(got[np.isnan(ref)])) and np.array_equal(got[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+def test_f16_rounding_matches_numpy_from_float64():
+    """Library cross-check: numpy's float64 -> float16 conversion rounds to
+    nearest even in one step (no float32 in between)."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.normal(0, 1, 20000), rng.normal(0, 3e4, 5000),
+                        rng.normal(0, 1e-5, 5000), np.ldexp(rng.uniform(-1, 1, 5000), -20),
+                        np.array([65504.0, 65519.99, 65520.0, 1e6, -65520.0, 0.0, -0.0])])
+    with np.errstate(over="ignore"):   # 1e6 overflows to infinity, as intended
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f16_from_double(float(v)) for v in x], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_f16_ties_to_even():
+    # 1 + 2^-11 is halfway between 1 and 1 + 2^-10: even mantissa (1.0) wins;
+    # 1 + 3 * 2^-11 is halfway between 1 + 2^-10 and 1 + 2^-9: 1 + 2^-9 wins
+    assert oracle.f16_from_double(1 + 2.0 ** -11) == 0x3C00
+    assert oracle.f16_from_double(1 + 3 * 2.0 ** -11) == 0x3C02
+    assert oracle.f16_from_double(2.0 ** -25) == 0x0000          # half the smallest subnormal
+    assert oracle.f16_from_double(3 * 2.0 ** -25) == 0x0002
+
+
+@pytest.mark.parametrize("out", ["f16", "e4m3"])
+def test_output_format_closed_form(out):
+    """A = W = 1, token/channel scales 1: v = K exactly, so Y is the format's
+    encoding of K (E4M3: of K / s_y)."""
+    K = 256
+    p = inputs.make_problem(2, 3, K, "e4m3", "token_channel", seed=1)
+    p.A = np.full((2, K), 0x38, np.uint8)   # e4m3 1.0
+    p.W = np.full((3, K), 0x38, np.uint8)
+    p.s_a = np.ones(2, np.float32)
+    p.s_w = np.ones(3, np.float32)
+    p.out = out
+    p.s_y = 2.0
+    y = oracle.linear(p)
+    if out == "f16":
+        assert np.all(y == np.float16(K).view(np.uint16))
+    else:
+        assert y.dtype == np.uint8 and np.all(y == oracle.e4m3_from_float(K / 2.0))
+        assert oracle.e4m3_to_double(int(y[0, 0])) * 2.0 == K
+
+
+def test_output_formats_agree_with_bf16_path():
+    """The same epilogue value rounded three ways: the fp16 and E4M3 outputs
+    decode to within half a step of the bf16 output's exact value."""
+    p = inputs.make_problem(5, 40, 512, "e4m3", "token_channel", act="gelu_tanh", bias=True,
+                            residual=True, seed=4)
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    yb = oracle.linear(p)
+    p.out = "f16"
+    yh = oracle.linear(p)
+    p.out, p.s_y = "e4m3", 0.0625
+    ye = oracle.linear(p)
+    vb = (yb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    vh = yh.view(np.float16).astype(np.float64)
+    ve = np.vectorize(oracle.e4m3_to_double)(ye.astype(int)) * 0.0625
+    # bf16 keeps 8 significant bits, fp16 11, E4M3 4: each within its own
+    # half step of the exact value, so within the sum of the two half steps
+    assert np.all(np.abs(vh - vb) <= np.abs(vb) * (2.0 ** -8 + 2.0 ** -11) + 2.0 ** -24)
+    assert np.all(np.abs(ve - vb) <= np.abs(vb) * (2.0 ** -8 + 2.0 ** -4) + 0.0625 * 2.0 ** -9)
+
+
+def test_output_format_flags_rejected_together():
+    p = inputs.make_problem(2, 3, 64, "bf16", seed=1)
+    pr = oracle._problem(p, oracle.OUT_F16 | oracle.OUT_E4M3)
+    A, W, sa, sw, b, r = oracle._arrays(p)
+    Y = np.zeros((2, 3), np.uint16)
+    import ctypes
+    assert oracle.lib().orc_linear(ctypes.byref(pr), oracle._ptr(A), oracle._ptr(W), None, None,
+                                   None, None, oracle._ptr(Y), None, None, 1) == -1
