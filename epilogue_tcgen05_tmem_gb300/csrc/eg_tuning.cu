@@ -3,7 +3,10 @@
 // num_tokens in {1, 2, 4, 8, 16, 24, 32} ("Helion linear backend in vLLM",
 // sections "Hybrid dispatch" and "How the autotuner searches"), and ship a
 // default configuration for functional tests next to the tuned sets
-// (section "How it will be deployed").
+// (section "How it will be deployed").  Above 32 tokens the pages hand the
+// layer to library kernels; here the same kernel keeps going, with swept
+// entries at 64, 128, ..., 2048 tokens (a token count uses the first bucket
+// at or above it).
 #include "eg_registry.h"
 #include "eg_tuning.h"
 
@@ -16,7 +19,8 @@ const TuningRow kTable[] = {
 #include "eg_tuning_table.inc"
     {-1, -1, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
 
-constexpr int kBuckets[] = {1, 2, 4, 8, 16, 24, 32};
+// decode buckets, then the mid-range (prefill ramp) buckets
+constexpr int kBuckets[] = {1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048};
 
 int bucket_of(int64_t M) {
   for (int b : kBuckets)

@@ -5,8 +5,9 @@
 
 namespace eg {
 
-// One row of the swept table.  m_max is the token bucket (1,2,4,8,16,24,32)
-// the row was tuned at; rows with m_max == 0 cover every M above 32.
+// One row of the swept table.  m_max is the token bucket the row was tuned
+// at (1, 2, 4, 8, 16, 24, 32, 64, ..., 2048); rows with m_max == 0 cover
+// every M above the largest bucket.
 struct TuningRow {
   int32_t dtype, scale;
   int64_t N, K;

@@ -41,6 +41,9 @@ def candidates(p, swaps=(0, 1)):
     max_bn = 64 if p.dtype == "int8" else (128 if promote else 256)
     elems = 64 if p.dtype == "bf16" else 128
     k_tiles = -(-p.K // elems)
+    if p.M > 32:
+        yield from _midrange_candidates(p, swaps, max_bn, k_tiles)
+        return
     for swap in swaps:
         cols = p.M if swap else p.N
         for bn in TILE_N:
@@ -62,6 +65,26 @@ def candidates(p, swaps=(0, 1)):
                 for sk in (1, 2):
                     yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=swap, stream_k=sk,
                                cluster_reduce=0)
+
+
+def _midrange_candidates(p, swaps, max_bn, k_tiles):
+    """A smaller space above 32 tokens: wide tiles, a few ring depths, light
+    split-K and balanced split-K with one CTA per SM."""
+    for swap in swaps:
+        cols = p.M if swap else p.N
+        if swap and p.M > 256:
+            continue
+        for bn in (64, 128, 256):
+            if bn > max_bn or (bn > 64 and bn // 2 >= cols):
+                continue
+            for stages in (3, 4, 6):
+                for s in (1, 2, 4):
+                    if s > k_tiles or (s > 1 and k_tiles // s < 2):
+                        continue
+                    yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0,
+                               cluster_reduce=0)
+                yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=swap, stream_k=1,
+                           cluster_reduce=0)
 
 
 def time_config(eg, torch, p, d, Ws, tuning, reps=3, calls=None):
@@ -142,7 +165,7 @@ def sweep(workload, tokens, swaps=(0, 1), verbose=True):
             if t is not None:
                 results.append((c, t))
         c, t = pick(results)
-        bucket = M if M <= 32 else 0
+        bucket = M if M <= 2048 else 0
         row = (eg.DTYPES[p.dtype], eg.SCALES[p.scale], p.N, p.K, bucket, c["tile_n"],
                c["stages"], c["split_k"], c["swap_ab"], c["stream_k"], c["cluster_reduce"])
         rows.append(row)

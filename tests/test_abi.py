@@ -118,7 +118,8 @@ def test_tuning_table_rows_are_valid():
     for r in rows:
         assert len(r) == 11, r
         dtype, scale, N, K, bucket, tn, stages, split, swap, sk, cl = r
-        assert bucket in (0, 1, 2, 4, 8, 16, 24, 32) and tn in (16, 32, 64, 128, 256)
+        assert bucket in (0, 1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048)
+        assert tn in (16, 32, 64, 128, 256)
         assert 2 <= stages <= 8 and swap in (0, 1) and cl in (0, 1)
         if cl:
             assert split in (2, 4, 8) and sk == 0, r
