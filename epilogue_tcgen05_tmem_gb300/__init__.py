@@ -27,7 +27,8 @@ DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2}
 SCALES = {"none": 0, "token_channel": 1, "block": 2}
 ACTS = {"none": 0, "relu": 1, "gelu_erf": 2, "gelu_tanh": 3, "silu": 4}
 EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RUN_GRAPH, \
-    EG_RUN_PDL, EG_RUN_QUANT_A = 1, 2, 4, 8, 16, 32, 64
+    EG_RUN_PDL, EG_RUN_QUANT_A, EG_OUT_F16, EG_OUT_E4M3 = 1, 2, 4, 8, 16, 32, 64, 128, 256
+OUTS = {"bf16": 0, "f16": EG_OUT_F16, "e4m3": EG_OUT_E4M3}
 
 EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "eg_plan_run",
             "eg_plan_run_unfused", "eg_plan_device_status", "eg_plan_destroy",
@@ -60,7 +61,7 @@ class eg_args(ctypes.Structure):
     _fields_ = [("A", ctypes.c_void_p), ("W", ctypes.c_void_p), ("s_a", ctypes.c_void_p),
                 ("s_w", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p),
                 ("Y", ctypes.c_void_p), ("lda", ctypes.c_int64), ("ldw", ctypes.c_int64),
-                ("ldr", ctypes.c_int64), ("ldy", ctypes.c_int64)]
+                ("ldr", ctypes.c_int64), ("ldy", ctypes.c_int64), ("s_y", ctypes.c_void_p)]
 
 
 class eg_launch_info(ctypes.Structure):
@@ -230,13 +231,15 @@ class Plan:
 
     A [M,K] and W [N,K] hold the input codes (torch.bfloat16, torch.uint8 for
     e4m3 codes or torch.int8), s_a/s_w float32, bias [N] and residual [M,N]
-    bf16, Y [M,N] bf16 (float32/int32 in debug mode).  With ``quant_a`` A is
-    bf16 and each run quantises it per token first (s_a is not used).
+    bf16, Y [M,N] bf16 (float32/int32 in debug mode; ``out="f16"``: fp16;
+    ``out="e4m3"``: uint8 codes of v / s_y, s_y a one-element float32
+    tensor).  With ``quant_a`` A is bf16 and each run quantises it per token
+    first (s_a is not used).
     """
 
     def __init__(self, M, N, K, dtype="bf16", scale="none", act="none", bias=False,
                  residual=False, residual_pre_act=False, debug_accum=False, graph=False,
-                 pdl=False, tuning: dict | None = None, quant_a=False):
+                 pdl=False, tuning: dict | None = None, quant_a=False, out="bf16"):
         flags = 0
         if bias:
             flags |= EG_EPI_BIAS
@@ -250,6 +253,7 @@ class Plan:
             flags |= EG_RUN_PDL
         if quant_a:
             flags |= EG_RUN_QUANT_A
+        flags |= OUTS[out]
         self.problem = make_problem(M, N, K, dtype, scale, act, flags)
         t = make_tuning(**tuning) if tuning is not None else None
         s, h = eg_plan_create(self.problem, t)
@@ -279,11 +283,11 @@ class Plan:
         else:
             _check(lib().eg_plan_set_trace(self.handle, buf.data_ptr(), buf.shape[0]))
 
-    def args(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None) -> eg_args:
+    def args(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None, s_y=None) -> eg_args:
         return eg_args(_ptr(A), _ptr(W), _ptr(s_a), _ptr(s_w), _ptr(bias), _ptr(residual),
                        _ptr(Y), A.stride(0) if A is not None else 0,
                        W.stride(0) if W is not None else 0,
-                       residual.stride(0) if residual is not None else 0, Y.stride(0))
+                       residual.stride(0) if residual is not None else 0, Y.stride(0), _ptr(s_y))
 
     @staticmethod
     def _stream(stream):
@@ -292,8 +296,8 @@ class Plan:
             return torch.cuda.current_stream().cuda_stream
         return stream
 
-    def run(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None, stream=None):
-        _check(eg_plan_run(self.handle, self.args(A, W, Y, s_a, s_w, bias, residual),
+    def run(self, A, W, Y, s_a=None, s_w=None, bias=None, residual=None, stream=None, s_y=None):
+        _check(eg_plan_run(self.handle, self.args(A, W, Y, s_a, s_w, bias, residual, s_y),
                            self._stream(stream)))
         return Y
 

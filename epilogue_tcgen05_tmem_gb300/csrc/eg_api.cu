@@ -78,6 +78,13 @@ uint64_t default_wait_limit_ns() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Bytes of one Y element for the output flags.
+int out_elt_bytes(uint32_t flags) {
+  if (flags & EG_OUT_DEBUG_ACCUM) return 4;
+  if (flags & EG_OUT_E4M3) return 1;
+  return 2;
+}
+
 }  // namespace
 
 struct GraphEntry {
@@ -152,8 +159,11 @@ eg_status validate_problem(const eg_problem* p) {
     return fail(EG_ERR_INVALID_ARG, "unknown activation %d", p->act);
   const uint32_t known =
       EG_EPI_BIAS | EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH |
-      EG_RUN_PDL | EG_RUN_QUANT_A;
+      EG_RUN_PDL | EG_RUN_QUANT_A | EG_OUT_F16 | EG_OUT_E4M3;
   if (p->flags & ~known) return fail(EG_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
+  const uint32_t outs = p->flags & (EG_OUT_F16 | EG_OUT_E4M3 | EG_OUT_DEBUG_ACCUM);
+  if (outs & (outs - 1))
+    return fail(EG_ERR_INVALID_ARG, "EG_OUT_F16, EG_OUT_E4M3 and EG_OUT_DEBUG_ACCUM exclude each other");
   if ((p->flags & EG_RUN_QUANT_A) &&
       !((p->dtype == EG_IN_E4M3 || p->dtype == EG_IN_INT8) && p->scale == EG_SCALE_TOKEN_CHANNEL))
     return fail(EG_ERR_INVALID_ARG, "EG_RUN_QUANT_A needs E4M3 or INT8 inputs with per-token scales");
@@ -349,9 +359,13 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
     if ((!quant_a && !aligned16(a->s_a)) || !aligned16(a->s_w))
       return fail(EG_ERR_INVALID_ARG, "s_a and s_w must be 16-byte aligned");
   }
-  const int esz = debug_out ? 4 : 2;
+  const int esz = out_elt_bytes(p.flags);
   if (reinterpret_cast<uintptr_t>(a->Y) % esz)
     return fail(EG_ERR_INVALID_ARG, "Y must be aligned to its element size");
+  if (p.flags & EG_OUT_E4M3) {
+    if (!a->s_y || (reinterpret_cast<uintptr_t>(a->s_y) & 3u))
+      return fail(EG_ERR_INVALID_ARG, "EG_OUT_E4M3 needs s_y, 4-byte aligned");
+  }
   if (a->ldy < p.N) return fail(EG_ERR_INVALID_ARG, "ldy must be >= N");
   if (!debug_out && (p.flags & EG_EPI_BIAS)) {
     if (!a->bias) return fail(EG_ERR_INVALID_ARG, "EG_EPI_BIAS needs bias");
@@ -429,8 +443,11 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.wait_limit_ns = pl->wait_limit_ns;
   k.stall_producer = pl->stall;
   const bool res = (flags & (eg::F_RES | eg::F_RES_PRE)) != 0;
-  k.vec_ok = aligned16(Y) && (ldy * 2) % 16 == 0 &&
+  const int yb = (flags & eg::F_DEBUG) ? 4 : out_elt_bytes(p.flags);
+  k.vec_ok = aligned16(Y) && (ldy * yb) % 16 == 0 &&
              (!res || (aligned16(a->residual) && (a->ldr * 2) % 16 == 0));
+  k.out = (p.flags & EG_OUT_F16) ? eg::OUT_F16 : (p.flags & EG_OUT_E4M3) ? eg::OUT_E4M3 : eg::OUT_BF16;
+  k.s_y = a->s_y;
   k.pdl = (p.flags & EG_RUN_PDL) ? 1 : 0;
   k.l2_prefetch = pl->l2_prefetch;
   k.trace = pl->trace;
@@ -797,6 +814,8 @@ eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1, void
     return fail(EG_ERR_INVALID_ARG, "the unfused path has no debug output mode");
   if (p.flags & EG_RUN_QUANT_A)
     return fail(EG_ERR_UNSUPPORTED, "the unfused path takes quantised A (no EG_RUN_QUANT_A)");
+  if (p.flags & (EG_OUT_F16 | EG_OUT_E4M3))
+    return fail(EG_ERR_UNSUPPORTED, "the unfused path writes bf16 only");
   eg_status s = validate_args(plan, args, false);
   if (s != EG_OK) return s;
   plan->last_launches = 0;

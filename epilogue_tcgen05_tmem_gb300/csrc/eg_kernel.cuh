@@ -38,6 +38,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "eg_ptx.cuh"
 
@@ -47,6 +48,8 @@ enum : int { IN_BF16 = 0, IN_E4M3 = 1, IN_INT8 = 2 };
 enum : int { SC_NONE = 0, SC_TC = 1, SC_BLOCK = 2 };
 enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_ERF = 2, ACT_GELU_TANH = 3, ACT_SILU = 4 };
 enum : uint32_t { F_BIAS = 1, F_RES = 2, F_RES_PRE = 4, F_DEBUG = 8 };
+// Output element formats: bf16, fp16, or the E4M3 code of v / s_y.
+enum : int { OUT_BF16 = 0, OUT_F16 = 1, OUT_E4M3 = 2 };
 // Device status codes (first failure wins).
 enum : int { ST_TIMEOUT_PRODUCER = 1, ST_TIMEOUT_MMA = 2, ST_TIMEOUT_EPILOGUE = 3,
              ST_TIMEOUT_CONVERT = 4, ST_TIMEOUT_TEARDOWN = 5 };
@@ -83,6 +86,8 @@ struct KParams {
   int32_t stream_k;               // balanced split-K over the grid (else split_k)
   int32_t max_contrib;            // workspace slots per tile
   int32_t cluster_reduce;         // split-K through distributed shared memory
+  int32_t out;                    // OUT_BF16 / OUT_F16 / OUT_E4M3
+  const float* s_y;               // per-tensor output scale (OUT_E4M3)
 };
 
 constexpr int kTracePoints = 8;
@@ -288,6 +293,62 @@ __device__ __forceinline__ float bf16_to_f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// The single narrowing of an epilogue value to the output format: bf16 or
+// fp16 bits, or (E4M3) the code of v * (1 / s_y), saturated to +-448, in the
+// low byte.  All round to nearest even.  Each is one or two instructions,
+// so the per-element code stays compact whatever the format.
+__device__ __forceinline__ uint16_t out_bits(float v, int out, float inv_sy) {
+  if (out == OUT_F16) return __half_as_ushort(__float2half_rn(v));
+  if (out == OUT_E4M3)
+    return static_cast<uint16_t>(
+        __nv_cvt_float_to_fp8(__fmul_rn(v, inv_sy), __NV_SATFINITE, __NV_E4M3));
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// The same with the format known at compile time (the decode store loop).
+template <int OUT>
+__device__ __forceinline__ uint16_t out_bits_c(float v, float inv_sy) {
+  if constexpr (OUT == OUT_F16) return __half_as_ushort(__float2half_rn(v));
+  if constexpr (OUT == OUT_E4M3)
+    return static_cast<uint16_t>(
+        __nv_cvt_float_to_fp8(__fmul_rn(v, inv_sy), __NV_SATFINITE, __NV_E4M3));
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// 1 / s_y for E4M3 outputs (the multiply may differ from the division by
+// one float32 ulp of v / s_y, far below the E4M3 step).
+__device__ __forceinline__ float out_scale(const KParams& p) {
+  return p.out == OUT_E4M3 ? __frcp_rn(__ldg(p.s_y)) : 1.0f;
+}
+
+// Store one output element at element index i of Y.
+__device__ __forceinline__ void store_out(const KParams& p, int64_t i, uint16_t bits) {
+  if (p.out == OUT_E4M3)
+    reinterpret_cast<uint8_t*>(p.Y)[i] = static_cast<uint8_t>(bits);
+  else
+    reinterpret_cast<uint16_t*>(p.Y)[i] = bits;
+}
+
+// Store 8 consecutive output elements at element index i (vector path: Y
+// rows 16-byte aligned, i a multiple of 8).
+__device__ __forceinline__ void store_out8(const KParams& p, int64_t i, const uint16_t (&o)[8]) {
+  if (p.out == OUT_E4M3) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      w[h] = static_cast<uint32_t>(o[4 * h] & 0xFF) | (static_cast<uint32_t>(o[4 * h + 1] & 0xFF) << 8) |
+             (static_cast<uint32_t>(o[4 * h + 2] & 0xFF) << 16) |
+             (static_cast<uint32_t>(o[4 * h + 3] & 0xFF) << 24);
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.Y) + i) = make_uint2(w[0], w[1]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      w[h] = static_cast<uint32_t>(o[2 * h]) | (static_cast<uint32_t>(o[2 * h + 1]) << 16);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.Y) + i) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // One output element of the epilogue (float path).  `bias` and `r` are the
 // bf16 inputs already widened; unused ones are ignored by the flags.
 template <int ACT>
@@ -305,20 +366,23 @@ __device__ __forceinline__ float epi_value(float v, float scale, float bias, flo
   return v;
 }
 
-// INT8 epilogue element: exact int32 accumulator -> bf16 bits.
+// INT8 epilogue element: exact int32 accumulator -> output bits (bf16 from
+// the float pair directly; fp16 and E4M3 from its float sum).
 template <int ACT>
 __device__ __forceinline__ uint16_t epi_int8(int32_t acc, float sa, float sw, float bias, float r,
-                                             uint32_t flags) {
+                                             uint32_t flags, int out, float inv_sy) {
+  constexpr int kAct = ACT;
   DF v = df_scale_int(acc, sa, sw);
   if (flags & F_BIAS) v = df_add(v, bias);
   if (flags & F_RES_PRE) {
     v = df_add(v, r);
-    if (ACT != ACT_NONE) v = DF{act_c<ACT>(__fadd_rn(v.hi, v.lo)), 0.0f};
+    if (kAct != ACT_NONE) v = DF{act_c<kAct>(__fadd_rn(v.hi, v.lo)), 0.0f};
   } else {
-    if (ACT != ACT_NONE) v = DF{act_c<ACT>(__fadd_rn(v.hi, v.lo)), 0.0f};
+    if (kAct != ACT_NONE) v = DF{act_c<kAct>(__fadd_rn(v.hi, v.lo)), 0.0f};
     if (flags & F_RES) v = df_add(v, r);
   }
-  return bf16_bits_from_df(v);
+  if (out == OUT_BF16) return bf16_bits_from_df(v);
+  return out_bits(__fadd_rn(v.hi, v.lo), out, inv_sy);
 }
 
 // ------------------------------------------------------------ epilogue ----
@@ -347,12 +411,13 @@ __device__ __forceinline__ void load_swap_inputs(const KParams& p, int n, int co
 
 // Swap-AB epilogue compute and store: lanes of a warp hold consecutive n, so
 // each token's residual loads and Y stores are coalesced across the warp.
-template <int IN, int SC, int CW, int ACT>
-__device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
-                                           const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
+// The output format is a compile-time choice here (store_swap picks it once).
+template <int IN, int SC, int CW, int ACT, int OUT>
+__device__ __forceinline__ void store_swap_o(const KParams& p, int n, int col0,
+                                             const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
   if (n >= p.N) return;
   const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
-  __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y);
+  const float sy = out_scale(p);
   // groups of 8 tokens: the group's loads first, then its arithmetic
   constexpr int G = CW < 8 ? CW : 8;
 #pragma unroll
@@ -370,15 +435,30 @@ __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
       if (m < p.M) {
         uint16_t o;
         if (IN == IN_INT8)
-          o = epi_int8<ACT>(static_cast<int32_t>(vals[g + j]), sa[j], in.sw, in.b, r[j], p.flags);
+          o = epi_int8<ACT>(static_cast<int32_t>(vals[g + j]), sa[j], in.sw, in.b, r[j], p.flags, OUT, sy);
         else
-          o = __bfloat16_as_ushort(__float2bfloat16_rn(
-              epi_value<ACT>(__uint_as_float(vals[g + j]), (SC == SC_TC) ? sa[j] * in.sw : 1.0f,
-                             in.b, r[j], p.flags)));
-        Y[static_cast<int64_t>(m) * p.ldy + n] = __ushort_as_bfloat16(o);
+          o = out_bits_c<OUT>(epi_value<ACT>(__uint_as_float(vals[g + j]),
+                                             (SC == SC_TC) ? sa[j] * in.sw : 1.0f, in.b, r[j], p.flags),
+                              sy);
+        const int64_t at = static_cast<int64_t>(m) * p.ldy + n;
+        if constexpr (OUT == OUT_E4M3)
+          reinterpret_cast<uint8_t*>(p.Y)[at] = static_cast<uint8_t>(o);
+        else
+          reinterpret_cast<uint16_t*>(p.Y)[at] = o;
       }
     }
   }
+}
+
+template <int IN, int SC, int CW, int ACT>
+__device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
+                                           const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
+  if (p.out == OUT_F16)
+    store_swap_o<IN, SC, CW, ACT, OUT_F16>(p, n, col0, vals, in);
+  else if (p.out == OUT_E4M3)
+    store_swap_o<IN, SC, CW, ACT, OUT_E4M3>(p, n, col0, vals, in);
+  else
+    store_swap_o<IN, SC, CW, ACT, OUT_BF16>(p, n, col0, vals, in);
 }
 
 // Apply the epilogue to CW consecutive accumulator columns of one TMEM lane
@@ -402,11 +482,12 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
       return;
     }
     const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
-    __nv_bfloat16* yrow = reinterpret_cast<__nv_bfloat16*>(p.Y) + static_cast<int64_t>(m) * p.ldy;
+    const float sy = out_scale(p);
+    const int64_t yrow = static_cast<int64_t>(m) * p.ldy;  // element index of row m
     const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
     if (p.vec_ok && col0 + CW <= p.N) {
       // full chunk: 16-byte vector loads of bias / R and vector stores of Y
-      uint32_t out[CW / 2];
+      uint16_t out[CW];
 #pragma unroll
       for (int g = 0; g < CW / 8; ++g) {
         uint4 bv = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
@@ -429,20 +510,24 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
             const float b = bf16_to_f(static_cast<uint16_t>(bw[h] >> (16 * e)));
             const float r = bf16_to_f(static_cast<uint16_t>(rw[h] >> (16 * e)));
             if (IN == IN_INT8) {
-              o[e] = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.flags);
+              o[e] = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.flags,
+                                   p.out, sy);
             } else {
               const float s = (SC == SC_TC) ? sa * sws[h * 2 + e] : 1.0f;
-              o[e] = __bfloat16_as_ushort(__float2bfloat16_rn(
-                  epi_value<ACT>(__uint_as_float(vals[j]), s, b, r, p.flags)));
+              o[e] = out_bits(epi_value<ACT>(__uint_as_float(vals[j]), s, b, r, p.flags), p.out, sy);
             }
           }
-          out[g * 4 + h] = static_cast<uint32_t>(o[0]) | (static_cast<uint32_t>(o[1]) << 16);
+          out[g * 8 + h * 2] = o[0];
+          out[g * 8 + h * 2 + 1] = o[1];
         }
       }
 #pragma unroll
-      for (int g = 0; g < CW / 8; ++g)
-        reinterpret_cast<uint4*>(yrow + col0)[g] =
-            make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
+      for (int g = 0; g < CW / 8; ++g) {
+        uint16_t o8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o8[e] = out[g * 8 + e];
+        store_out8(p, yrow + col0 + g * 8, o8);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < CW; ++j) {
@@ -453,12 +538,12 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
         const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
         uint16_t o;
         if (IN == IN_INT8)
-          o = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.flags);
+          o = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.flags, p.out, sy);
         else
-          o = __bfloat16_as_ushort(__float2bfloat16_rn(
-              epi_value<ACT>(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r,
-                             p.flags)));
-        yrow[n] = __ushort_as_bfloat16(o);
+          o = out_bits(epi_value<ACT>(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b,
+                                      r, p.flags),
+                       p.out, sy);
+        store_out(p, yrow + n, o);
       }
     }
   } else {
@@ -874,6 +959,7 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
   const bool debug = (p.flags & F_DEBUG) != 0;
   const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
   const bool has_bias = (p.flags & F_BIAS) != 0;
+  const float sy = out_scale(p);
   constexpr int W = red_row_words(BN);
   for (int c0 = 4 * (ept / R); c0 < cv; c0 += step) {
     float rv[4], cs[4], cb[4];
@@ -917,11 +1003,12 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
       const float bias = SWAP ? in.b : cb[g];
       uint16_t o;
       if (IN == IN_INT8)
-        o = epi_int8<ACT>(static_cast<int32_t>(acc[g]), sa, sw, bias, rv[g], p.flags);
+        o = epi_int8<ACT>(static_cast<int32_t>(acc[g]), sa, sw, bias, rv[g], p.flags, p.out, sy);
       else
-        o = __bfloat16_as_ushort(__float2bfloat16_rn(epi_value<ACT>(
-            __uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f, bias, rv[g], p.flags)));
-      reinterpret_cast<__nv_bfloat16*>(p.Y)[at] = __ushort_as_bfloat16(o);
+        o = out_bits(epi_value<ACT>(__uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f,
+                                    bias, rv[g], p.flags),
+                     p.out, sy);
+      store_out(p, at, o);
     }
   }
   return true;

@@ -32,7 +32,9 @@
  *   if EG_EPI_BIAS:              v += bias[n]
  *   if EG_EPI_RESIDUAL_PRE_ACT:  v += R[m][n]; v = act(v)
  *   else:                        v = act(v); if EG_EPI_RESIDUAL: v += R[m][n]
- *   Y[m][n] = bf16_round_nearest_even(v)
+ *   Y[m][n] = bf16_round_nearest_even(v)   (EG_OUT_F16: fp16; EG_OUT_E4M3: the
+ *             E4M3 code of v / s_y -- the FP32 -> narrow conversion right
+ *             before the store that the fusion page describes)
  *
  * Layouts (all row-major, leading dimensions in ELEMENTS):
  *   A  [M][lda]  activations, K contiguous (bf16, e4m3 or int8 codes)
@@ -123,7 +125,7 @@ enum {
                                    A, s_a, R, bias or s_w and before writing.
                                    Requires that the previous kernel does not
                                    write W. */
-  EG_RUN_QUANT_A = 64           /* E4M3 / INT8 with per-token scales only:
+  EG_RUN_QUANT_A = 64,          /* E4M3 / INT8 with per-token scales only:
                                    eg_args.A holds bf16 activations [M][lda]
                                    (lda in elements); each run first
                                    quantises them per token as
@@ -131,6 +133,14 @@ enum {
                                    scales the plan owns (eg_args.s_a is not
                                    read), then runs the GEMM on them as its
                                    programmatic dependent. */
+  EG_OUT_F16 = 128,             /* Y is fp16 [M][ldy] (nearest even) */
+  EG_OUT_E4M3 = 256             /* Y is E4M3 codes [M][ldy] (one byte each) of
+                                   v / s_y with s_y = *eg_args.s_y (computed
+                                   as v times the float32 reciprocal of s_y,
+                                   nearest even, saturated to +-448).
+                                   EG_OUT_F16, EG_OUT_E4M3 and
+                                   EG_OUT_DEBUG_ACCUM exclude each other; the
+                                   unfused path writes bf16 only. */
 };
 
 typedef struct {
@@ -173,6 +183,7 @@ typedef struct {
   const void* residual;  /* bf16 [M][ldr], needed with a residual flag */
   void* Y;
   int64_t lda, ldw, ldr, ldy;
+  const float* s_y;      /* device float: output scale, needed with EG_OUT_E4M3 */
 } eg_args;
 
 typedef struct eg_plan eg_plan;

@@ -39,11 +39,16 @@ def to_device(p, debug=False, y_pad=0):
     d["s_w"] = None if p.s_w is None else torch.from_numpy(np.ascontiguousarray(p.s_w, np.float32)).cuda()
     d["bias"] = None if p.bias is None else dev_codes(p.bias, "bf16")
     d["residual"] = None if p.residual is None else dev_codes(p.residual, "bf16")
+    out = getattr(p, "out", "bf16")
     if debug:
         dt = torch.int32 if p.dtype == "int8" else torch.float32
         buf = torch.full((p.M * p.N + 2 * y_pad,), -1, dtype=torch.int32, device="cuda").view(dt)
+    elif out == "e4m3":
+        buf = torch.full((p.M * p.N + 2 * y_pad,), 0xFF, dtype=torch.uint8, device="cuda")
     else:
-        buf = torch.full((p.M * p.N + 2 * y_pad,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        buf = torch.full((p.M * p.N + 2 * y_pad,), -1, dtype=torch.int16, device="cuda").view(
+            torch.float16 if out == "f16" else torch.bfloat16)
+    d["s_y"] = torch.tensor([p.s_y], dtype=torch.float32, device="cuda") if out == "e4m3" else None
     d["_ybuf"] = buf
     d["Y"] = buf[y_pad:y_pad + p.M * p.N].view(p.M, p.N)
     d["_pad"] = y_pad
@@ -54,21 +59,25 @@ def canaries_intact(d):
     pad = d["_pad"]
     if pad == 0:
         return True
-    raw = d["_ybuf"].view(torch.int16 if d["_ybuf"].dtype == torch.bfloat16 else torch.int32)
+    b = d["_ybuf"]
+    if b.dtype == torch.uint8:
+        return bool((b[:pad] == 0xFF).all().item() and (b[-pad:] == 0xFF).all().item())
+    raw = b.view(torch.int32 if b.element_size() == 4 else torch.int16)
     return bool((raw[:pad] == -1).all().item() and (raw[-pad:] == -1).all().item())
 
 
 def make_plan(p, tuning=None, debug=False, graph=False):
     return eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
                    residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
-                   debug_accum=debug, graph=graph, tuning=tuning)
+                   debug_accum=debug, graph=graph, tuning=tuning,
+                   out="bf16" if debug else getattr(p, "out", "bf16"))
 
 
 def run(p, tuning=None, debug=False, graph=False, y_pad=64, plan=None, d=None):
     own = plan is None
     plan = plan or make_plan(p, tuning, debug, graph)
     d = d or to_device(p, debug, y_pad)
-    plan.run(d["A"], d["W"], d["Y"], d["s_a"], d["s_w"], d["bias"], d["residual"])
+    plan.run(d["A"], d["W"], d["Y"], d["s_a"], d["s_w"], d["bias"], d["residual"], s_y=d.get("s_y"))
     torch.cuda.synchronize()
     st = plan.device_status()
     assert st == eg.EG_OK, eg.last_error_detail()
@@ -80,7 +89,9 @@ def run(p, tuning=None, debug=False, graph=False, y_pad=64, plan=None, d=None):
 
 
 def bits(y):
-    """torch bf16 tensor -> numpy uint16 bits."""
+    """torch bf16 / fp16 tensor -> numpy uint16 bits (uint8 codes stay codes)."""
+    if y.dtype == torch.uint8:
+        return y.contiguous().numpy()
     return y.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
@@ -122,3 +133,38 @@ def ulp_dist(a_bits, b_bits):
         x = x.astype(np.int64)
         return np.where(x & 0x8000, -(x & 0x7FFF), x)
     return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def f16_ulp(x):
+    """Spacing of fp16 values at |x| (11 significant bits, subnormal floor)."""
+    a = np.abs(x)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return np.exp2(e - 10)
+
+
+def assert_close_out(y, ref, out, rel=1e-2, max_off_frac=1e-2):
+    """The bound for the narrowed outputs.  fp16: as for bf16, per element
+    max(1e-2 * rms, one fp16 ulp of the oracle value).  E4M3 codes: the
+    format's own step is coarser than 1e-2 * rms, so the kernel's code is the
+    oracle's or its neighbour (the float32 epilogue value can sit on the
+    other side of a rounding boundary than the float64 one), neighbours
+    being rare."""
+    if out == "bf16":
+        return assert_close_rms(y, ref, rel)
+    if out == "f16":
+        yv = y.view(np.float16).astype(np.float64)
+        rv = ref.view(np.float16).astype(np.float64)
+        assert np.all(np.isfinite(yv)), "non-finite output"
+        rms = float(np.sqrt(np.mean(rv * rv))) if rv.size else 0.0
+        diff = np.abs(yv - rv)
+        over = diff > rel * rms + 1e-30
+        if over.any():
+            assert np.all(diff[over] <= f16_ulp(rv[over])), f"max err {diff.max():.4g}"
+            assert over.mean() <= 1e-3
+        return
+    def ordered(c):
+        c = c.astype(np.int64)
+        return np.where(c & 0x80, -(c & 0x7F), c)
+    d = np.abs(ordered(y) - ordered(ref))
+    assert d.max() <= 1, f"E4M3 codes {int(d.max())} steps apart"
+    assert (d > 0).mean() <= max_off_frac, f"{int((d > 0).sum())} codes one step off"

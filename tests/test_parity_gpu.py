@@ -13,8 +13,8 @@ import torch
 import epilogue_tcgen05_tmem_gb300 as eg
 import oracle
 from epilogue_tcgen05_tmem_gb300 import inputs
-from tests._gpu_helpers import (assert_close_rms, bits, make_plan, run, to_device,
-                                ulp_dist)
+from tests._gpu_helpers import (assert_close_out, assert_close_rms, bits, make_plan, run,
+                                to_device, ulp_dist)
 
 pytestmark = pytest.mark.gpu
 
@@ -451,3 +451,64 @@ def test_cluster_split_k_rejected_tunings(bad, status):
     with pytest.raises(eg.EgError) as ei:
         eg.Plan(4, 1024, 4096, "e4m3", "token_channel", "silu", bias=True, tuning=t)
     assert ei.value.status == status
+
+
+# ------------------------------------------------ mid-range token counts ---
+
+@pytest.mark.parametrize("wl,M", [("fp8_dynamic", 48), ("fp8_dynamic", 700), ("w8a8_int8", 100),
+                                  ("block_fp8", 300)])
+def test_midrange_tokens_table_entries(wl, M):
+    """Token counts between the decode buckets and the large-M rule use the
+    swept mid-range rows (the first bucket at or above M); sampled outputs
+    at the full layer sizes against the oracle."""
+    p = inputs.workload(wl, M)
+    plan = make_plan(p)
+    assert plan.tuning["swap_ab"] == 0  # the mid-range rows all run rows over M
+    y, _ = run(p, plan=plan)
+    plan.close()
+    _sampled(p, y, npts=1500, int8_ulp=(p.dtype == "int8"))
+
+
+# ------------------------------------------------------ output narrowing ---
+
+OUT_CASES = [
+    # dtype, scale, M, N, K, tuning (None: table / default rule)
+    ("bf16", "none", 64, 256, 512, None),
+    ("bf16", "none", 40, 320, 1024, dict(tile_n=64, stages=4, split_k=3, swap_ab=1)),
+    ("e4m3", "token_channel", 5, 1000, 1024, None),
+    ("e4m3", "token_channel", 16, 2048, 4096, dict(tile_n=16, stages=4, split_k=4, swap_ab=1,
+                                                  cluster_reduce=1)),
+    ("e4m3", "token_channel", 130, 200, 640, dict(tile_n=64, stages=3, split_k=1, swap_ab=0)),
+    ("int8", "token_channel", 7, 256, 1024, None),
+    ("int8", "token_channel", 130, 200, 640, dict(tile_n=64, stages=3, split_k=1, swap_ab=0)),
+    ("e4m3", "block", 8, 384, 1024, None),
+    ("e4m3", "block", 200, 264, 640, dict(tile_n=128, stages=4, split_k=1, swap_ab=0)),
+]
+
+
+@pytest.mark.parametrize("out", ["f16", "e4m3"])
+@pytest.mark.parametrize("dtype,scale,M,N,K,tuning", OUT_CASES)
+def test_output_narrowing(out, dtype, scale, M, N, K, tuning):
+    """fp16 output, and E4M3 output codes of v / s_y (s_y set so that the
+    outputs span most of the E4M3 range), against the oracle."""
+    p = inputs.make_problem(M, N, K, dtype, scale, act="silu", bias=True, residual=True, seed=17)
+    if out == "e4m3":
+        v = (oracle.linear(p).astype(np.uint32) << 16).view(np.float32)   # bf16 output
+        p.s_y = float(np.abs(v).max()) / 200.0
+    p.out = out
+    y, _ = run(p, tuning)
+    assert_close_out(bits(y), oracle.linear(p), out)
+
+
+def test_output_narrowing_rejections():
+    for flags in (eg.EG_OUT_F16 | eg.EG_OUT_E4M3, eg.EG_OUT_F16 | eg.EG_OUT_DEBUG_ACCUM):
+        s, _ = eg.eg_plan_create(eg.make_problem(4, 256, 512, flags=flags))
+        assert s == eg.EG_ERR_INVALID_ARG
+    plan = eg.Plan(4, 256, 512, out="e4m3")
+    A = torch.zeros(4, 512, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(256, 512, dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty(4, 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(eg.EgError) as ei:
+        plan.run(A, W, Y)   # no s_y
+    assert ei.value.status == eg.EG_ERR_INVALID_ARG
+    plan.close()
