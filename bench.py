@@ -395,11 +395,16 @@ def cpu_baseline(base, target_s=10.0):
     nbytes, dt = oracle_sample(base, 256)
     n = int(min(base.N, max(256, 256 * target_s / max(dt, 1e-3))))
     n = max(256, (n // 256) * 256)
-    nbytes, dt = oracle_sample(base, n)
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    # the whole sample, repeated until about target_s seconds of CPU work
+    total_b, total_t, reps = 0, 0.0, 0
+    while total_t < target_s or reps == 0:
+        b, t = oracle_sample(base, n)
+        total_b, total_t, reps = total_b + b, total_t + t, reps + 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
             "sample": f"all 7 token buckets (M=1..32) over the first {n} of {base.N} output "
-                      f"channels, one weight set; {dt:.2f} s",
-            "seconds": round(dt, 3)}
+                      f"channels, one weight set, {reps} passes; {total_t:.2f} s",
+            "seconds": round(total_t, 3)}
 
 
 def run_reference(args):

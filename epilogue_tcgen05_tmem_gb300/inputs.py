@@ -271,3 +271,17 @@ def activations_bf16(M: int, K: int, seed: int = 0, outlier_frac: float = 0.0,
         cols = np.sort(permutation(seed, STREAM_OUTLIER, K)[:nout])
         a[:, cols] *= outlier_mult
     return to_bf16_bits(a)
+
+
+def make_gated_problem(M, N, K, dtype="bf16", scale=None, act="silu", bias=False,
+                       residual=False, seed=0, outlier_frac=0.0) -> Problem:
+    """A gated (SwiGLU when act is SiLU) layer: W [2N, K] holds the gate half
+    then the up half (each quantised per row like any weight), s_w and bias
+    cover the 2N rows; the output and the residual are [M, N]."""
+    p = make_problem(M, 2 * N, K, dtype, scale, act=act, bias=bias, residual=False, seed=seed,
+                     outlier_frac=outlier_frac)
+    p.N = N
+    if residual:
+        p.residual = to_bf16_bits(normal(seed, STREAM_RES, (M, N)))
+    p.meta["gated"] = True
+    return p

@@ -76,6 +76,8 @@ def lib():
             L.orc_accum_splitk.argtypes = [P, vp, vp, vp, vp, ctypes.c_int64,
                                            ctypes.c_int64, vp, vp]
             L.orc_default_threads.argtypes = []
+            L.orc_linear_gated.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
+            L.orc_linear_gated.restype = ctypes.c_int
             L.orc_quant_rows.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int32, vp, ctypes.c_int64, vp]
             L.orc_quant_rows.restype = ctypes.c_int
@@ -234,3 +236,19 @@ def f16_to_double(bits: int) -> float:
 
 def f16_from_double(v: float) -> int:
     return lib().orc_f16_from_double(v)
+
+
+def linear_gated(p, nthreads: int = 0):
+    """Gated output Y [M, N] (bf16 bits, or the format ``p.out`` names) of a
+    problem whose W holds 2N rows (gate half, then up half); ``p.N`` is the
+    output width N, s_w / bias cover the 2N rows."""
+    A, W, sa, sw, b, r = _arrays(p)
+    Y = np.zeros((p.M, p.N), np.uint16)
+    pr = _problem(p, _flags(p))
+    rc = lib().orc_linear_gated(ctypes.byref(pr), _ptr(A), _ptr(W), _ptr(sa), _ptr(sw),
+                                _ptr(b), _ptr(r), _ptr(Y), nthreads)
+    if rc:
+        raise ValueError("oracle rejected the gated problem")
+    if getattr(p, "out", "bf16") == "e4m3":
+        Y = Y.astype(np.uint8)
+    return Y

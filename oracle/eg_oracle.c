@@ -476,3 +476,52 @@ uint16_t orc_f16_from_double(double v) {
   const int mant = (int)((fr * 2.0 - 1.0) * 1024.0);
   return sign | (uint16_t)((exp_field << 10) | mant);
 }
+
+
+/* ---------------------------------------------------------------------- */
+/* Gated linear unit over the two W halves.                                */
+
+static uint16_t round_out(const orc_problem* p, double v) {
+  if (p->flags & ORC_OUT_F16) return orc_f16_from_double(v);
+  if (p->flags & ORC_OUT_E4M3) return orc_e4m3_from_double(v / (double)p->s_y);
+  return orc_bf16_from_double(v);
+}
+
+int orc_linear_gated(const orc_problem* p, const void* A, const void* W, const float* sa,
+                     const float* sw, const uint16_t* bias, const uint16_t* R, uint16_t* Y,
+                     int nthreads) {
+  if (!p || (p->flags & ORC_RESIDUAL_PRE_ACT)) return -1;
+  if ((p->flags & ORC_BIAS) && !bias) return -1;
+  if ((p->flags & ORC_RESIDUAL) && !R) return -1;
+  if (p->scale == ORC_SCALE_BLOCK && p->N % 128) return -1;
+  const int64_t M = p->M, N = p->N;
+  if (M == 0 || N == 0) return 0;
+  /* the accumulators of all 2N weight rows, from the plain accumulation */
+  orc_problem inner = *p;
+  inner.N = 2 * N;
+  inner.flags = 0;
+  inner.act = ORC_ACT_NONE;
+  double* acc = (double*)malloc(sizeof(double) * (size_t)(M * 2 * N));
+  if (!acc) return -1;
+  int rc = orc_linear(&inner, A, W, sa, sw, NULL, NULL, NULL, acc, NULL, nthreads);
+  if (rc == 0) {
+    for (int64_t m = 0; m < M; m++) {
+      for (int64_t n = 0; n < N; n++) {
+        double g = acc[m * 2 * N + n], u = acc[m * 2 * N + N + n];
+        if (p->scale == ORC_SCALE_TOKEN_CHANNEL) {
+          g = g * ((double)sa[m] * (double)sw[n]);
+          u = u * ((double)sa[m] * (double)sw[N + n]);
+        }
+        if (p->flags & ORC_BIAS) {
+          g = g + orc_bf16_to_double(bias[n]);
+          u = u + orc_bf16_to_double(bias[N + n]);
+        }
+        double y = orc_act(p->act, g) * u;
+        if (p->flags & ORC_RESIDUAL) y = y + orc_bf16_to_double(R[m * N + n]);
+        Y[m * N + n] = round_out(p, y);
+      }
+    }
+  }
+  free(acc);
+  return rc;
+}

@@ -110,6 +110,20 @@ int orc_accum_splitk(const orc_problem* p, const void* A, const void* W,
 /* Number of worker threads orc_linear uses for nthreads <= 0. */
 int orc_default_threads(void);
 
+/* Gated linear unit (the SwiGLU epilogue when act is SiLU): W holds 2N rows,
+ * the gate half [0, N) and the up half [N, 2N) ("two W halves"); s_w (token/
+ * channel) has 2N entries, or 2N/128 block rows (block scaling); bias has 2N
+ * entries.  With acc = A . W^T over all 2N rows (the accumulation of
+ * orc_linear), per output (m, n), n < N:
+ *   g = scale(acc[m][n]) + bias[n],  u = scale(acc[m][N + n]) + bias[N + n]
+ *   y = act(g) * u;  y += R[m][n] (ORC_RESIDUAL);  Y[m][n] = round(y)
+ * where scale() is the token/channel scaling (sa[m] * sw[row]) or nothing
+ * (bf16, block: already scaled), and round() follows the output flags.
+ * ORC_RESIDUAL_PRE_ACT is rejected.  Returns 0 or -1. */
+int orc_linear_gated(const orc_problem* p, const void* A, const void* W, const float* sa,
+                     const float* sw, const uint16_t* bias, const uint16_t* R, uint16_t* Y,
+                     int nthreads);
+
 /* Dynamic per-token quantisation of activations (the prologue transform
  * that precedes the FP8_Dynamic and W8A8_INT8 layers; "Helion linear backend
  * in vLLM", section "One kernel instead of three", scale formats, and

@@ -537,3 +537,58 @@ def test_output_format_flags_rejected_together():
     import ctypes
     assert oracle.lib().orc_linear(ctypes.byref(pr), oracle._ptr(A), oracle._ptr(W), None, None,
                                    None, None, oracle._ptr(Y), None, None, 1) == -1
+
+
+# ------------------------------------------------ gated linear unit (SwiGLU) ---
+
+def test_gated_zero_weights_is_act_of_bias_times_bias():
+    """W = 0: g = bias[n], u = bias[N + n], so y = act(bias_g) * bias_u (+ R)."""
+    p = inputs.make_gated_problem(3, 40, 64, "bf16", act="silu", bias=True, residual=True, seed=2)
+    p.W = np.zeros_like(p.W)
+    y = oracle.linear_gated(p)
+    bg = np.array([oracle.bf16_to_double(int(b)) for b in p.bias[:40]])
+    bu = np.array([oracle.bf16_to_double(int(b)) for b in p.bias[40:]])
+    r = np.array([[oracle.bf16_to_double(int(v)) for v in row] for row in p.residual])
+    want = np.array([[oracle.bf16_from_double(oracle.act("silu", bg[n]) * bu[n] + r[m, n])
+                      for n in range(40)] for m in range(3)], np.uint16)
+    assert np.array_equal(y, want)
+
+
+def test_gated_scales_pick_each_half():
+    """A = W = 1 with distinct per-row weight scales: g = K sa sw[n],
+    u = K sa sw[N + n]; a halves mix-up changes the result."""
+    M, N, K = 2, 3, 128
+    p = inputs.make_gated_problem(M, N, K, "e4m3", "token_channel", act="silu", seed=3)
+    p.A = np.full((M, K), 0x38, np.uint8)
+    p.W = np.full((2 * N, K), 0x38, np.uint8)
+    p.s_a = np.array([1.0, 0.5], np.float32)
+    p.s_w = np.array([0.01, 0.02, -0.03, 0.2, 0.3, 0.4], np.float32)
+    y = oracle.linear_gated(p)
+    for m in range(M):
+        for n in range(N):
+            g = K * float(p.s_a[m]) * float(p.s_w[n])
+            u = K * float(p.s_a[m]) * float(p.s_w[N + n])
+            assert y[m, n] == oracle.bf16_from_double(oracle.act("silu", g) * u)
+
+
+def test_gated_halves_not_swapped():
+    """A strongly negative gate closes the unit (g = -80: y ~ -4e-33),
+    whereas the swapped unit would give silu(2.5) * (-80) ~ -186."""
+    M, N, K = 1, 1, 128
+    p = inputs.make_gated_problem(M, N, K, "bf16", act="silu", seed=4)
+    one = np.uint16(0x3F80)  # bf16 1.0
+    p.A = np.full((M, K), one, np.uint16)
+    p.W = np.zeros((2, K), np.uint16)
+    p.W[0, :] = np.uint16(0xBF20)  # -0.625 * 128 = -80 -> gate
+    p.W[1, :] = np.uint16(0x3CA0)  # 0.01953125 * 128 = 2.5 -> up
+    y = oracle.linear_gated(p)
+    v = oracle.bf16_to_double(int(y[0, 0]))
+    assert y[0, 0] == oracle.bf16_from_double(oracle.act("silu", -80.0) * 2.5)
+    assert abs(v) < 1e-20 and abs(oracle.act("silu", 2.5) * -80.0) > 100
+
+
+def test_gated_rejects_pre_activation_residual():
+    p = inputs.make_gated_problem(2, 8, 64, "bf16", act="silu", residual=True, seed=5)
+    p.residual_pre_act = True
+    with pytest.raises(ValueError):
+        oracle.linear_gated(p)
