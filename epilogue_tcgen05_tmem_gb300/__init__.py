@@ -27,7 +27,8 @@ DTYPES = {"bf16": 0, "e4m3": 1, "int8": 2}
 SCALES = {"none": 0, "token_channel": 1, "block": 2}
 ACTS = {"none": 0, "relu": 1, "gelu_erf": 2, "gelu_tanh": 3, "silu": 4}
 EG_EPI_BIAS, EG_EPI_RESIDUAL, EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM, EG_RUN_GRAPH, \
-    EG_RUN_PDL, EG_RUN_QUANT_A, EG_OUT_F16, EG_OUT_E4M3 = 1, 2, 4, 8, 16, 32, 64, 128, 256
+    EG_RUN_PDL, EG_RUN_QUANT_A, EG_OUT_F16, EG_OUT_E4M3, EG_EPI_GATED = \
+    1, 2, 4, 8, 16, 32, 64, 128, 256, 512
 OUTS = {"bf16": 0, "f16": EG_OUT_F16, "e4m3": EG_OUT_E4M3}
 
 EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "eg_plan_run",
@@ -234,12 +235,14 @@ class Plan:
     bf16, Y [M,N] bf16 (float32/int32 in debug mode; ``out="f16"``: fp16;
     ``out="e4m3"``: uint8 codes of v / s_y, s_y a one-element float32
     tensor).  With ``quant_a`` A is bf16 and each run quantises it per token
-    first (s_a is not used).
+    first (s_a is not used).  With ``gated`` (SwiGLU when act is silu) W is
+    [2N, K], gate half then up half, and s_w / bias cover the 2N rows.
     """
 
     def __init__(self, M, N, K, dtype="bf16", scale="none", act="none", bias=False,
                  residual=False, residual_pre_act=False, debug_accum=False, graph=False,
-                 pdl=False, tuning: dict | None = None, quant_a=False, out="bf16"):
+                 pdl=False, tuning: dict | None = None, quant_a=False, out="bf16",
+                 gated=False):
         flags = 0
         if bias:
             flags |= EG_EPI_BIAS
@@ -254,6 +257,8 @@ class Plan:
         if quant_a:
             flags |= EG_RUN_QUANT_A
         flags |= OUTS[out]
+        if gated:
+            flags |= EG_EPI_GATED
         self.problem = make_problem(M, N, K, dtype, scale, act, flags)
         t = make_tuning(**tuning) if tuning is not None else None
         s, h = eg_plan_create(self.problem, t)

@@ -159,11 +159,21 @@ eg_status validate_problem(const eg_problem* p) {
     return fail(EG_ERR_INVALID_ARG, "unknown activation %d", p->act);
   const uint32_t known =
       EG_EPI_BIAS | EG_EPI_RESIDUAL | EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM | EG_RUN_GRAPH |
-      EG_RUN_PDL | EG_RUN_QUANT_A | EG_OUT_F16 | EG_OUT_E4M3;
+      EG_RUN_PDL | EG_RUN_QUANT_A | EG_OUT_F16 | EG_OUT_E4M3 | EG_EPI_GATED;
   if (p->flags & ~known) return fail(EG_ERR_INVALID_ARG, "unknown flag bits 0x%x", p->flags);
   const uint32_t outs = p->flags & (EG_OUT_F16 | EG_OUT_E4M3 | EG_OUT_DEBUG_ACCUM);
   if (outs & (outs - 1))
     return fail(EG_ERR_INVALID_ARG, "EG_OUT_F16, EG_OUT_E4M3 and EG_OUT_DEBUG_ACCUM exclude each other");
+  if (p->flags & EG_EPI_GATED) {
+    const bool ok_in = p->scale == EG_SCALE_NONE ||
+                       (p->dtype == EG_IN_E4M3 && p->scale == EG_SCALE_TOKEN_CHANNEL);
+    if (!ok_in)
+      return fail(EG_ERR_UNSUPPORTED, "gated units take bf16 or E4M3 per-token/per-channel inputs");
+    if (p->flags & (EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM))
+      return fail(EG_ERR_INVALID_ARG,
+                  "EG_EPI_GATED excludes EG_EPI_RESIDUAL_PRE_ACT and EG_OUT_DEBUG_ACCUM");
+    if (p->N > INT32_MAX / 2) return fail(EG_ERR_UNSUPPORTED, "2N must fit in int32");
+  }
   if ((p->flags & EG_RUN_QUANT_A) &&
       !((p->dtype == EG_IN_E4M3 || p->dtype == EG_IN_INT8) && p->scale == EG_SCALE_TOKEN_CHANNEL))
     return fail(EG_ERR_INVALID_ARG, "EG_RUN_QUANT_A needs E4M3 or INT8 inputs with per-token scales");
@@ -178,6 +188,12 @@ eg_status validate_problem(const eg_problem* p) {
 }
 
 bool lookup_kernel(const eg_problem& p, int swap, int bn, eg::KernelEntry* ke) {
+  if (p.flags & EG_EPI_GATED) {
+    if (p.dtype == EG_IN_BF16) return eg::lookup_bf16_gated(swap, bn, ke);
+    if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
+      return eg::lookup_e4m3_tc_gated(swap, bn, ke);
+    return false;
+  }
   if (p.dtype == EG_IN_BF16) return eg::lookup_bf16(swap, bn, ke);
   if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
     return eg::lookup_e4m3_tc(swap, bn, ke);
@@ -207,6 +223,8 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
     return fail(EG_ERR_UNSUPPORTED, "stages must be in 2..8 (got %d)", t.stages);
   if (t.cluster_reduce != 0 && t.cluster_reduce != 1)
     return fail(EG_ERR_INVALID_ARG, "cluster_reduce must be 0 or 1");
+  if (t.cluster_reduce && (p.flags & EG_EPI_GATED))
+    return fail(EG_ERR_UNSUPPORTED, "gated units reduce split-K through the workspace (cluster_reduce 0)");
   if (t.cluster_reduce) {
     if (t.split_k != 2 && t.split_k != 4 && t.split_k != 8)
       return fail(EG_ERR_UNSUPPORTED, "cluster_reduce needs split_k in {2, 4, 8} (got %d)", t.split_k);
@@ -381,7 +399,8 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
   const size_t ybytes = size_t(p.M - 1) * size_t(a->ldy) * esz + size_t(p.N) * esz;
   const int ab = quant_a ? 2 : eb;
   if (overlaps(a->Y, ybytes, a->A, size_t(p.M - 1) * a->lda * ab + size_t(p.K) * ab) ||
-      overlaps(a->Y, ybytes, a->W, size_t(p.N - 1) * a->ldw * eb + size_t(p.K) * eb) ||
+      overlaps(a->Y, ybytes, a->W,
+               size_t((p.flags & EG_EPI_GATED) ? 2 * p.N - 1 : p.N - 1) * a->ldw * eb + size_t(p.K) * eb) ||
       (res && !debug_out &&
        overlaps(a->Y, ybytes, a->residual, size_t(p.M - 1) * a->ldr * 2 + size_t(p.N) * 2)))
     return fail(EG_ERR_INVALID_ARG, "Y must not alias A, W or the residual");
@@ -400,7 +419,8 @@ eg_status ensure_maps(eg_plan* pl, const eg_args* a) {
   eg_status s;
   const bool swap = pl->tune.swap_ab != 0;
   if ((s = encode_map(&mA, a->A, p.dtype, p.M, p.K, a->lda, box_k, swap ? bn : 128)) != EG_OK) return s;
-  if ((s = encode_map(&mW, a->W, p.dtype, p.N, p.K, a->ldw, box_k, swap ? 128 : bn)) != EG_OK) return s;
+  const int64_t wrows = (p.flags & EG_EPI_GATED) ? 2 * p.N : p.N;  // gated: gate + up halves
+  if ((s = encode_map(&mW, a->W, p.dtype, wrows, p.K, a->ldw, box_k, swap ? 128 : bn)) != EG_OK) return s;
   pl->tmP = swap ? mW : mA;
   pl->tmQ = swap ? mA : mW;
   pl->mapA = a->A;
@@ -671,7 +691,7 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   plan_grid(pl, sm_count_of(dev), per_sm);
   const size_t tiles = size_t(pl->tiles_rows) * pl->tiles_cols;
   if (pl->max_contrib > 1 && tiles > 0) {
-    pl->ws_bytes = size_t(pl->max_contrib) * tiles * size_t(t.tile_n) * 128 * 4;
+    pl->ws_bytes = size_t(pl->max_contrib) * tiles * size_t(ke.acc_n) * 128 * 4;
     if ((e = cudaMalloc(&pl->ws, pl->ws_bytes)) != cudaSuccess)
       return cleanup(cuda_fail(e, "allocating the split-K workspace"));
     // INT8 accumulates its splits into slot 0 of each tile, which the kernel
@@ -816,6 +836,8 @@ eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1, void
     return fail(EG_ERR_UNSUPPORTED, "the unfused path takes quantised A (no EG_RUN_QUANT_A)");
   if (p.flags & (EG_OUT_F16 | EG_OUT_E4M3))
     return fail(EG_ERR_UNSUPPORTED, "the unfused path writes bf16 only");
+  if (p.flags & EG_EPI_GATED)
+    return fail(EG_ERR_UNSUPPORTED, "the unfused path has no gated unit");
   eg_status s = validate_args(plan, args, false);
   if (s != EG_OK) return s;
   plan->last_launches = 0;
@@ -974,7 +996,8 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   int per_sm = 0;
   if ((s = residency(&pl, dev, &per_sm)) != EG_OK) return s;
   plan_grid(&pl, sm_count_of(dev), per_sm);
-  const size_t ws_need = pl.max_contrib > 1 ? size_t(pl.max_contrib) * tiles * size_t(t.tile_n) * 128 * 4 : 0;
+  const size_t ws_need =
+      pl.max_contrib > 1 ? size_t(pl.max_contrib) * tiles * size_t(pl.ke.acc_n) * 128 * 4 : 0;
   if (tiles > kScratchCounters || ws_need > kScratchWorkspaceBytes)
     return fail(EG_ERR_UNSUPPORTED,
                 "problem needs %zu tile counters and %zu bytes of split-K scratch; "
@@ -997,7 +1020,7 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   EG_CUDA(cudaMemsetAsync(pl.status, 0, sizeof(int), st), "clearing the status word");
   // INT8 split-K adds every split into one zeroed slot per tile
   if (p.dtype == EG_IN_INT8 && pl.max_contrib > 1)
-    EG_CUDA(cudaMemsetAsync(pl.ws, 0, tiles * size_t(t.tile_n) * 128 * 4, st),
+    EG_CUDA(cudaMemsetAsync(pl.ws, 0, tiles * size_t(pl.ke.acc_n) * 128 * 4, st),
             "clearing the INT8 split-K sums");
   if ((s = ensure_maps(&pl, args)) != EG_OK) return s;
   const eg::KParams kp = make_params(&pl, args, p.act, epi_flags(p.flags), args->Y, args->ldy);

@@ -48,6 +48,7 @@ enum : int { IN_BF16 = 0, IN_E4M3 = 1, IN_INT8 = 2 };
 enum : int { SC_NONE = 0, SC_TC = 1, SC_BLOCK = 2 };
 enum : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU_ERF = 2, ACT_GELU_TANH = 3, ACT_SILU = 4 };
 enum : uint32_t { F_BIAS = 1, F_RES = 2, F_RES_PRE = 4, F_DEBUG = 8 };
+// (gated units are a compile-time variant of the kernel, G below)
 // Output element formats: bf16, fp16, or the E4M3 code of v / s_y.
 enum : int { OUT_BF16 = 0, OUT_F16 = 1, OUT_E4M3 = 2 };
 // Device status codes (first failure wins).
@@ -99,7 +100,11 @@ __device__ __forceinline__ void trace_point(const KParams& p, int point) {
     p.trace[static_cast<int64_t>(blockIdx.x) * kTracePoints + point] = global_timer_ns();
 }
 
-template <int IN, int SC, bool SWAP, int BN>
+// G: gated linear unit (SwiGLU with SiLU).  W holds 2N rows, the gate half
+// then the up half; each stage also carries the up half's weight tile and
+// UMMA fills two accumulators per unit, gate in columns [0, BN) and up in
+// [BN, 2 BN).
+template <int IN, int SC, bool SWAP, int BN, bool G = false>
 struct Cfg {
   static constexpr bool kConvert = (IN == IN_INT8);
   static constexpr bool kPromote = (SC == SC_BLOCK) || kConvert;
@@ -114,10 +119,13 @@ struct Cfg {
   // operand, two buffers of 64 columns) and Q into fp16 in a 2-slot shared
   // ring, so the int8 ring can be deep while the fp16 operands stay small
   // and shared memory carries the conversion's traffic for Q only.
-  static constexpr uint32_t kStageBytes = kConvert ? kP8Bytes + kQ8Bytes : kPBytes + kQBytes;
+  static constexpr uint32_t kWBytes = SWAP ? kPBytes : kQBytes;  // one weight operand tile
+  static constexpr uint32_t kStageBytes =
+      kConvert ? kP8Bytes + kQ8Bytes : kPBytes + kQBytes + (G ? kWBytes : 0u);
   static constexpr int kOpSlots = 2;
   static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * kQBytes : 0u;
-  static constexpr uint32_t kTxBytes = (128u + BN) * 128u;  // bytes one stage's TMA delivers
+  static constexpr uint32_t kTxBytes =  // bytes one stage's TMA delivers
+      (128u + BN) * 128u + (G ? (SWAP ? 128u : uint32_t(BN)) * 128u : 0u);
   // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for block-scale
   // promotion of wide tiles (two column halves per quarter, so each thread
   // keeps BN/2 running sums and the promotion keeps up with UMMA).
@@ -130,9 +138,12 @@ struct Cfg {
   // Decode tiles (BN 16) keep a third slot per SM free so that the next
   // call's CTAs (programmatic dependents) become resident while this grid
   // still runs.
+  // Gated units hold twice the accumulator values in the epilogue: two
+  // CTAs per SM for decode tiles.
   static constexpr int kMinBlocks =
-      kConvert ? (BN <= 16 ? 2 : 1)
-               : ((kPromote && BN >= 64) || BN >= 128) ? 1 : (BN <= 32 ? 3 : 2);
+      G ? (BN <= 32 ? 2 : 1)
+        : kConvert ? (BN <= 16 ? 2 : 1)
+                   : ((kPromote && BN >= 64) || BN >= 128) ? 1 : (BN <= 32 ? 3 : 2);
   // Register cap per thread for that residency.  The SM's 64K registers are
   // split over its 4 sub-partitions (16K each) and warps are spread over
   // them, so the busiest sub-partition holds ceil(warps / 4) warps of
@@ -145,7 +156,8 @@ struct Cfg {
   // TMEM accumulator buffers: 2 (one unit drains while the next fills), or
   // 4 when promoting K blocks so UMMA runs further ahead of the epilogue
   static constexpr int kAccBufs = (kPromote && 4 * BN <= 512) ? 4 : 2;
-  static constexpr uint32_t kAccCols = kAccBufs * BN;
+  static constexpr int kAccN = G ? 2 * BN : BN;  // accumulator columns of one unit
+  static constexpr uint32_t kAccCols = kAccBufs * kAccN;
   static constexpr uint32_t kTmemACols = kConvert ? kOpSlots * 64u : 0u;  // fp16 P, 128 K each
   static constexpr uint32_t kTmemUsed = kAccCols + kTmemACols;
   static constexpr uint32_t kTmemCols =
@@ -156,11 +168,12 @@ struct Cfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(!kPromote || BN <= 128, "promotion keeps BN fp32 values per thread");
   static_assert(kTmemUsed <= 512, "tensor memory holds 512 columns");
+  static_assert(!G || !kPromote, "gated units use the tensor-memory accumulator path");
 };
 
-template <int IN, int SC, bool SWAP, int BN>
+template <int IN, int SC, bool SWAP, int BN, bool G = false>
 constexpr uint32_t smem_bytes_for(int stages) {
-  using C = Cfg<IN, SC, SWAP, BN>;
+  using C = Cfg<IN, SC, SWAP, BN, G>;
   return 1024u + uint32_t(stages) * C::kStageBytes + C::kOpBytes + 512u;
 }
 
@@ -570,6 +583,78 @@ template <int IN, int SC, bool SWAP, int CW>
 __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int col0,
                                                const uint32_t (&vals)[CW]) {
   EG_ACT_DISPATCH(p.act, (epilogue_chunk_a<IN, SC, SWAP, CW, A_>(p, row, col0, vals)))
+}
+
+// Gated unit epilogue of CW consecutive accumulator columns of one TMEM lane:
+// gate values g and up values u (fp32 bits).  Per output (m, n):
+// gate = scale(g) + bias[n], up = scale(u) + bias[N + n] (scale: s_a[m] *
+// s_w[n] and s_a[m] * s_w[N + n]), y = act(gate) * up (+ R[m][n]), one
+// narrowing, one store.  Rows over N (swap-AB: row = n, columns = tokens)
+// or over M (row = m, columns = n).
+template <int SC, bool SWAP, int CW, int ACT>
+__device__ __forceinline__ void epilogue_gated_a(const KParams& p, int row, int col0,
+                                                 const uint32_t (&g)[CW], const uint32_t (&u)[CW]) {
+  const bool has_bias = (p.flags & F_BIAS) != 0;
+  const bool has_res = (p.flags & F_RES) != 0;
+  const float sy = out_scale(p);
+  if (SWAP ? row >= p.N : row >= p.M) return;
+  float rsg = 1.0f, rsu = 1.0f, rbg = 0.0f, rbu = 0.0f;  // per-row inputs
+  if (SWAP) {
+    if (SC == SC_TC) { rsg = __ldg(p.s_w + row); rsu = __ldg(p.s_w + p.N + row); }
+    if (has_bias) { rbg = __bfloat162float(p.bias[row]); rbu = __bfloat162float(p.bias[p.N + row]); }
+  } else if (SC == SC_TC) {
+    rsg = rsu = __ldg(p.s_a + row);
+  }
+  constexpr int GR = CW < 8 ? CW : 8;
+#pragma unroll
+  for (int c0 = 0; c0 < CW; c0 += GR) {
+    float sg[GR], su[GR], bg[GR], bu[GR], rr[GR];
+#pragma unroll
+    for (int j = 0; j < GR; ++j) {
+      const int col = col0 + c0 + j;
+      const bool ok = SWAP ? col < p.M : col < p.N;
+      const int m = SWAP ? col : row, n = SWAP ? row : col;
+      sg[j] = su[j] = 1.0f;
+      bg[j] = rbg;
+      bu[j] = rbu;
+      if (ok && SC == SC_TC) {
+        if (SWAP) {
+          const float sa = __ldg(p.s_a + col);
+          sg[j] = sa * rsg;
+          su[j] = sa * rsu;
+        } else {
+          sg[j] = rsg * __ldg(p.s_w + col);
+          su[j] = rsu * __ldg(p.s_w + p.N + col);
+        }
+      }
+      if (ok && !SWAP && has_bias) {
+        bg[j] = __bfloat162float(p.bias[col]);
+        bu[j] = __bfloat162float(p.bias[p.N + col]);
+      }
+      rr[j] = (ok && has_res) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < GR; ++j) {
+      const int col = col0 + c0 + j;
+      if (SWAP ? col >= p.M : col >= p.N) break;
+      const int m = SWAP ? col : row, n = SWAP ? row : col;
+      float gv = __uint_as_float(g[c0 + j]) * sg[j];
+      float uv = __uint_as_float(u[c0 + j]) * su[j];
+      if (has_bias) {
+        gv += bg[j];
+        uv += bu[j];
+      }
+      float y = act_c<ACT>(gv) * uv;
+      if (has_res) y += rr[j];
+      store_out(p, static_cast<int64_t>(m) * p.ldy + n, out_bits(y, p.out, sy));
+    }
+  }
+}
+
+template <int SC, bool SWAP, int CW>
+__device__ __forceinline__ void epilogue_gated(const KParams& p, int row, int col0,
+                                               const uint32_t (&g)[CW], const uint32_t (&u)[CW]) {
+  EG_ACT_DISPATCH(p.act, (epilogue_gated_a<SC, SWAP, CW, A_>(p, row, col0, g, u)))
 }
 
 template <int CW>
@@ -1020,12 +1105,12 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
 // TMEM accumulator buffers and promotion buffers carry their phases across
 // units, so the epilogue of one unit overlaps the UMMA mainloop of the next.
 
-template <int IN, int SC, bool SWAP, int BN>
-__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
-    __maxnreg__((Cfg<IN, SC, SWAP, BN>::kMaxRegs))
+template <int IN, int SC, bool SWAP, int BN, bool G = false>
+__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
+    __maxnreg__((Cfg<IN, SC, SWAP, BN, G>::kMaxRegs))
     fused_linear_kernel(const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmQ, const KParams p) {
-  using C = Cfg<IN, SC, SWAP, BN>;
+  using C = Cfg<IN, SC, SWAP, BN, G>;
   constexpr int CW = C::kCW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1128,6 +1213,16 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           tma_load_2d_hint(dst, map, &full[s], kx, y, pol_first);
         else
           tma_load_2d(dst, map, &full[s], kx, y);
+        if constexpr (G) {
+          // gated: the up half's tile, N weight rows further, after P and Q
+          if (weight) {
+            uint8_t* dst2 = base + C::kPBytes + C::kQBytes;
+            if (isP ? p.evict_first_p : p.evict_first_q)
+              tma_load_2d_hint(dst2, map, &full[s], kx, y + p.N, pol_first);
+            else
+              tma_load_2d(dst2, map, &full[s], kx, y + p.N);
+          }
+        }
       };
       uint32_t g = 0;  // ring iteration across units
       bool first = true;
@@ -1149,8 +1244,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           if (p.pdl && p.l2_prefetch) {
             const CUtensorMap* wmap = SWAP ? &tmP : &tmQ;
             const int wy = SWAP ? w.row0 : w.col0;
-            for (int i = pre; i < w.nk; ++i)
+            for (int i = pre; i < w.nk; ++i) {
               tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy);
+              if constexpr (G) tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy + p.N);
+            }
           }
           griddep_wait();
           for (int i = 0; i < pre; ++i) load_op(false, w, i, i);
@@ -1209,7 +1306,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
           }
           tc_fence_after();
           if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
-          const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(b * C::kAccN);
           const uint32_t pa = smem_u32(op_base(g));
           const uint32_t qa = C::kConvert ? pa : pa + C::kPBytes;
           // INT8: P is in tensor memory, buffer os, 8 columns per K step of 16
@@ -1228,6 +1325,17 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
                   umma_f8(d, ad, bd, C::kIdesc, accum);
                 else
                   umma_f16(d, ad, bd, C::kIdesc, accum);
+                if constexpr (G) {
+                  // up half: its weight tile replaces the gate's, same
+                  // activation tile, accumulator columns [BN, 2 BN)
+                  const uint32_t wa = pa + C::kPBytes + C::kQBytes;
+                  const uint64_t ad2 = SWAP ? sdesc_k_sw128(wa + 32u * k) : ad;
+                  const uint64_t bd2 = SWAP ? bd : sdesc_k_sw128(wa + 32u * k);
+                  if (IN == IN_E4M3)
+                    umma_f8(d + BN, ad2, bd2, C::kIdesc, accum);
+                  else
+                    umma_f16(d + BN, ad2, bd2, C::kIdesc, accum);
+                }
               }
             }
           }
@@ -1447,10 +1555,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
       } else {
         // ---- accumulator in TMEM buffer blk&1 until the unit is done ----
         const int b = blk % NB;
-        const uint32_t tb = t_lane + static_cast<uint32_t>(b * BN);
+        const uint32_t tb = t_lane + static_cast<uint32_t>(b * C::kAccN);
         // swap-AB with one chunk (decode): epilogue inputs load while the
         // mainloop runs
-        constexpr bool kPre = SWAP && BN == CW;
+        constexpr bool kPre = SWAP && BN == CW && !G;
         SwapIn<CW> pre;
         if constexpr (kPre) {
           if (!(p.flags & F_DEBUG) && !p.cluster_reduce) load_swap_inputs<SC, CW>(p, row, w.col0, pre);
@@ -1498,15 +1606,17 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
         }
         bool do_epi = true;
         if (w.contrib > 1) {
+          // every accumulator column of the unit (gated: gate, then up)
 #pragma unroll 1
-          for (int c = 0; c < BN; c += CW) {
+          for (int c = 0; c < C::kAccN; c += CW) {
             uint32_t r[CW];
             tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
             tmem_ld_wait();
-            uint32_t* wsb = ws_slot<BN>(p, w.j, w.tile, c, lane_row);  // column stride 128
+            uint32_t* wsb = ws_slot<C::kAccN>(p, w.j, w.tile, c, lane_row);  // column stride 128
+            const int ct = c % BN;  // the chunk's first output column in the tile
 #pragma unroll
             for (int j = 0; j < CW; ++j)
-              if (row < p.rows && w.col0 + c + j < p.cols) __stcg(wsb + j * 128, r[j]);
+              if (row < p.rows && w.col0 + ct + j < p.cols) __stcg(wsb + j * 128, r[j]);
           }
           do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
         }
@@ -1525,8 +1635,24 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN>::kThreads)
               // partials summed in split order 0..S-1 (deterministic; this
               // CTA's own one is read back too); per split, the chunk's loads
               // are independent and overlap
-              reduce_partials<IN, BN, CW>(p, w.tile, w.contrib, c, lane_row, row < p.rows,
-                                          p.cols - (w.col0 + c), r);
+              reduce_partials<IN, C::kAccN, CW>(p, w.tile, w.contrib, c, lane_row, row < p.rows,
+                                                p.cols - (w.col0 + c), r);
+            }
+            if constexpr (G) {
+              // the up half's columns of the same outputs
+              uint32_t u[CW];
+              if (w.nk > 0) {
+                tmem_load_chunk<CW>(tb + static_cast<uint32_t>(BN + c), u);
+                tmem_ld_wait();
+              } else {
+#pragma unroll
+                for (int j = 0; j < CW; ++j) u[j] = 0u;
+              }
+              if (w.contrib > 1)
+                reduce_partials<IN, C::kAccN, CW>(p, w.tile, w.contrib, BN + c, lane_row,
+                                                  row < p.rows, p.cols - (w.col0 + c), u);
+              epilogue_gated<SC, SWAP, CW>(p, row, w.col0 + c, r, u);
+              continue;
             }
             if constexpr (kPre) {
               if (!(p.flags & F_DEBUG)) {

@@ -12,6 +12,7 @@ struct KernelEntry {
   int threads = 0;
   int elems_per_stage = 0;       // K elements one stage covers
   int tmem_cols = 0;             // TMEM columns one CTA allocates
+  int acc_n = 0;                 // accumulator columns per unit (gated: 2 tile_n)
 };
 
 // Each returns false when bn has no instantiation for that kind and swap.
@@ -25,20 +26,24 @@ EG_DECLARE_LOOKUP(lookup_bf16)
 EG_DECLARE_LOOKUP(lookup_e4m3_tc)
 EG_DECLARE_LOOKUP(lookup_e4m3_block)
 EG_DECLARE_LOOKUP(lookup_int8_tc)
+EG_DECLARE_LOOKUP(lookup_bf16_gated)
+EG_DECLARE_LOOKUP(lookup_e4m3_tc_gated)
 #undef EG_DECLARE_LOOKUP
 
 }  // namespace eg
 
-// Instantiation helper used by the eg_kernels_*.cu files.
-#define EG_KERNEL_ENTRY(IN, SC, SWAP, BN)                                              \
+// Instantiation helpers used by the eg_kernels_*.cu files.
+#define EG_KERNEL_ENTRY(IN, SC, SWAP, BN) EG_KERNEL_ENTRY_G(IN, SC, SWAP, BN, false)
+#define EG_KERNEL_ENTRY_G(IN, SC, SWAP, BN, G)                                         \
   do {                                                                                 \
-    using C_ = ::eg::Cfg<IN, SC, SWAP, BN>;                                            \
-    out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN>); \
+    using C_ = ::eg::Cfg<IN, SC, SWAP, BN, G>;                                         \
+    out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN, G>); \
     out->stage_bytes = C_::kStageBytes;                                                \
     out->fixed_bytes = 1024u + 512u + C_::kOpBytes;                                    \
     out->op_bytes = C_::kOpBytes;                                                      \
     out->threads = C_::kThreads;                                                       \
     out->elems_per_stage = C_::kElemsPerStage;                                         \
     out->tmem_cols = static_cast<int>(C_::kTmemCols);                                  \
+    out->acc_n = C_::kAccN;                                                            \
     return true;                                                                       \
   } while (0)

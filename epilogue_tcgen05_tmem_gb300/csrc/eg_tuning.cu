@@ -29,6 +29,12 @@ int bucket_of(int64_t M) {
 }
 
 bool entry_for(const eg_problem& p, int swap, int bn, KernelEntry* ke) {
+  if (p.flags & EG_EPI_GATED) {
+    if (p.dtype == EG_IN_BF16) return lookup_bf16_gated(swap, bn, ke);
+    if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
+      return lookup_e4m3_tc_gated(swap, bn, ke);
+    return false;
+  }
   if (p.dtype == EG_IN_BF16) return lookup_bf16(swap, bn, ke);
   if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL) return lookup_e4m3_tc(swap, bn, ke);
   if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_BLOCK) return lookup_e4m3_block(swap, bn, ke);
@@ -52,8 +58,10 @@ bool tuning_default(const eg_problem& p, int sms, eg_tuning* out) {
     t.stages = (p.dtype == EG_IN_INT8) ? 8 : 4;
   } else {
     t.swap_ab = 0;
-    const int max_bn = p.dtype == EG_IN_INT8 ? 64 : (promote ? 128 : 256);
-    int bn = 16;
+    const bool gated = (p.flags & EG_EPI_GATED) != 0;  // tiles 64 and 128 (two accumulators)
+    const int max_bn = (p.dtype == EG_IN_INT8 || (gated && p.N <= 64)) ? 64
+                       : (promote || gated) ? 128 : 256;
+    int bn = gated ? 64 : 16;
     while (bn < max_bn && bn < p.N) bn *= 2;
     t.tile_n = bn;
     t.stages = 8;
@@ -82,6 +90,8 @@ bool tuning_default(const eg_problem& p, int sms, eg_tuning* out) {
 }
 
 bool tuning_lookup(const eg_problem& p, int sms, eg_tuning* out) {
+  // the swept rows are for plain (ungated) layers
+  if (p.flags & EG_EPI_GATED) return tuning_default(p, sms, out);
   const int b = bucket_of(p.M);
   for (const TuningRow& r : kTable) {
     if (r.dtype < 0) break;

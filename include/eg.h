@@ -133,6 +133,16 @@ enum {
                                    scales the plan owns (eg_args.s_a is not
                                    read), then runs the GEMM on them as its
                                    programmatic dependent. */
+  EG_EPI_GATED = 512,           /* gated linear unit (SwiGLU with SiLU): W is
+                                   [2N][ldw], the gate half (rows 0..N-1)
+                                   then the up half (rows N..2N-1); s_w and
+                                   bias cover the 2N rows; per output (m, n)
+                                   gate = scale * acc[m][n] + bias[n],
+                                   up = scale * acc[m][N + n] + bias[N + n],
+                                   y = act(gate) * up (+ R[m][n]).  bf16 or
+                                   E4M3 token/channel inputs; not with
+                                   EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM
+                                   or cluster_reduce. */
   EG_OUT_F16 = 128,             /* Y is fp16 [M][ldy] (nearest even) */
   EG_OUT_E4M3 = 256             /* Y is E4M3 codes [M][ldy] (one byte each) of
                                    v / s_y with s_y = *eg_args.s_y (computed

@@ -70,7 +70,8 @@ def make_plan(p, tuning=None, debug=False, graph=False):
     return eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
                    residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
                    debug_accum=debug, graph=graph, tuning=tuning,
-                   out="bf16" if debug else getattr(p, "out", "bf16"))
+                   out="bf16" if debug else getattr(p, "out", "bf16"),
+                   gated=bool(p.meta.get("gated")))
 
 
 def run(p, tuning=None, debug=False, graph=False, y_pad=64, plan=None, d=None):

@@ -41,7 +41,7 @@ BAD = [
     (dict(M=4, N=8, K=136, dtype="e4m3", scale="token_channel"), eg.EG_ERR_INVALID_ARG),
     (dict(M=4, N=8, K=133152, dtype="int8", scale="token_channel"), eg.EG_ERR_UNSUPPORTED),
     (dict(M=4, N=8, K=64, flags=eg.EG_EPI_RESIDUAL | eg.EG_EPI_RESIDUAL_PRE_ACT), eg.EG_ERR_INVALID_ARG),
-    (dict(M=4, N=8, K=64, flags=1 << 9), eg.EG_ERR_INVALID_ARG),
+    (dict(M=4, N=8, K=64, flags=1 << 12), eg.EG_ERR_INVALID_ARG),
 ]
 
 

@@ -512,3 +512,52 @@ def test_output_narrowing_rejections():
         plan.run(A, W, Y)   # no s_y
     assert ei.value.status == eg.EG_ERR_INVALID_ARG
     plan.close()
+
+
+# --------------------------------------------- gated linear unit (SwiGLU) ---
+
+GATED_CASES = [
+    # dtype, scale, M, N, K, tuning
+    ("e4m3", "token_channel", 1, 1024, 2048, None),
+    ("e4m3", "token_channel", 5, 1000, 1024, dict(tile_n=16, stages=4, split_k=3, swap_ab=1)),
+    ("e4m3", "token_channel", 16, 512, 4096, dict(tile_n=16, stages=4, split_k=1, swap_ab=1,
+                                                 stream_k=2)),
+    ("e4m3", "token_channel", 40, 384, 1024, dict(tile_n=64, stages=3, split_k=2, swap_ab=1)),
+    ("e4m3", "token_channel", 200, 264, 640, None),
+    ("bf16", "none", 7, 300, 512, None),
+    ("bf16", "none", 130, 256, 512, dict(tile_n=128, stages=3, split_k=2, swap_ab=0)),
+    ("bf16", "none", 130, 200, 512, dict(tile_n=64, stages=4, split_k=1, swap_ab=0)),
+]
+
+
+@pytest.mark.parametrize("dtype,scale,M,N,K,tuning", GATED_CASES)
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+def test_gated_unit(dtype, scale, M, N, K, tuning, act):
+    """y = act(gate) * up (+ R) over the two weight halves, against the
+    oracle (SiLU: SwiGLU; GELU: GeGLU)."""
+    p = inputs.make_gated_problem(M, N, K, dtype, scale, act=act, bias=True, residual=True, seed=23)
+    y, _ = run(p, tuning)
+    assert_close_rms(bits(y), oracle.linear_gated(p))
+
+
+@pytest.mark.parametrize("out", ["f16", "e4m3"])
+def test_gated_unit_narrow_outputs(out):
+    p = inputs.make_gated_problem(8, 512, 1024, "e4m3", "token_channel", act="silu", seed=24)
+    if out == "e4m3":
+        v = (oracle.linear_gated(p).astype(np.uint32) << 16).view(np.float32)
+        p.s_y = float(np.abs(v).max()) / 200.0
+    p.out = out
+    y, _ = run(p)
+    assert_close_out(bits(y), oracle.linear_gated(p), out)
+
+
+def test_gated_unit_rejections():
+    for kw, status in [(dict(dtype="int8", scale="token_channel"), eg.EG_ERR_UNSUPPORTED),
+                       (dict(dtype="e4m3", scale="block"), eg.EG_ERR_UNSUPPORTED)]:
+        with pytest.raises(eg.EgError) as ei:
+            eg.Plan(4, 256, 512, gated=True, **kw)
+        assert ei.value.status == status
+    with pytest.raises(eg.EgError) as ei:
+        eg.Plan(4, 256, 512, "e4m3", "token_channel", gated=True,
+                tuning=dict(tile_n=16, stages=4, split_k=4, swap_ab=1, cluster_reduce=1))
+    assert ei.value.status == eg.EG_ERR_UNSUPPORTED
