@@ -300,16 +300,18 @@ void plan_grid(eg_plan* pl, int sms, int per_sm) {
   pl->blocks_per_sm = per_sm;
   pl->max_contrib = t.split_k;
   if (t.stream_k > 0) {
-    // balanced split-K: G CTAs share I = tiles x K-tiles iterations; CTA c
-    // owns [floor(c I/G), floor((c+1) I/G)); a tile has as many partial sums
-    // as CTAs whose ranges overlap it
-    const long long iters = tiles * pl->k_tiles;
+    // balanced split-K: whole tiles data-parallel for all but the last full
+    // wave, then G CTAs share the remaining I = tiles x K-tiles iterations;
+    // CTA c owns [floor(c I/G), floor((c+1) I/G)) of them; a split tile has
+    // as many partial sums as CTAs whose ranges overlap it
     long long G = static_cast<long long>(sms) * std::min(per_sm, t.stream_k);
-    if (G > iters) G = iters;
+    if (G > tiles * pl->k_tiles) G = tiles * pl->k_tiles;
+    const long long dp = G > 0 ? eg::stream_dp_tiles(tiles, G) : 0;
+    const long long iters = (tiles - dp) * pl->k_tiles;
     pl->grid = static_cast<int>(G);
-    pl->units = static_cast<int>(std::min<long long>(iters, INT32_MAX));
+    pl->units = static_cast<int>(std::min<long long>(dp + iters, INT32_MAX));
     int mc = 1;
-    for (long long tile = 0; tile < tiles && G > 0; ++tile) {
+    for (long long tile = 0; tile < tiles - dp && G > 0; ++tile) {
       const long long b = tile * pl->k_tiles, e2 = b + pl->k_tiles;
       const long long first = ((b + 1) * G - 1) / iters, last = (e2 * G - 1) / iters;
       mc = std::max(mc, static_cast<int>(last - first + 1));

@@ -784,28 +784,52 @@ __device__ __forceinline__ void unit_tile(const KParams& p, int tile, int bn, Un
 
 // Work assignment of this CTA.  Split-K: units u = blockIdx.x, +gridDim.x,
 // ... each one (tile, split) with even K splits.  Balanced split-K (stream
-// K): the tiles x K-tiles iteration space is cut into gridDim.x equal
-// contiguous ranges; CTA c owns [floor(c I / G), floor((c+1) I / G)) and
-// walks it tile by tile, so a tile's K range is shared by the CTAs whose
-// ranges overlap it.
+// K), over T tiles and G CTAs: the first stream_dp_tiles() tiles are whole
+// units handed out data-parallel (tile c, c + G, ...: concurrently running
+// CTAs work on neighbouring tiles, so each weight tile is fetched from DRAM
+// once and shared through L2); the remaining tiles' tiles x K-tiles
+// iterations are cut into G equal contiguous ranges, CTA c owning
+// [floor(c I / G), floor((c+1) I / G)) and walking it tile by tile, so a
+// tile's K range is shared by the CTAs whose ranges overlap it.
 struct WorkIter {
-  int64_t pos, end;
+  int64_t pos, end;      // stream-K iterations (relative to the split tiles)
+  int64_t dp, dp_tiles;  // next data-parallel tile; tiles before the split ones
 };
+
+// Whole-tile waves before the split tail: all but the last full wave, so the
+// split part covers between one and two waves of tiles.
+__host__ __device__ __forceinline__ int64_t stream_dp_tiles(int64_t T, int64_t G) {
+  return T / G >= 2 ? (T / G - 1) * G : 0;
+}
 
 __device__ __forceinline__ WorkIter work_begin(const KParams& p) {
   WorkIter it;
+  const int64_t T = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols;
   if (p.stream_k) {
-    const int64_t I = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols * p.k_tiles;
+    it.dp_tiles = stream_dp_tiles(T, gridDim.x);
+    it.dp = blockIdx.x;
+    const int64_t I = (T - it.dp_tiles) * p.k_tiles;
     it.pos = I * blockIdx.x / gridDim.x;
     it.end = I * (blockIdx.x + 1) / gridDim.x;
   } else {
+    it.dp = it.dp_tiles = 0;
     it.pos = blockIdx.x;
-    it.end = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols * p.split_k;
+    it.end = T * p.split_k;
   }
   return it;
 }
 
 __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it, Unit& w) {
+  if (p.stream_k && it.dp < it.dp_tiles) {
+    // a whole tile, data-parallel
+    unit_tile(p, static_cast<int>(it.dp), bn, w);
+    it.dp += gridDim.x;
+    w.j = 0;
+    w.contrib = 1;
+    w.kt0 = 0;
+    w.nk = p.k_tiles;
+    return true;
+  }
   if (it.pos >= it.end) return false;
   if (!p.stream_k) {
     const int u = static_cast<int>(it.pos);
@@ -818,12 +842,13 @@ __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it
     return true;
   }
   const int64_t KT = p.k_tiles;
-  const int64_t I = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols * KT;
+  const int64_t T = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols;
+  const int64_t I = (T - it.dp_tiles) * KT;
   const int64_t G = gridDim.x;
-  const int tile = static_cast<int>(it.pos / KT);
-  const int64_t tile_begin = tile * KT, tile_end = tile_begin + KT;
+  const int64_t rt = it.pos / KT;  // tile within the split part
+  const int64_t tile_begin = rt * KT, tile_end = tile_begin + KT;
   const int64_t seg_end = it.end < tile_end ? it.end : tile_end;
-  unit_tile(p, tile, bn, w);
+  unit_tile(p, static_cast<int>(it.dp_tiles + rt), bn, w);
   w.kt0 = static_cast<int>(it.pos - tile_begin);
   w.nk = static_cast<int>(seg_end - it.pos);
   // owner of iteration i: the CTA c with floor(c I/G) <= i < floor((c+1) I/G)

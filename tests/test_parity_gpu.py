@@ -561,3 +561,23 @@ def test_gated_unit_rejections():
         eg.Plan(4, 256, 512, "e4m3", "token_channel", gated=True,
                 tuning=dict(tile_n=16, stages=4, split_k=4, swap_ab=1, cluster_reduce=1))
     assert ei.value.status == eg.EG_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype,scale,tn", [("bf16", "none", 64), ("e4m3", "token_channel", 64),
+                                            ("e4m3", "block", 128)])
+def test_balanced_split_k_with_data_parallel_waves(dtype, scale, tn):
+    """More than two waves of tiles: whole tiles go data-parallel first and
+    only the last one to two waves split their K range across CTAs."""
+    M, N, K = (2560, 1024, 384) if tn == 64 else (4864, 1280, 512)
+    p = inputs.make_problem(M, N, K, dtype, scale, act="silu", bias=True, residual=True, seed=44)
+    t = dict(tile_n=tn, stages=3, split_k=1, swap_ab=0, stream_k=1)
+    plan = make_plan(p, t)
+    li = plan.launch_info
+    tiles = ((M + 127) // 128) * ((N + tn - 1) // tn)
+    assert tiles >= 2 * li["grid"], (tiles, li)
+    d = to_device(p)
+    y1, _ = run(p, plan=plan, d=d)
+    y2, _ = run(p, plan=plan, d=d)
+    plan.close()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), "not deterministic"
+    assert_close_rms(bits(y1), oracle.linear(p))
