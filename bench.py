@@ -19,6 +19,7 @@ sample of the same workload instead.
 ``--config NAME`` measures another workload (bf16_small, fp8_calls,
 w8a8_int8, block_fp8, prefill_bf16, prefill_unfused, and fp8_quant_calls /
 int8_quant_calls: bf16 activations quantised per token in the same plan run;
+fp8_swiglu_calls: the gated unit of an MLP, W [2 x 12288, 4096];
 ``--m`` picks token counts) and prints its own line.
 """
 from __future__ import annotations
@@ -462,8 +463,11 @@ def run_config(args):
     # quantisation prologue: bf16 activations in, per-token quantisation
     # and the GEMM in one plan run
     quant = name in ("fp8_quant_calls", "int8_quant_calls")
+    # gated unit (SwiGLU) of an MLP with hidden 4096 and intermediate 12288:
+    # W [2 x 12288, 4096] FP8, per-token / per-channel scales
+    gated = name == "fp8_swiglu_calls"
     wl = {"prefill_unfused": "prefill_bf16", "fp8_quant_calls": "fp8_calls",
-          "int8_quant_calls": "w8a8_int8"}.get(name, name)
+          "int8_quant_calls": "w8a8_int8", "fp8_swiglu_calls": "fp8_calls"}.get(name, name)
     Ms = [None]
     if wl in ("w8a8_int8", "fp8_calls"):
         Ms = list(inputs.DECODE_TOKENS)
@@ -475,13 +479,20 @@ def run_config(args):
         wl = "fp8_dynamic"
     rows = []
     for M in Ms:
-        p = inputs.workload(wl, M)
+        if gated:
+            p = inputs.make_gated_problem(M, 12288, 4096, "e4m3", "token_channel", act="silu",
+                                          outlier_frac=0.01)
+        else:
+            p = inputs.workload(wl, M)
         d = device_problem(p, torch)
         plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
                        residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
-                       pdl=not unfused, quant_a=quant,
+                       pdl=not unfused, quant_a=quant, gated=gated,
                        tuning=json.loads(args.tuning) if args.tuning else None)
         nb = traffic.problem_bytes(p)
+        if gated:
+            # two weight halves and their scales; the output is N wide
+            nb += p.N * p.K + p.N * 4
         if quant:
             # the layer reads bf16 activations instead of codes and scales
             X = torch.from_numpy(inputs.activations_bf16(p.M, p.K, outlier_frac=0.01)).view(
