@@ -244,6 +244,13 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
   *smem = static_cast<uint32_t>(s);
   const int kt = static_cast<int>((p.K + ke->elems_per_stage - 1) / ke->elems_per_stage);
   *k_tiles = kt;
+  {
+    // the kernel walks units and K-tile iterations in 32-bit integers
+    const int64_t rows = t.swap_ab ? p.N : p.M, cols = t.swap_ab ? p.M : p.N;
+    const int64_t tiles = ((rows + 127) / 128) * ((cols + t.tile_n - 1) / t.tile_n);
+    if (tiles * std::max<int64_t>(std::max(kt, 1), t.split_k) > INT32_MAX)
+      return fail(EG_ERR_UNSUPPORTED, "tiles x K tiles exceeds the kernel's 32-bit work counters");
+  }
   if (t.split_k < 1 || t.split_k > 256)
     return fail(EG_ERR_UNSUPPORTED, "split_k must be in 1..256 (got %d)", t.split_k);
   if (t.split_k > (kt > 0 ? kt : 1))

@@ -791,9 +791,11 @@ __device__ __forceinline__ void unit_tile(const KParams& p, int tile, int bn, Un
 // iterations are cut into G equal contiguous ranges, CTA c owning
 // [floor(c I / G), floor((c+1) I / G)) and walking it tile by tile, so a
 // tile's K range is shared by the CTAs whose ranges overlap it.
+// 32-bit positions (the host keeps tiles x max(split_k, K tiles) within
+// int32): the iterator lives in registers of all three roles.
 struct WorkIter {
-  int64_t pos, end;      // stream-K iterations (relative to the split tiles)
-  int64_t dp, dp_tiles;  // next data-parallel tile; tiles before the split ones
+  int pos, end;      // stream-K iterations (relative to the split tiles), or units
+  int dp, dp_tiles;  // next data-parallel tile; tiles before the split ones
 };
 
 // Whole-tile waves before the split tail: all but the last full wave, so the
@@ -804,16 +806,16 @@ __host__ __device__ __forceinline__ int64_t stream_dp_tiles(int64_t T, int64_t G
 
 __device__ __forceinline__ WorkIter work_begin(const KParams& p) {
   WorkIter it;
-  const int64_t T = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols;
+  const int T = p.tiles_rows * p.tiles_cols;
   if (p.stream_k) {
-    it.dp_tiles = stream_dp_tiles(T, gridDim.x);
-    it.dp = blockIdx.x;
-    const int64_t I = (T - it.dp_tiles) * p.k_tiles;
-    it.pos = I * blockIdx.x / gridDim.x;
-    it.end = I * (blockIdx.x + 1) / gridDim.x;
+    it.dp_tiles = static_cast<int>(stream_dp_tiles(T, gridDim.x));
+    it.dp = static_cast<int>(blockIdx.x);
+    const int64_t I = static_cast<int64_t>(T - it.dp_tiles) * p.k_tiles;
+    it.pos = static_cast<int>(I * blockIdx.x / gridDim.x);
+    it.end = static_cast<int>(I * (blockIdx.x + 1) / gridDim.x);
   } else {
     it.dp = it.dp_tiles = 0;
-    it.pos = blockIdx.x;
+    it.pos = static_cast<int>(blockIdx.x);
     it.end = T * p.split_k;
   }
   return it;
@@ -822,8 +824,8 @@ __device__ __forceinline__ WorkIter work_begin(const KParams& p) {
 __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it, Unit& w) {
   if (p.stream_k && it.dp < it.dp_tiles) {
     // a whole tile, data-parallel
-    unit_tile(p, static_cast<int>(it.dp), bn, w);
-    it.dp += gridDim.x;
+    unit_tile(p, it.dp, bn, w);
+    it.dp += static_cast<int>(gridDim.x);
     w.j = 0;
     w.contrib = 1;
     w.kt0 = 0;
@@ -832,8 +834,8 @@ __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it
   }
   if (it.pos >= it.end) return false;
   if (!p.stream_k) {
-    const int u = static_cast<int>(it.pos);
-    it.pos += gridDim.x;
+    const int u = it.pos;
+    it.pos += static_cast<int>(gridDim.x);
     w.j = u % p.split_k;
     w.contrib = p.split_k;
     unit_tile(p, u / p.split_k, bn, w);
@@ -841,19 +843,19 @@ __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it
     w.nk = static_cast<int>(static_cast<int64_t>(w.j + 1) * p.k_tiles / p.split_k) - w.kt0;
     return true;
   }
-  const int64_t KT = p.k_tiles;
-  const int64_t T = static_cast<int64_t>(p.tiles_rows) * p.tiles_cols;
-  const int64_t I = (T - it.dp_tiles) * KT;
+  const int KT = p.k_tiles;
+  const int T = p.tiles_rows * p.tiles_cols;
+  const int64_t I = static_cast<int64_t>(T - it.dp_tiles) * KT;
   const int64_t G = gridDim.x;
-  const int64_t rt = it.pos / KT;  // tile within the split part
-  const int64_t tile_begin = rt * KT, tile_end = tile_begin + KT;
-  const int64_t seg_end = it.end < tile_end ? it.end : tile_end;
-  unit_tile(p, static_cast<int>(it.dp_tiles + rt), bn, w);
-  w.kt0 = static_cast<int>(it.pos - tile_begin);
-  w.nk = static_cast<int>(seg_end - it.pos);
+  const int rt = it.pos / KT;  // tile within the split part
+  const int tile_begin = rt * KT, tile_end = tile_begin + KT;
+  const int seg_end = it.end < tile_end ? it.end : tile_end;
+  unit_tile(p, it.dp_tiles + rt, bn, w);
+  w.kt0 = it.pos - tile_begin;
+  w.nk = seg_end - it.pos;
   // owner of iteration i: the CTA c with floor(c I/G) <= i < floor((c+1) I/G)
   const int first = static_cast<int>(((tile_begin + 1) * G - 1) / I);
-  const int last = static_cast<int>((tile_end * G - 1) / I);
+  const int last = static_cast<int>((static_cast<int64_t>(tile_end) * G - 1) / I);
   w.contrib = last - first + 1;
   w.j = static_cast<int>(blockIdx.x) - first;
   it.pos = seg_end;
