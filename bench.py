@@ -525,13 +525,23 @@ def run_config(args):
         e1.record()
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
+        # SM clocks and throttle reasons under this load: about 0.6 s more of
+        # the same calls, sampled by nvidia-smi
+        sampler = ClockSampler(torch.cuda.current_device())
+        sampler.start()
+        time.sleep(0.15)
+        for i in range(max(1, int(0.6e6 / max(us, 1e-3)))):
+            call(Ws[i % len(Ws)])
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
         tf = fl / (us * 1e-6) / 1e12
         gbs = nb / (us * 1e-6) / 1e9
         peak_tf = peaks["bf16_tflops"] * (2 if p.dtype == "e4m3" else 1)
         rows.append({"M": p.M, "N": p.N, "K": p.K, "us_per_call": round(us, 3),
                      "TFLOP_s": round(tf, 2), "GB_s": round(gbs, 1),
                      "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-                     "tensor_frac": round(tf / peak_tf, 4), "tuning": plan.tuning})
+                     "tensor_frac": round(tf / peak_tf, 4), "tuning": plan.tuning,
+                     "clocks": clocks})
         plan.close()
         del d, Ws
         torch.cuda.empty_cache()

@@ -50,12 +50,13 @@ class eg_problem(ctypes.Structure):
 class eg_tuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("swap_ab", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32), ("cluster_reduce", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("cluster_reduce", ctypes.c_int32),
+                ("cta_pair", ctypes.c_int32)]
 
     def as_dict(self):
         return {"tile_n": self.tile_n, "stages": self.stages, "split_k": self.split_k,
                 "swap_ab": self.swap_ab, "stream_k": self.stream_k,
-                "cluster_reduce": self.cluster_reduce}
+                "cluster_reduce": self.cluster_reduce, "cta_pair": self.cta_pair}
 
 
 class eg_args(ctypes.Structure):
@@ -144,8 +145,10 @@ def make_problem(M, N, K, dtype="bf16", scale="none", act="none", flags=0) -> eg
     return eg_problem(M, N, K, DTYPES[dtype], SCALES[scale], ACTS[act], flags)
 
 
-def make_tuning(tile_n, stages, split_k, swap_ab, stream_k=0, cluster_reduce=0) -> eg_tuning:
-    return eg_tuning(tile_n, stages, split_k, int(bool(swap_ab)), stream_k, int(bool(cluster_reduce)))
+def make_tuning(tile_n, stages, split_k, swap_ab, stream_k=0, cluster_reduce=0,
+                cta_pair=0) -> eg_tuning:
+    return eg_tuning(tile_n, stages, split_k, int(bool(swap_ab)), stream_k, int(bool(cluster_reduce)),
+                     int(bool(cta_pair)))
 
 
 # ------------------------------------------------------ C-ABI functions ---

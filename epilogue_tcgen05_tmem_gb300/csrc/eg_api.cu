@@ -187,7 +187,15 @@ eg_status validate_problem(const eg_problem* p) {
   return EG_OK;
 }
 
-bool lookup_kernel(const eg_problem& p, int swap, int bn, eg::KernelEntry* ke) {
+bool lookup_kernel(const eg_problem& p, int swap, int bn, int pair, eg::KernelEntry* ke) {
+  if (pair) {
+    // CTA pairs: plain layers without swap-AB, bf16 or FP8 per-token/channel
+    if (swap || (p.flags & EG_EPI_GATED)) return false;
+    if (p.dtype == EG_IN_BF16) return eg::lookup_bf16_pair(bn, ke);
+    if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
+      return eg::lookup_e4m3_tc_pair(bn, ke);
+    return false;
+  }
   if (p.flags & EG_EPI_GATED) {
     if (p.dtype == EG_IN_BF16) return eg::lookup_bf16_gated(swap, bn, ke);
     if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
@@ -216,9 +224,14 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
                           uint32_t* smem, int* k_tiles) {
   if (t.swap_ab != 0 && t.swap_ab != 1)
     return fail(EG_ERR_INVALID_ARG, "swap_ab must be 0 or 1");
-  if (!lookup_kernel(p, t.swap_ab, t.tile_n, ke))
-    return fail(EG_ERR_UNSUPPORTED, "no kernel for tile_n=%d swap_ab=%d with this dtype/scale",
-                t.tile_n, t.swap_ab);
+  if (t.cta_pair != 0 && t.cta_pair != 1)
+    return fail(EG_ERR_INVALID_ARG, "cta_pair must be 0 or 1");
+  if (t.cta_pair && (t.split_k != 1 || t.stream_k != 0 || t.cluster_reduce != 0))
+    return fail(EG_ERR_UNSUPPORTED, "cta_pair takes split_k 1, stream_k 0 and cluster_reduce 0");
+  if (!lookup_kernel(p, t.swap_ab, t.tile_n, t.cta_pair, ke))
+    return fail(EG_ERR_UNSUPPORTED,
+                "no kernel for tile_n=%d swap_ab=%d cta_pair=%d with this dtype/scale/epilogue",
+                t.tile_n, t.swap_ab, t.cta_pair);
   if (t.stages < 2 || t.stages > 8)
     return fail(EG_ERR_UNSUPPORTED, "stages must be in 2..8 (got %d)", t.stages);
   if (t.cluster_reduce != 0 && t.cluster_reduce != 1)
@@ -330,6 +343,11 @@ void plan_grid(eg_plan* pl, int sms, int per_sm) {
     pl->grid = static_cast<int>(units);
     pl->units = static_cast<int>(units);
     pl->max_contrib = 1;
+  } else if (t.cta_pair) {
+    // persistent CTA pairs: one work slot per 2-CTA cluster
+    const long long slots = static_cast<long long>(sms / 2) * per_sm;
+    pl->grid = 2 * static_cast<int>(units < slots ? units : slots);
+    pl->units = static_cast<int>(units);
   } else {
     const long long slots = static_cast<long long>(sms) * per_sm;
     pl->grid = static_cast<int>(units < slots ? units : slots);
@@ -429,7 +447,9 @@ eg_status ensure_maps(eg_plan* pl, const eg_args* a) {
   const bool swap = pl->tune.swap_ab != 0;
   if ((s = encode_map(&mA, a->A, p.dtype, p.M, p.K, a->lda, box_k, swap ? bn : 128)) != EG_OK) return s;
   const int64_t wrows = (p.flags & EG_EPI_GATED) ? 2 * p.N : p.N;  // gated: gate + up halves
-  if ((s = encode_map(&mW, a->W, p.dtype, wrows, p.K, a->ldw, box_k, swap ? 128 : bn)) != EG_OK) return s;
+  // CTA pairs: each CTA loads half of the weight tile
+  const int wbox = swap ? 128 : (pl->tune.cta_pair ? bn / 2 : bn);
+  if ((s = encode_map(&mW, a->W, p.dtype, wrows, p.K, a->ldw, box_k, wbox)) != EG_OK) return s;
   pl->tmP = swap ? mW : mA;
   pl->tmQ = swap ? mA : mW;
   pl->mapA = a->A;
@@ -512,10 +532,11 @@ eg_status launch_fused(eg_plan* pl, const eg::KParams& kp, cudaStream_t st) {
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
-  if (kp.cluster_reduce) {
-    // the split_k CTAs of a tile (consecutive blocks) form one cluster
+  if (kp.cluster_reduce || pl->tune.cta_pair) {
+    // the split_k CTAs of a tile, or a CTA pair (consecutive blocks), form
+    // one cluster
     attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = static_cast<unsigned>(kp.split_k);
+    attr[n].val.clusterDim.x = pl->tune.cta_pair ? 2u : static_cast<unsigned>(kp.split_k);
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
@@ -676,7 +697,7 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   const bool swap = t.swap_ab != 0;
   pl->rows = static_cast<int>(swap ? p.N : p.M);
   pl->cols = static_cast<int>(swap ? p.M : p.N);
-  pl->tiles_rows = (pl->rows + 127) / 128;
+  pl->tiles_rows = t.cta_pair ? (pl->rows + 255) / 256 : (pl->rows + 127) / 128;
   pl->tiles_cols = (pl->cols + t.tile_n - 1) / t.tile_n;
   pl->wait_limit_ns = default_wait_limit_ns();
   if (const char* e2 = getenv("EG_PDL_L2_PREFETCH")) pl->l2_prefetch = atoi(e2) != 0;
@@ -994,7 +1015,7 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   const bool swap = t.swap_ab != 0;
   pl.rows = static_cast<int>(swap ? p.N : p.M);
   pl.cols = static_cast<int>(swap ? p.M : p.N);
-  pl.tiles_rows = (pl.rows + 127) / 128;
+  pl.tiles_rows = t.cta_pair ? (pl.rows + 255) / 256 : (pl.rows + 127) / 128;
   pl.tiles_cols = (pl.cols + t.tile_n - 1) / t.tile_n;
   pl.wait_limit_ns = default_wait_limit_ns();
   if ((s = validate_args(&pl, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0)) != EG_OK) return s;

@@ -104,14 +104,18 @@ __device__ __forceinline__ void trace_point(const KParams& p, int point) {
 // then the up half; each stage also carries the up half's weight tile and
 // UMMA fills two accumulators per unit, gate in columns [0, BN) and up in
 // [BN, 2 BN).
-template <int IN, int SC, bool SWAP, int BN, bool G = false>
+// PR: CTA pair.  Two CTAs of a cluster compute one 256 x BN tile with pair
+// UMMAs (M = 256): each holds its 128 activation rows and half of the
+// weight tile (BN/2 rows) per stage, and its 128 output rows in tensor
+// memory; the even CTA issues the UMMAs.
+template <int IN, int SC, bool SWAP, int BN, bool G = false, bool PR = false>
 struct Cfg {
   static constexpr bool kConvert = (IN == IN_INT8);
   static constexpr bool kPromote = (SC == SC_BLOCK) || kConvert;
   static constexpr int kAtoms = kConvert ? 2 : 1;          // 128-byte K atoms per UMMA stage
   static constexpr int kElemsPerStage = (IN == IN_BF16) ? 64 : 128;
   static constexpr uint32_t kPBytes = 128u * 128u * kAtoms; // UMMA operand P per stage
-  static constexpr uint32_t kQBytes = uint32_t(BN) * 128u * kAtoms;
+  static constexpr uint32_t kQBytes = uint32_t(PR ? BN / 2 : BN) * 128u * kAtoms;
   static constexpr uint32_t kP8Bytes = kConvert ? 128u * 128u : 0u;  // int8 staging
   static constexpr uint32_t kQ8Bytes = kConvert ? uint32_t(BN) * 128u : 0u;
   // TMA ring stage: the UMMA operands, or (INT8) the int8 staging tiles.
@@ -124,12 +128,16 @@ struct Cfg {
       kConvert ? kP8Bytes + kQ8Bytes : kPBytes + kQBytes + (G ? kWBytes : 0u);
   static constexpr int kOpSlots = 2;
   static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * kQBytes : 0u;
-  static constexpr uint32_t kTxBytes =  // bytes one stage's TMA delivers
-      (128u + BN) * 128u + (G ? (SWAP ? 128u : uint32_t(BN)) * 128u : 0u);
-  // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for block-scale
-  // promotion of wide tiles (two column halves per quarter, so each thread
-  // keeps BN/2 running sums and the promotion keeps up with UMMA).
-  static constexpr int kEpiWarps = (kPromote && !kConvert && BN >= 64) ? 8 : 4;
+  static constexpr uint32_t kTxBytes =  // bytes one stage's TMA delivers (PR: to both CTAs)
+      PR ? 2u * (128u + BN / 2) * 128u
+         : (128u + BN) * 128u + (G ? (SWAP ? 128u : uint32_t(BN)) * 128u : 0u);
+  // Epilogue warps: 4 (one per TMEM lane quarter), or 8 (two column halves
+  // per quarter) for block-scale promotion of wide tiles, so each thread
+  // keeps BN/2 running sums and the promotion keeps up with UMMA, and for
+  // wide large-M tiles, so two warps per SM sub-partition hide the TMEM,
+  // residual-load and activation latencies of a 128 x 128..256 epilogue.
+  static constexpr int kEpiWarps =
+      ((kPromote && !kConvert && BN >= 64) || (!SWAP && !kPromote && !G && BN >= 128)) ? 8 : 4;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kColsPerThread = BN / (kEpiWarps / 4);
   static constexpr int kThreads = 64 + kEpiThreads + (kConvert ? 128 : 0);
@@ -162,18 +170,21 @@ struct Cfg {
   static constexpr uint32_t kTmemUsed = kAccCols + kTmemACols;
   static constexpr uint32_t kTmemCols =
       kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
+  static constexpr uint32_t kUmmaM = PR ? 256u : 128u;
   static constexpr uint32_t kIdesc =
-      (IN == IN_BF16) ? idesc_f32acc(1, 1, 128, BN)
-                      : idesc_f32acc(0, 0, 128, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
+      (IN == IN_BF16) ? idesc_f32acc(1, 1, kUmmaM, BN)
+                      : idesc_f32acc(0, 0, kUmmaM, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
   static_assert(!kPromote || BN <= 128, "promotion keeps BN fp32 values per thread");
   static_assert(kTmemUsed <= 512, "tensor memory holds 512 columns");
   static_assert(!G || !kPromote, "gated units use the tensor-memory accumulator path");
+  static_assert(!PR || (!SWAP && !kPromote && !G && (BN == 128 || BN == 256)),
+                "CTA pairs: tiles of 256 x 128 or 256 x 256, per-token/channel or bf16");
 };
 
-template <int IN, int SC, bool SWAP, int BN, bool G = false>
+template <int IN, int SC, bool SWAP, int BN, bool G = false, bool PR = false>
 constexpr uint32_t smem_bytes_for(int stages) {
-  using C = Cfg<IN, SC, SWAP, BN, G>;
+  using C = Cfg<IN, SC, SWAP, BN, G, PR>;
   return 1024u + uint32_t(stages) * C::kStageBytes + C::kOpBytes + 512u;
 }
 
@@ -774,12 +785,26 @@ struct Unit {
   int j, contrib, tile, tile_r, tile_c, row0, col0, kt0, nk;
 };
 
+// PR: tiles are 256 rows high (tiles_rows counts them); the odd CTA of the
+// pair owns the tile's second 128 rows.
+template <bool PR = false>
 __device__ __forceinline__ void unit_tile(const KParams& p, int tile, int bn, Unit& w) {
   w.tile = tile;
   w.tile_r = tile % p.tiles_rows;
   w.tile_c = tile / p.tiles_rows;
-  w.row0 = w.tile_r * 128;
+  w.row0 = PR ? w.tile_r * 256 + static_cast<int>(blockIdx.x & 1u) * 128 : w.tile_r * 128;
   w.col0 = w.tile_c * bn;
+}
+
+// The work slot of this CTA and the number of slots: one per CTA, or (PR)
+// one per CTA pair, both CTAs of a pair walking the same units.
+template <bool PR>
+__device__ __forceinline__ int work_slot() {
+  return PR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+}
+template <bool PR>
+__device__ __forceinline__ int work_slots() {
+  return PR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 }
 
 // Work assignment of this CTA.  Split-K: units u = blockIdx.x, +gridDim.x,
@@ -804,28 +829,31 @@ __host__ __device__ __forceinline__ int64_t stream_dp_tiles(int64_t T, int64_t G
   return T / G >= 2 ? (T / G - 1) * G : 0;
 }
 
+template <bool PR = false>
 __device__ __forceinline__ WorkIter work_begin(const KParams& p) {
   WorkIter it;
   const int T = p.tiles_rows * p.tiles_cols;
+  const int c = work_slot<PR>(), G = work_slots<PR>();
   if (p.stream_k) {
-    it.dp_tiles = static_cast<int>(stream_dp_tiles(T, gridDim.x));
-    it.dp = static_cast<int>(blockIdx.x);
+    it.dp_tiles = static_cast<int>(stream_dp_tiles(T, G));
+    it.dp = c;
     const int64_t I = static_cast<int64_t>(T - it.dp_tiles) * p.k_tiles;
-    it.pos = static_cast<int>(I * blockIdx.x / gridDim.x);
-    it.end = static_cast<int>(I * (blockIdx.x + 1) / gridDim.x);
+    it.pos = static_cast<int>(I * c / G);
+    it.end = static_cast<int>(I * (c + 1) / G);
   } else {
     it.dp = it.dp_tiles = 0;
-    it.pos = static_cast<int>(blockIdx.x);
+    it.pos = c;
     it.end = T * p.split_k;
   }
   return it;
 }
 
+template <bool PR = false>
 __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it, Unit& w) {
   if (p.stream_k && it.dp < it.dp_tiles) {
     // a whole tile, data-parallel
-    unit_tile(p, it.dp, bn, w);
-    it.dp += static_cast<int>(gridDim.x);
+    unit_tile<PR>(p, it.dp, bn, w);
+    it.dp += work_slots<PR>();
     w.j = 0;
     w.contrib = 1;
     w.kt0 = 0;
@@ -835,10 +863,10 @@ __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it
   if (it.pos >= it.end) return false;
   if (!p.stream_k) {
     const int u = it.pos;
-    it.pos += static_cast<int>(gridDim.x);
+    it.pos += work_slots<PR>();
     w.j = u % p.split_k;
     w.contrib = p.split_k;
-    unit_tile(p, u / p.split_k, bn, w);
+    unit_tile<PR>(p, u / p.split_k, bn, w);
     w.kt0 = static_cast<int>(static_cast<int64_t>(w.j) * p.k_tiles / p.split_k);
     w.nk = static_cast<int>(static_cast<int64_t>(w.j + 1) * p.k_tiles / p.split_k) - w.kt0;
     return true;
@@ -846,18 +874,18 @@ __device__ __forceinline__ bool work_next(const KParams& p, int bn, WorkIter& it
   const int KT = p.k_tiles;
   const int T = p.tiles_rows * p.tiles_cols;
   const int64_t I = static_cast<int64_t>(T - it.dp_tiles) * KT;
-  const int64_t G = gridDim.x;
+  const int64_t G = work_slots<PR>();
   const int rt = it.pos / KT;  // tile within the split part
   const int tile_begin = rt * KT, tile_end = tile_begin + KT;
   const int seg_end = it.end < tile_end ? it.end : tile_end;
-  unit_tile(p, it.dp_tiles + rt, bn, w);
+  unit_tile<PR>(p, it.dp_tiles + rt, bn, w);
   w.kt0 = it.pos - tile_begin;
   w.nk = seg_end - it.pos;
   // owner of iteration i: the CTA c with floor(c I/G) <= i < floor((c+1) I/G)
   const int first = static_cast<int>(((tile_begin + 1) * G - 1) / I);
   const int last = static_cast<int>((static_cast<int64_t>(tile_end) * G - 1) / I);
   w.contrib = last - first + 1;
-  w.j = static_cast<int>(blockIdx.x) - first;
+  w.j = work_slot<PR>() - first;
   it.pos = seg_end;
   return true;
 }
@@ -1132,12 +1160,12 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
 // TMEM accumulator buffers and promotion buffers carry their phases across
 // units, so the epilogue of one unit overlaps the UMMA mainloop of the next.
 
-template <int IN, int SC, bool SWAP, int BN, bool G = false>
-__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
-    __maxnreg__((Cfg<IN, SC, SWAP, BN, G>::kMaxRegs))
+template <int IN, int SC, bool SWAP, int BN, bool G = false, bool PR = false>
+__global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
+    __maxnreg__((Cfg<IN, SC, SWAP, BN, G, PR>::kMaxRegs))
     fused_linear_kernel(const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmQ, const KParams p) {
-  using C = Cfg<IN, SC, SWAP, BN, G>;
+  using C = Cfg<IN, SC, SWAP, BN, G, PR>;
   constexpr int CW = C::kCW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1178,6 +1206,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
   const bool has_work = p.k_tiles > 0;
+  // CTA pair: the even CTA issues the UMMAs; stage barriers and the
+  // accumulator-free barriers that count are the even CTA's
+  const bool pair_leader = !PR || (blockIdx.x & 1u) == 0;
 
   if (threadIdx.x == 0) trace_point(p, TR_START);
   if (warp == 0 && lane == 0 && has_work) {
@@ -1193,7 +1224,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], C::kEpiThreads);
+      // per epilogue thread, or (PR) one arrival per CTA of the pair
+      mbar_init(&tempty[b], PR ? 2 : C::kEpiThreads);
     }
     mbar_init(mma_done, 1);
     mbar_init(red_full, 1);
@@ -1210,15 +1242,20 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PR) {
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // cluster split-K: every CTA's barriers are initialised before any remote
-  // arrival
-  if (p.cluster_reduce) cluster_sync_all();
+  // cluster split-K and CTA pairs: every CTA's barriers are initialised
+  // before any remote arrival
+  if (PR || p.cluster_reduce) cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
   if (p.pdl && threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) trace_point(p, TR_SETUP);
@@ -1229,13 +1266,25 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
       const uint64_t pol_first = policy_evict_first();
       // The weight operand (P with swap-AB, else Q) is constant across calls;
       // the activation operand may be written by the previous kernel.
+      // PR: loads complete on the even CTA's stage barrier; this CTA's half
+      // of the weight tile starts BN/2 rows further for the odd CTA
+      const uint32_t full_pair0 = PR ? cluster_map(smem_u32(&full[0]), 0) : 0u;
+      const int q_off = PR ? static_cast<int>(blockIdx.x & 1u) * (BN / 2) : 0;
       auto load_op = [&](bool weight, const Unit& w, int i, int s) {
         uint8_t* base = stage_base(s);
         const bool isP = (weight == SWAP);
         uint8_t* dst = base + (isP ? 0u : (C::kConvert ? C::kP8Bytes : C::kPBytes));
         const int kx = (w.kt0 + i) * C::kElemsPerStage;
         const CUtensorMap* map = isP ? &tmP : &tmQ;
-        const int y = isP ? w.row0 : w.col0;
+        const int y = isP ? w.row0 : w.col0 + q_off;
+        if constexpr (PR) {
+          const uint32_t cbar = full_pair0 + static_cast<uint32_t>(s) * 8u;
+          if (isP ? p.evict_first_p : p.evict_first_q)
+            tma_load_2d_pair_hint(dst, map, cbar, kx, y, pol_first);
+          else
+            tma_load_2d_pair(dst, map, cbar, kx, y);
+          return;
+        }
         if (isP ? p.evict_first_p : p.evict_first_q)
           tma_load_2d_hint(dst, map, &full[s], kx, y, pol_first);
         else
@@ -1254,9 +1303,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
       uint32_t g = 0;  // ring iteration across units
       bool first = true;
       bool ok = true;
-      WorkIter it = work_begin(p);
+      WorkIter it = work_begin<PR>(p);
       Unit w;
-      while (ok && work_next(p, BN, it, w)) {
+      while (ok && work_next<PR>(p, BN, it, w)) {
         int i0 = 0;
         if (first) {
           first = false;
@@ -1265,12 +1314,12 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
           // the previous kernel finishes; then wait for its results.
           const int pre = p.pdl ? (w.nk < S ? w.nk : S) : 0;
           for (int i = 0; i < pre; ++i) {
-            mbar_arrive_expect_tx(&full[i], C::kTxBytes);
+            if (pair_leader) mbar_arrive_expect_tx(&full[i], C::kTxBytes);
             load_op(true, w, i, i);
           }
           if (p.pdl && p.l2_prefetch) {
             const CUtensorMap* wmap = SWAP ? &tmP : &tmQ;
-            const int wy = SWAP ? w.row0 : w.col0;
+            const int wy = SWAP ? w.row0 : w.col0 + q_off;
             for (int i = pre; i < w.nk; ++i) {
               tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy);
               if constexpr (G) tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy + p.N);
@@ -1290,7 +1339,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+          if (pair_leader) mbar_arrive_expect_tx(&full[s], C::kTxBytes);
           load_op(true, w, i, s);
           load_op(false, w, i, s);
         }
@@ -1298,17 +1347,20 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
     }
   } else if (warp == 1) {
     // ------------------------------------------------- UMMA issuer ----
-    if (lane == 0 && has_work) {
+    // (PR: the even CTA's thread issues for the pair)
+    if (lane == 0 && has_work && pair_leader) {
       uint32_t g = 0;     // ring iteration
       uint32_t blk = 0;   // TMEM buffer use (per K block when promoting, else per unit)
       bool ok = true;
-      WorkIter it = work_begin(p);
+      WorkIter it = work_begin<PR>(p);
       Unit w;
-      while (ok && work_next(p, BN, it, w)) {
+      while (ok && work_next<PR>(p, BN, it, w)) {
         if (!C::kPromote) {
           // one TMEM buffer per unit; wait until the epilogue drained it
+          // (PR: both CTAs' epilogues, the odd one's arrival remote)
           const int b = blk % NB;
-          if (!mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
+          const uint32_t tph = ((blk / NB) & 1u) ^ 1u;
+          if (!(PR ? mbar_wait_cluster(&tempty[b], tph, lim) : mbar_wait(&tempty[b], tph, lim))) {
             record_status(p.status, ST_TIMEOUT_MMA);
             ok = false;
             break;
@@ -1348,10 +1400,16 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
                 umma_f16_ts(d, pt + static_cast<uint32_t>(a * 4 + k) * 8u, bd, C::kIdesc, accum);
               } else {
                 const uint64_t ad = sdesc_k_sw128(pa + static_cast<uint32_t>(a) * 128u * 128u + 32u * k);
-                if (IN == IN_E4M3)
+                if constexpr (PR) {
+                  if (IN == IN_E4M3)
+                    umma_f8_pair(d, ad, bd, C::kIdesc, accum);
+                  else
+                    umma_f16_pair(d, ad, bd, C::kIdesc, accum);
+                } else if (IN == IN_E4M3) {
                   umma_f8(d, ad, bd, C::kIdesc, accum);
-                else
+                } else {
                   umma_f16(d, ad, bd, C::kIdesc, accum);
+                }
                 if constexpr (G) {
                   // up half: its weight tile replaces the gate's, same
                   // activation tile, accumulator columns [BN, 2 BN)
@@ -1366,19 +1424,31 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
               }
             }
           }
-          umma_commit(C::kConvert ? &bempty[os] : &empty[s]);
+          if constexpr (PR) {
+            umma_commit_pair(&empty[s]);  // frees the stage in both CTAs
+          } else {
+            umma_commit(C::kConvert ? &bempty[os] : &empty[s]);
+          }
           if (C::kPromote) {
             umma_commit(&tfull[b]);
             ++blk;
           }
         }
         if (!C::kPromote && ok) {
-          if (w.nk > 0) umma_commit(&tfull[blk % NB]);
+          if (w.nk > 0) {
+            if constexpr (PR)
+              umma_commit_pair(&tfull[blk % NB]);
+            else
+              umma_commit(&tfull[blk % NB]);
+          }
           ++blk;
         }
       }
       trace_point(p, TR_LAST_COMMIT);
-      umma_commit(mma_done);
+      if constexpr (PR)
+        umma_commit_pair(mma_done);
+      else
+        umma_commit(mma_done);
     }
   } else if (C::kConvert && warp >= 6) {
     // ---------------------------------- INT8 -> fp16 prologue transform ----
@@ -1390,9 +1460,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
       const uint32_t t_conv = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kAccCols;
       uint32_t g = 0;
       bool ok = true;
-      WorkIter it = work_begin(p);
+      WorkIter it = work_begin<PR>(p);
       Unit w;
-      while (ok && work_next(p, BN, it, w)) {
+      while (ok && work_next<PR>(p, BN, it, w)) {
         for (int i = 0; i < w.nk; ++i, ++g) {
           const int s = static_cast<int>(g % S);           // int8 ring stage
           const uint32_t ph = (g / S) & 1u;
@@ -1421,7 +1491,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
     const int quarter = warp & 3;
     const int lane_row = quarter * 32 + lane;
     constexpr int CPT = C::kColsPerThread;
-    static_assert(C::kPromote || CPT == BN, "the TMEM-resident path uses 4 epilogue warps");
+    static_assert(CPT % C::kCW == 0, "whole TMEM load chunks per thread");
+    static_assert(!G || CPT == BN, "gated units use 4 epilogue warps");
     // this thread's first column in the tile
     const int cbeg = (C::kEpiWarps == 4) ? 0 : ((warp - 2) >> 2) * CPT;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -1430,7 +1501,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
     griddep_wait();
     uint32_t blk = 0;
     bool ok = true;
-    WorkIter it = work_begin(p);
+    WorkIter it = work_begin<PR>(p);
     Unit w;
     // Block scales: without swap-AB (large M, many units per CTA) they are
     // staged one unit ahead, into the other of two buffers, so their global
@@ -1443,11 +1514,11 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
     uint32_t su = 0;
     if constexpr (kAhead) {
       Unit w0;
-      if (work_next(p, BN, it_pf, w0))
+      if (work_next<PR>(p, BN, it_pf, w0))
         stage_block_scales<SWAP, BN, C::kEpiThreads>(p, w0, scale_smem, ept);
       cp_async_commit();
     }
-    while (ok && work_next(p, BN, it, w)) {
+    while (ok && work_next<PR>(p, BN, it, w)) {
       const int row = w.row0 + lane_row;
       const uint32_t cur = su++;
       if constexpr (C::kPromote) {
@@ -1464,7 +1535,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
           // every thread is done with the other buffer (the previous unit's)
           epi_bar_sync(C::kEpiThreads);
           Unit wn;
-          if (work_next(p, BN, it_pf, wn))
+          if (work_next<PR>(p, BN, it_pf, wn))
             stage_block_scales<SWAP, BN, C::kEpiThreads>(
                 p, wn, scale_smem + ((cur + 1u) & 1u) * scale_buf_floats, ept);
           cp_async_commit();
@@ -1612,11 +1683,11 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
           }
           // this row's partial sums go to the CTA of the cluster owning it
 #pragma unroll 1
-          for (int c = 0; c < BN; c += CW) {
+          for (int c = 0; c < CPT; c += CW) {
             uint32_t r[CW];
             tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
             tmem_ld_wait();
-            cluster_send<BN, CW>(p, smem_u32(red_buf), red_full, w, lane_row, c, r);
+            cluster_send<BN, CW>(p, smem_u32(red_buf), red_full, w, lane_row, cbeg + c, r);
           }
           tc_fence_before();
           mbar_arrive(&tempty[b]);
@@ -1633,14 +1704,15 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
         }
         bool do_epi = true;
         if (w.contrib > 1) {
-          // every accumulator column of the unit (gated: gate, then up)
+          // this thread's accumulator columns of the unit (gated: all of
+          // them, gate then up)
 #pragma unroll 1
-          for (int c = 0; c < C::kAccN; c += CW) {
+          for (int c = 0; c < (G ? C::kAccN : CPT); c += CW) {
             uint32_t r[CW];
             tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
             tmem_ld_wait();
-            uint32_t* wsb = ws_slot<C::kAccN>(p, w.j, w.tile, c, lane_row);  // column stride 128
-            const int ct = c % BN;  // the chunk's first output column in the tile
+            uint32_t* wsb = ws_slot<C::kAccN>(p, w.j, w.tile, cbeg + c, lane_row);  // column stride 128
+            const int ct = (cbeg + c) % BN;  // the chunk's first output column in the tile
 #pragma unroll
             for (int j = 0; j < CW; ++j)
               if (row < p.rows && w.col0 + ct + j < p.cols) __stcg(wsb + j * 128, r[j]);
@@ -1649,7 +1721,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
         }
         if (do_epi) {
 #pragma unroll 1
-          for (int c = 0; c < BN; c += CW) {
+          for (int c = 0; c < CPT; c += CW) {
+            // this thread's columns cbeg + c ... (tb already points at cbeg)
+            const int cc = cbeg + c;
             uint32_t r[CW];
             if (w.nk > 0) {
               tmem_load_chunk<CW>(tb + static_cast<uint32_t>(c), r);
@@ -1662,8 +1736,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
               // partials summed in split order 0..S-1 (deterministic; this
               // CTA's own one is read back too); per split, the chunk's loads
               // are independent and overlap
-              reduce_partials<IN, C::kAccN, CW>(p, w.tile, w.contrib, c, lane_row, row < p.rows,
-                                                p.cols - (w.col0 + c), r);
+              reduce_partials<IN, C::kAccN, CW>(p, w.tile, w.contrib, cc, lane_row, row < p.rows,
+                                                p.cols - (w.col0 + cc), r);
             }
             if constexpr (G) {
               // the up half's columns of the same outputs
@@ -1687,12 +1761,19 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
                 continue;
               }
             }
-            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + c, r);
+            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + cc, r);
           }
         }
         // TMEM buffer b may take the unit after next
         tc_fence_before();
-        mbar_arrive(&tempty[b]);
+        if constexpr (PR) {
+          // every epilogue thread of this CTA is done with buffer b; one
+          // arrival on the even CTA's barrier
+          epi_bar_sync(C::kEpiThreads);
+          if (ept == 0) mbar_arrive_cluster(cluster_map(smem_u32(&tempty[b]), 0));
+        } else {
+          mbar_arrive(&tempty[b]);
+        }
         ++blk;
       }
     }
@@ -1702,8 +1783,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
   // ------------------------------------------------------------ teardown ---
   tc_fence_before();
   __syncthreads();
-  // no CTA of a cluster leaves while another may still write its buffer
-  if (p.cluster_reduce) cluster_sync_all();
+  // no CTA of a cluster leaves while another may still write its buffer (or,
+  // CTA pairs, still issue UMMAs into its tensor memory)
+  if (PR || p.cluster_reduce) cluster_sync_all();
   if (threadIdx.x == 0) trace_point(p, TR_END);
   if (warp == 1) {
     tc_fence_after();
@@ -1715,7 +1797,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G>::kThreads)
       if (!done && lane == 0) record_status(p.status, ST_TIMEOUT_TEARDOWN);
     }
     __syncwarp();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 

@@ -29,15 +29,19 @@ EG_DECLARE_LOOKUP(lookup_int8_tc)
 EG_DECLARE_LOOKUP(lookup_bf16_gated)
 EG_DECLARE_LOOKUP(lookup_e4m3_tc_gated)
 #undef EG_DECLARE_LOOKUP
+// CTA-pair kernels (no swap-AB): bf16 and FP8 per-token/channel.
+bool lookup_bf16_pair(int bn, KernelEntry* out);
+bool lookup_e4m3_tc_pair(int bn, KernelEntry* out);
 
 }  // namespace eg
 
 // Instantiation helpers used by the eg_kernels_*.cu files.
-#define EG_KERNEL_ENTRY(IN, SC, SWAP, BN) EG_KERNEL_ENTRY_G(IN, SC, SWAP, BN, false)
-#define EG_KERNEL_ENTRY_G(IN, SC, SWAP, BN, G)                                         \
+#define EG_KERNEL_ENTRY(IN, SC, SWAP, BN) EG_KERNEL_ENTRY_GP(IN, SC, SWAP, BN, false, false)
+#define EG_KERNEL_ENTRY_G(IN, SC, SWAP, BN, G) EG_KERNEL_ENTRY_GP(IN, SC, SWAP, BN, G, false)
+#define EG_KERNEL_ENTRY_GP(IN, SC, SWAP, BN, G, PR)                                    \
   do {                                                                                 \
-    using C_ = ::eg::Cfg<IN, SC, SWAP, BN, G>;                                         \
-    out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN, G>); \
+    using C_ = ::eg::Cfg<IN, SC, SWAP, BN, G, PR>;                                     \
+    out->fn = reinterpret_cast<const void*>(&::eg::fused_linear_kernel<IN, SC, SWAP, BN, G, PR>); \
     out->stage_bytes = C_::kStageBytes;                                                \
     out->fixed_bytes = 1024u + 512u + C_::kOpBytes;                                    \
     out->op_bytes = C_::kOpBytes;                                                      \

@@ -17,7 +17,7 @@ namespace {
 // Rows written by the offline sweep (bench/sweep tool); empty until swept.
 const TuningRow kTable[] = {
 #include "eg_tuning_table.inc"
-    {-1, -1, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
+    {-1, -1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
 
 // decode buckets, then the mid-range (prefill ramp) buckets
 constexpr int kBuckets[] = {1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048};
@@ -96,7 +96,8 @@ bool tuning_lookup(const eg_problem& p, int sms, eg_tuning* out) {
   for (const TuningRow& r : kTable) {
     if (r.dtype < 0) break;
     if (r.dtype == p.dtype && r.scale == p.scale && r.N == p.N && r.K == p.K && r.m_max == b) {
-      *out = eg_tuning{r.tile_n, r.stages, r.split_k, r.swap_ab, r.stream_k, r.cluster_reduce};
+      *out = eg_tuning{r.tile_n, r.stages, r.split_k, r.swap_ab, r.stream_k, r.cluster_reduce,
+                       r.cta_pair};
       return true;
     }
   }

@@ -12,7 +12,7 @@ struct TuningRow {
   int32_t dtype, scale;
   int64_t N, K;
   int32_t m_max;
-  int32_t tile_n, stages, split_k, swap_ab, stream_k, cluster_reduce;
+  int32_t tile_n, stages, split_k, swap_ab, stream_k, cluster_reduce, cta_pair;
 };
 
 // Fill *out for problem p on a device with `sms` SMs.  Returns false when

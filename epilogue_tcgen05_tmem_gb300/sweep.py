@@ -56,15 +56,15 @@ def candidates(p, swaps=(0, 1)):
                     if s > k_tiles or (s > 1 and k_tiles // s < 2):
                         continue
                     yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0,
-                               cluster_reduce=0)
+                               cluster_reduce=0, cta_pair=0)
                     # the same split reduced inside a cluster (2, 4 or 8 CTAs)
                     if s in (2, 4, 8):
                         yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0,
-                                   cluster_reduce=1)
+                                   cluster_reduce=1, cta_pair=0)
                 # balanced split-K with 1 or 2 CTAs per SM
                 for sk in (1, 2):
                     yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=swap, stream_k=sk,
-                               cluster_reduce=0)
+                               cluster_reduce=0, cta_pair=0)
 
 
 def _midrange_candidates(p, swaps, max_bn, k_tiles):
@@ -82,9 +82,19 @@ def _midrange_candidates(p, swaps, max_bn, k_tiles):
                     if s > k_tiles or (s > 1 and k_tiles // s < 2):
                         continue
                     yield dict(tile_n=bn, stages=stages, split_k=s, swap_ab=swap, stream_k=0,
-                               cluster_reduce=0)
+                               cluster_reduce=0, cta_pair=0)
                 yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=swap, stream_k=1,
-                           cluster_reduce=0)
+                           cluster_reduce=0, cta_pair=0)
+        # CTA pairs (256-row tiles, half the weight tile per CTA): plain
+        # per-token/channel or bf16 layers, rows over M
+        if swap or p.scale == "block" or p.dtype == "int8":
+            continue
+        for bn in (128, 256):
+            if bn > max_bn or (bn > 128 and bn // 2 >= cols):
+                continue
+            for stages in (4, 5, 6, 8):
+                yield dict(tile_n=bn, stages=stages, split_k=1, swap_ab=0, stream_k=0,
+                           cluster_reduce=0, cta_pair=1)
 
 
 def time_config(eg, torch, p, d, Ws, tuning, reps=3, calls=None):
@@ -167,7 +177,8 @@ def sweep(workload, tokens, swaps=(0, 1), verbose=True):
         c, t = pick(results)
         bucket = M if M <= 2048 else 0
         row = (eg.DTYPES[p.dtype], eg.SCALES[p.scale], p.N, p.K, bucket, c["tile_n"],
-               c["stages"], c["split_k"], c["swap_ab"], c["stream_k"], c["cluster_reduce"])
+               c["stages"], c["split_k"], c["swap_ab"], c["stream_k"], c["cluster_reduce"],
+               c["cta_pair"])
         rows.append(row)
         if verbose:
             top = sorted(results, key=lambda ct: ct[1])[:6]
@@ -188,7 +199,7 @@ def format_rows(rows, comment=""):
     if comment:
         out.append(f"// {comment}")
     for r in rows:
-        out.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % r)
+        out.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % r)
     return "\n".join(out) + "\n"
 
 

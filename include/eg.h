@@ -161,8 +161,9 @@ typedef struct {
   uint32_t flags; /* EG_EPI_* | EG_OUT_DEBUG_ACCUM | EG_RUN_* */
 } eg_problem;
 
-/* One point of the kernel's tuning space.  The UMMA tile is 128 rows by
- * tile_n columns; rows run over M, or over N when swap_ab is set. */
+/* One point of the kernel's tuning space.  The UMMA tile is 128 rows (256
+ * with cta_pair) by tile_n columns; rows run over M, or over N when swap_ab
+ * is set. */
 typedef struct {
   int32_t tile_n;   /* UMMA N: 16, 32, 64, 128 or 256 */
   int32_t stages;   /* shared-memory ring depth, 2..8 */
@@ -182,6 +183,14 @@ typedef struct {
                        split_k of the tile's rows (in split order, so the
                        result is the same) and runs their epilogue.  No
                        workspace or arrival counters are used. */
+  int32_t cta_pair;  /* 0: one CTA per 128-row tile.  1: CTA pairs: two CTAs
+                       of a 2-CTA cluster compute one 256-row tile with
+                       pair UMMAs (M = 256, cta_group::2), each holding its
+                       128 activation rows and half of the weight tile per
+                       stage, so each SM stages half as much of W.  bf16 or
+                       E4M3 per-token/channel, swap_ab 0, tile_n 128 or
+                       256, split_k 1, stream_k 0, cluster_reduce 0, not
+                       gated. */
 } eg_tuning;
 
 typedef struct {

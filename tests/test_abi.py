@@ -106,8 +106,9 @@ def test_binding_structs_match_header(name, cls):
 
 
 def test_tuning_table_rows_are_valid():
-    """Every swept row has the 11 fields of the table, and uses the cluster
-    reduction only with a split of 2, 4 or 8 and without balanced split-K."""
+    """Every swept row has the 12 fields of the table, uses the cluster
+    reduction only with a split of 2, 4 or 8 and without balanced split-K,
+    and CTA pairs only unsplit, without swap-AB, with tiles of 128 or 256."""
     import os
     import re
     path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
@@ -116,8 +117,8 @@ def test_tuning_table_rows_are_valid():
             for m in re.findall(r"^\s*\{([-\d, ]+)\},", open(path).read(), flags=re.M)]
     assert rows
     for r in rows:
-        assert len(r) == 11, r
-        dtype, scale, N, K, bucket, tn, stages, split, swap, sk, cl = r
+        assert len(r) == 12, r
+        dtype, scale, N, K, bucket, tn, stages, split, swap, sk, cl, pair = r
         assert bucket in (0, 1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048)
         assert tn in (16, 32, 64, 128, 256)
         assert 2 <= stages <= 8 and swap in (0, 1) and cl in (0, 1)
@@ -125,15 +126,33 @@ def test_tuning_table_rows_are_valid():
             assert split in (2, 4, 8) and sk == 0, r
         if sk:
             assert split == 1, r
+        assert pair in (0, 1)
+        if pair:
+            assert split == 1 and sk == 0 and cl == 0 and swap == 0 and tn in (128, 256), r
+            assert scale != 2 and dtype != 2, r
 
 
 def test_sweep_candidates_and_rows():
     from epilogue_tcgen05_tmem_gb300 import inputs, sweep
     p = inputs.make_problem(16, 1024, 4096, "e4m3", "token_channel", seed=0)
     cands = list(sweep.candidates(p, swaps=(1,)))
-    assert all(set(c) == {"tile_n", "stages", "split_k", "swap_ab", "stream_k", "cluster_reduce"}
-               for c in cands)
+    keys = {"tile_n", "stages", "split_k", "swap_ab", "stream_k", "cluster_reduce", "cta_pair"}
+    assert all(set(c) == keys for c in cands)
     cl = [c for c in cands if c["cluster_reduce"]]
     assert cl and all(c["split_k"] in (2, 4, 8) and c["stream_k"] == 0 for c in cl)
-    text = sweep.format_rows([(1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1)])
-    assert text.strip() == "{1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1},"
+    text = sweep.format_rows([(1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1, 0)])
+    assert text.strip() == "{1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1, 0},"
+
+
+def test_sweep_pair_candidates():
+    """Above the decode buckets the sweep also tries CTA pairs, only where the
+    pair kernels exist: no swap-AB, per-token/channel or bf16, unsplit."""
+    from epilogue_tcgen05_tmem_gb300 import inputs, sweep
+    p = inputs.make_problem(256, 512, 256, "e4m3", "token_channel", seed=0)
+    cands = list(sweep.candidates(p, swaps=(0, 1)))
+    pairs = [c for c in cands if c["cta_pair"]]
+    assert pairs
+    assert all(c["swap_ab"] == 0 and c["split_k"] == 1 and c["stream_k"] == 0
+               and c["cluster_reduce"] == 0 and c["tile_n"] in (128, 256) for c in pairs)
+    pb = inputs.make_problem(256, 512, 256, "e4m3", "block", seed=0)
+    assert not [c for c in sweep.candidates(pb, swaps=(0,)) if c["cta_pair"]]

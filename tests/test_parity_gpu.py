@@ -13,8 +13,8 @@ import torch
 import epilogue_tcgen05_tmem_gb300 as eg
 import oracle
 from epilogue_tcgen05_tmem_gb300 import inputs
-from tests._gpu_helpers import (assert_close_out, assert_close_rms, bits, make_plan, run,
-                                to_device, ulp_dist)
+from tests._gpu_helpers import (assert_close_out, assert_close_rms, bits, canaries_intact,
+                                make_plan, run, to_device, ulp_dist)
 
 pytestmark = pytest.mark.gpu
 
@@ -378,6 +378,8 @@ CLUSTER_CASES = [
     ("bf16", "none", 200, 136, 512, 32, 0, 2),              # rows over M, ragged both ways
     ("e4m3", "block", 8, 1024, 1024, 16, 1, 4),
     ("e4m3", "block", 130, 384, 1024, 64, 0, 2),            # 8 epilogue warps
+    ("e4m3", "token_channel", 130, 640, 2048, 256, 0, 2),   # 8 epilogue warps, TMEM path
+    ("bf16", "none", 200, 384, 1024, 128, 0, 4),
 ]
 
 
@@ -581,3 +583,75 @@ def test_balanced_split_k_with_data_parallel_waves(dtype, scale, tn):
     plan.close()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), "not deterministic"
     assert_close_rms(bits(y1), oracle.linear(p))
+
+
+# ------------------------------------------------------------ CTA pairs ----
+
+PAIR_CASES = [
+    # M, N, K, tile_n: one pair row; ragged M/N/K (odd CTA partly empty);
+    # M < 128 (odd CTA has no rows); more units than pairs (persistent)
+    (256, 512, 512, 128),
+    (300, 640, 1008, 256),
+    (100, 384, 256, 128),
+    (2048, 3072, 512, 256),
+]
+
+
+@pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel")])
+@pytest.mark.parametrize("M,N,K,tn", PAIR_CASES)
+def test_cta_pair(dtype, scale, M, N, K, tn):
+    """Pair UMMAs over a 2-CTA cluster (256-row tiles, half the weight tile
+    per CTA) meet the bound against the oracle and are deterministic."""
+    p = inputs.make_problem(M, N, K, dtype, scale, act="silu", bias=True, residual=True, seed=41)
+    plan = make_plan(p, dict(tile_n=tn, stages=4, split_k=1, swap_ab=0, cta_pair=1))
+    li = plan.launch_info
+    assert plan.tuning["cta_pair"] == 1
+    assert li["grid"] % 2 == 0 and li["units"] == -(-M // 256) * -(-N // tn)
+    d = to_device(p)
+    y1, _ = run(p, plan=plan, d=d)
+    y2, _ = run(p, plan=plan, d=d)
+    assert canaries_intact(d)
+    plan.close()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), "not deterministic"
+    assert_close_rms(bits(y1), oracle.linear(p))
+
+
+def test_cta_pair_prefill_epilogue():
+    """bf16 pair tiles with the prefill epilogue (bias + residual, then tanh
+    GELU) and deeper rings."""
+    p = inputs.make_problem(512, 768, 1024, "bf16", act="gelu_tanh", bias=True, residual=True,
+                            residual_pre_act=True, seed=43)
+    for stages in (5, 6):
+        y, _ = run(p, dict(tile_n=256, stages=stages, split_k=1, swap_ab=0, cta_pair=1))
+        assert_close_rms(bits(y), oracle.linear(p))
+
+
+@pytest.mark.parametrize("t", [
+    dict(tile_n=128, stages=4, split_k=1, swap_ab=1, cta_pair=1),
+    dict(tile_n=128, stages=4, split_k=2, swap_ab=0, cta_pair=1),
+    dict(tile_n=64, stages=4, split_k=1, swap_ab=0, cta_pair=1),
+    dict(tile_n=128, stages=4, split_k=1, swap_ab=0, stream_k=1, cta_pair=1),
+])
+def test_cta_pair_unsupported_tunings(t):
+    p = inputs.make_problem(256, 512, 512, "e4m3", "token_channel", seed=1)
+    with pytest.raises(eg.EgError):
+        make_plan(p, t)
+
+
+def test_cta_pair_rejects_block_scales():
+    p = inputs.make_problem(256, 512, 512, "e4m3", "block", seed=1)
+    with pytest.raises(eg.EgError):
+        make_plan(p, dict(tile_n=128, stages=3, split_k=1, swap_ab=0, cta_pair=1))
+
+
+@pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel")])
+@pytest.mark.parametrize("t", [dict(split_k=3, stream_k=0), dict(split_k=1, stream_k=1)])
+@pytest.mark.parametrize("tn", [128, 256])
+def test_wide_tile_split_k(dtype, scale, t, tn):
+    """Wide tiles without swap-AB (eight epilogue warps, each owning half of
+    a TMEM lane quarter's columns) through the split-K workspace and
+    balanced split-K."""
+    p = inputs.make_problem(300, 768, 2048, dtype, scale, act="gelu_tanh", bias=True,
+                            residual=True, seed=45)
+    y, _ = run(p, dict(tile_n=tn, stages=4, swap_ab=0, **t))
+    assert_close_rms(bits(y), oracle.linear(p))
