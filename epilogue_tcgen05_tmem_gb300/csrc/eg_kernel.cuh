@@ -160,12 +160,18 @@ struct Cfg {
   static constexpr int kWarpsPerSmsp = (kMinBlocks * (kThreads / 32) + 3) / 4;
   static constexpr int kMaxRegs =
       (512 / kWarpsPerSmsp) / 8 * 8 > 255 ? 255 : (512 / kWarpsPerSmsp) / 8 * 8;
-  static constexpr int kCW = BN < 32 ? BN : 32;            // TMEM load chunk (columns)
+  // TMEM load chunk (columns): 32, or 16 where a thread's share of a wide
+  // tile is not a multiple of 32 (tile_n 224 over two column halves)
+  static constexpr int kCW = BN < 32 ? BN : (kColsPerThread % 32 != 0 ? 16 : 32);
   // TMEM accumulator buffers: 2 (one unit drains while the next fills), or
   // 4 when promoting K blocks so UMMA runs further ahead of the epilogue
   static constexpr int kAccBufs = (kPromote && 4 * BN <= 512) ? 4 : 2;
   static constexpr int kAccN = G ? 2 * BN : BN;  // accumulator columns of one unit
-  static constexpr uint32_t kAccCols = kAccBufs * kAccN;
+  // TMEM columns between accumulator buffers: a unit's columns, rounded up
+  // to 256 for tiles between 128 and 256 columns (192, 224) so every buffer
+  // starts at column 0 or 256
+  static constexpr int kAccStride = (kAccN > 128 && kAccN < 256) ? 256 : kAccN;
+  static constexpr uint32_t kAccCols = kAccBufs * kAccStride;
   static constexpr uint32_t kTmemACols = kConvert ? kOpSlots * 64u : 0u;  // fp16 P, 128 K each
   static constexpr uint32_t kTmemUsed = kAccCols + kTmemACols;
   static constexpr uint32_t kTmemCols =
@@ -1385,7 +1391,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           }
           tc_fence_after();
           if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
-          const uint32_t d = tmem_base + static_cast<uint32_t>(b * C::kAccN);
+          const uint32_t d = tmem_base + static_cast<uint32_t>(b * C::kAccStride);
           const uint32_t pa = smem_u32(op_base(g));
           const uint32_t qa = C::kConvert ? pa : pa + C::kPBytes;
           // INT8: P is in tensor memory, buffer os, 8 columns per K step of 16
@@ -1653,7 +1659,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
       } else {
         // ---- accumulator in TMEM buffer blk&1 until the unit is done ----
         const int b = blk % NB;
-        const uint32_t tb = t_lane + static_cast<uint32_t>(b * C::kAccN);
+        const uint32_t tb = t_lane + static_cast<uint32_t>(b * C::kAccStride);
         // swap-AB with one chunk (decode): epilogue inputs load while the
         // mainloop runs
         constexpr bool kPre = SWAP && BN == CW && !G;

@@ -11,6 +11,8 @@ bool lookup_e4m3_tc_noswap(int bn, KernelEntry* out) {
     case 32: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, false, 32);
     case 64: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, false, 64);
     case 128: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, false, 128);
+    case 192: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, false, 192);
+    case 224: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, false, 224);
     case 256: EG_KERNEL_ENTRY(IN_E4M3, SC_TC, false, 256);
     default: return false;
   }

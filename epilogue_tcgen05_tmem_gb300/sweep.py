@@ -74,8 +74,12 @@ def _midrange_candidates(p, swaps, max_bn, k_tiles):
         cols = p.M if swap else p.N
         if swap and p.M > 256:
             continue
-        for bn in (64, 128, 256):
+        for bn in (64, 128, 192, 224, 256):
             if bn > max_bn or (bn > 64 and bn // 2 >= cols):
+                continue
+            # tile_n 192 and 224 (whole waves for some N) exist without
+            # swap-AB for bf16 and per-token/channel FP8
+            if bn in (192, 224) and (swap or p.scale == "block" or p.dtype == "int8"):
                 continue
             for stages in (3, 4, 6):
                 for s in (1, 2, 4):

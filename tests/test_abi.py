@@ -120,7 +120,9 @@ def test_tuning_table_rows_are_valid():
         assert len(r) == 12, r
         dtype, scale, N, K, bucket, tn, stages, split, swap, sk, cl, pair = r
         assert bucket in (0, 1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048)
-        assert tn in (16, 32, 64, 128, 256)
+        assert tn in (16, 32, 64, 128, 192, 224, 256)
+        if tn in (192, 224):
+            assert swap == 0 and scale != 2 and dtype != 2, r
         assert 2 <= stages <= 8 and swap in (0, 1) and cl in (0, 1)
         if cl:
             assert split in (2, 4, 8) and sk == 0, r

@@ -645,13 +645,15 @@ def test_cta_pair_rejects_block_scales():
 
 
 @pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel")])
-@pytest.mark.parametrize("t", [dict(split_k=3, stream_k=0), dict(split_k=1, stream_k=1)])
-@pytest.mark.parametrize("tn", [128, 256])
+@pytest.mark.parametrize("t", [dict(split_k=1, stream_k=0), dict(split_k=3, stream_k=0),
+                               dict(split_k=1, stream_k=1)])
+@pytest.mark.parametrize("tn", [128, 192, 224, 256])
 def test_wide_tile_split_k(dtype, scale, t, tn):
     """Wide tiles without swap-AB (eight epilogue warps, each owning half of
-    a TMEM lane quarter's columns) through the split-K workspace and
-    balanced split-K."""
-    p = inputs.make_problem(300, 768, 2048, dtype, scale, act="gelu_tanh", bias=True,
+    a TMEM lane quarter's columns; tile_n 192 and 224 with accumulator
+    buffers 256 columns apart), unsplit, through the split-K workspace and
+    balanced split-K; N = 700 leaves a ragged last tile column."""
+    p = inputs.make_problem(300, 700, 2048, dtype, scale, act="gelu_tanh", bias=True,
                             residual=True, seed=45)
     y, _ = run(p, dict(tile_n=tn, stages=4, swap_ab=0, **t))
     assert_close_rms(bits(y), oracle.linear(p))
