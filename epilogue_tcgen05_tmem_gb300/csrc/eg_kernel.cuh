@@ -1371,15 +1371,21 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             ok = false;
             break;
           }
+          // the epilogue's tensor-memory reads of buffer b are ordered
+          // before this unit's UMMAs overwrite it
+          tc_fence_after();
         }
         for (int i = 0; i < w.nk; ++i, ++g) {
           const int s = static_cast<int>(g % S);
           const uint32_t ph = (g / S) & 1u;
           const int b = blk % NB;
-          if (C::kPromote && !mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
-            record_status(p.status, ST_TIMEOUT_MMA);
-            ok = false;
-            break;
+          if (C::kPromote) {
+            if (!mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
+              record_status(p.status, ST_TIMEOUT_MMA);
+              ok = false;
+              break;
+            }
+            tc_fence_after();  // as above, per K block
           }
           // INT8: fp16 operand slot g%2 (its own phase); else the ring stage
           const int os = static_cast<int>(g % C::kOpSlots);
@@ -1389,7 +1395,12 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             ok = false;
             break;
           }
-          tc_fence_after();
+          // INT8: the converting threads wrote the A operand into tensor
+          // memory (tcgen05.st) before their arrival, so their tcgen05 ops
+          // are ordered before these UMMAs.  TMA-loaded stages need no
+          // tcgen05 fence: the stage barrier's transaction count makes the
+          // bulk copies visible to the UMMAs.
+          if constexpr (C::kConvert) tc_fence_after();
           if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
           const uint32_t d = tmem_base + static_cast<uint32_t>(b * C::kAccStride);
           const uint32_t pa = smem_u32(op_base(g));
