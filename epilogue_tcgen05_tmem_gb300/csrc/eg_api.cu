@@ -111,6 +111,7 @@ struct eg_plan {
   uint64_t wait_limit_ns = 0;
   int stall = 0;
   int l2_prefetch = 1;  // EG_PDL_L2_PREFETCH=0 turns the L2 weight prefetch off
+  int commit_group = 1; // ring stages released per UMMA commit (see commit_group_for)
   int units = 0, blocks_per_sm = 0, regs = 0, max_contrib = 1;
   uint64_t* trace = nullptr;
   int trace_ctas = 0;
@@ -499,6 +500,7 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.s_y = a->s_y;
   k.pdl = (p.flags & EG_RUN_PDL) ? 1 : 0;
   k.l2_prefetch = pl->l2_prefetch;
+  k.commit_group = pl->commit_group;
   k.trace = pl->trace;
   k.trace_ctas = pl->trace_ctas;
   k.cluster_reduce = pl->tune.cluster_reduce;
@@ -508,6 +510,28 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.evict_first_p = pl->tune.swap_ab ? w_once : 0;
   k.evict_first_q = pl->tune.swap_ab ? 0 : w_once;
   return k;
+}
+
+// Ring stages the UMMA issuer releases with one commit.  A tcgen05.commit
+// stalls the tensor pipe for a few hundred cycles unless enough UMMAs are
+// queued behind it (measured on GB300 with back-to-back 128 x 256 UMMAs: 4
+// per commit run at ~61% of the UMMA rate, 8 at ~81%, 16 at ~97%).
+// Releasing stages in pairs halves the commits but hands the producer two
+// stages at a time, which exposes the load latency in a 4-stage ring; with
+// the 6-stage rings of CTA pairs it pays (bf16 prefill 4096^3: 111 -> 105
+// us).  So: pairs of stages for CTA pairs with an even ring of 6 or more,
+// else one stage per commit.  Promotion (block scales, INT8) commits its
+// accumulator per K block anyway.  EG_COMMIT_GROUP=n overrides (n must
+// divide the stages).
+int commit_group_for(const eg_problem& p, const eg_tuning& t) {
+  const bool promote = p.scale == EG_SCALE_BLOCK || p.dtype == EG_IN_INT8;
+  if (promote) return 1;
+  int g = (t.cta_pair && t.stages >= 6 && t.stages % 2 == 0) ? 2 : 1;
+  if (const char* e = getenv("EG_COMMIT_GROUP")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= t.stages && t.stages % v == 0) g = v;
+  }
+  return g;
 }
 
 uint32_t epi_flags(uint32_t f) {
@@ -701,6 +725,7 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   pl->tiles_cols = (pl->cols + t.tile_n - 1) / t.tile_n;
   pl->wait_limit_ns = default_wait_limit_ns();
   if (const char* e2 = getenv("EG_PDL_L2_PREFETCH")) pl->l2_prefetch = atoi(e2) != 0;
+  pl->commit_group = commit_group_for(p, t);
   auto cleanup = [&](eg_status st) {
     eg_plan_destroy(pl);
     return st;
@@ -1018,6 +1043,7 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   pl.tiles_rows = t.cta_pair ? (pl.rows + 255) / 256 : (pl.rows + 127) / 128;
   pl.tiles_cols = (pl.cols + t.tile_n - 1) / t.tile_n;
   pl.wait_limit_ns = default_wait_limit_ns();
+  pl.commit_group = commit_group_for(p, t);
   if ((s = validate_args(&pl, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0)) != EG_OK) return s;
   if (p.M == 0 || p.N == 0) return EG_OK;
 

@@ -82,6 +82,7 @@ struct KParams {
   int32_t vec_ok;                 // Y (and R) rows 16-byte aligned: vector path
   int32_t pdl;                    // launched as a programmatic dependent
   int32_t l2_prefetch;            // ... and prefetches its weight range into L2
+  int32_t commit_group;           // ring stages released per UMMA commit (divides stages)
   uint64_t* trace;                // per-CTA timeline (nullable), kTracePoints each
   int32_t trace_ctas;             // CTAs the trace buffer holds
   int32_t stream_k;               // balanced split-K over the grid (else split_k)
@@ -1166,6 +1167,33 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
 // TMEM accumulator buffers and promotion buffers carry their phases across
 // units, so the epilogue of one unit overlaps the UMMA mainloop of the next.
 
+// Position in the ring of S stages whose stages are released in groups of CG
+// (NG = S / CG group slots): stage and the parity of its current use, index
+// within the group, group slot and the parity of its current use.  Kept as
+// counters: the producer and the UMMA issuer are single threads whose
+// per-stage instruction latency sits on the tensor pipe's critical path,
+// and a division by a runtime ring depth costs it a few hundred cycles.
+struct RingPos {
+  int s;
+  uint32_t ph;
+  int gi, gs;
+  uint32_t gph;
+};
+
+__device__ __forceinline__ void ring_next(RingPos& r, int S, int CG, int NG) {
+  if (++r.s == S) {
+    r.s = 0;
+    r.ph ^= 1u;
+  }
+  if (++r.gi == CG) {
+    r.gi = 0;
+    if (++r.gs == NG) {
+      r.gs = 0;
+      r.gph ^= 1u;
+    }
+  }
+}
+
 template <int IN, int SC, bool SWAP, int BN, bool G = false, bool PR = false>
 __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     __maxnreg__((Cfg<IN, SC, SWAP, BN, G, PR>::kMaxRegs))
@@ -1177,6 +1205,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
+  const int CG = p.commit_group > 0 ? p.commit_group : 1;  // divides S (host)
+  const int NG = S / CG;
   // Shared memory: [TMA ring: S stages of (P | Q), or (P8 | Q8) for INT8]
   // [INT8: 2 fp16 operand slots of (P | Q)] [barriers, 512 B] [block scales].
   // Every tile part is a multiple of 1 KB, so 1024-byte alignment holds.
@@ -1184,9 +1214,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
   uint8_t* op_area = smem + static_cast<uint32_t>(S) * C::kStageBytes;
   // UMMA operands of ring iteration g: the ring stage itself, or (INT8) the
   // fp16 slot the transform warps wrote
-  auto op_base = [&](uint32_t g) {
-    return C::kConvert ? op_area + (g % C::kOpSlots) * C::kQBytes
-                       : stage_base(static_cast<int>(g % S));
+  auto op_base = [&](uint32_t g, int s) {
+    return C::kConvert ? op_area + (g % C::kOpSlots) * C::kQBytes : stage_base(s);
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(op_area + C::kOpBytes);
   uint64_t* full = bars;              // TMA landed (expect_tx)
@@ -1306,7 +1335,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           }
         }
       };
-      uint32_t g = 0;  // ring iteration across units
+      RingPos rp = {0, 0u, 0, 0, 0u};  // ring position across units
       bool first = true;
       bool ok = true;
       WorkIter it = work_begin<PR>(p);
@@ -1335,12 +1364,13 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           for (int i = 0; i < pre; ++i) load_op(false, w, i, i);
           trace_point(p, TR_FIRST_TMA);
           i0 = pre;
-          g = pre;
+          for (int i = 0; i < pre; ++i) ring_next(rp, S, CG, NG);
         }
-        for (int i = i0; i < w.nk; ++i, ++g) {
-          const int s = static_cast<int>(g % S);
-          const uint32_t ph = (g / S) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, lim)) {
+        for (int i = i0; i < w.nk; ++i) {
+          const int s = rp.s;
+          // stages are released in groups of CG by one commit on the
+          // group's barrier: wait for the previous use of this group slot
+          if (!mbar_wait(&empty[rp.gs], rp.gph ^ 1u, lim)) {
             record_status(p.status, ST_TIMEOUT_PRODUCER);
             ok = false;
             break;
@@ -1348,6 +1378,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           if (pair_leader) mbar_arrive_expect_tx(&full[s], C::kTxBytes);
           load_op(true, w, i, s);
           load_op(false, w, i, s);
+          ring_next(rp, S, CG, NG);
         }
       }
     }
@@ -1355,7 +1386,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     // ------------------------------------------------- UMMA issuer ----
     // (PR: the even CTA's thread issues for the pair)
     if (lane == 0 && has_work && pair_leader) {
-      uint32_t g = 0;     // ring iteration
+      uint32_t g = 0;     // ring iteration (INT8 operand slots: g mod 2)
+      RingPos rm = {0, 0u, 0, 0, 0u};  // ring position of iteration g
       uint32_t blk = 0;   // TMEM buffer use (per K block when promoting, else per unit)
       bool ok = true;
       WorkIter it = work_begin<PR>(p);
@@ -1375,9 +1407,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           // before this unit's UMMAs overwrite it
           tc_fence_after();
         }
-        for (int i = 0; i < w.nk; ++i, ++g) {
-          const int s = static_cast<int>(g % S);
-          const uint32_t ph = (g / S) & 1u;
+        for (int i = 0; i < w.nk; ++i, ++g, ring_next(rm, S, CG, NG)) {
+          const int s = rm.s;
+          const uint32_t ph = rm.ph;
           const int b = blk % NB;
           if (C::kPromote) {
             if (!mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
@@ -1403,7 +1435,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           if constexpr (C::kConvert) tc_fence_after();
           if (g == 0) trace_point(p, TR_FIRST_OPERANDS);
           const uint32_t d = tmem_base + static_cast<uint32_t>(b * C::kAccStride);
-          const uint32_t pa = smem_u32(op_base(g));
+          const uint32_t pa = smem_u32(op_base(g, s));
           const uint32_t qa = C::kConvert ? pa : pa + C::kPBytes;
           // INT8: P is in tensor memory, buffer os, 8 columns per K step of 16
           const uint32_t pt = tmem_base + C::kAccCols + static_cast<uint32_t>(os) * 64u;
@@ -1441,10 +1473,17 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
               }
             }
           }
-          if constexpr (PR) {
-            umma_commit_pair(&empty[s]);  // frees the stage in both CTAs
-          } else {
-            umma_commit(C::kConvert ? &bempty[os] : &empty[s]);
+          // one commit per group of CG stages: a commit costs the tensor
+          // pipe a bubble of a few hundred cycles unless enough UMMAs
+          // follow it, so every-stage commits of 4 UMMAs run at ~60% rate
+          if (C::kConvert) {
+            umma_commit(&bempty[os]);
+          } else if (rm.gi == CG - 1) {
+            uint64_t* eb = &empty[rm.gs];  // the last stage of this group is done
+            if constexpr (PR)
+              umma_commit_pair(eb);  // frees the stages in both CTAs
+            else
+              umma_commit(eb);
           }
           if (C::kPromote) {
             umma_commit(&tfull[b]);
@@ -1476,13 +1515,14 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
       const int conv_row = (warp & 3) * 32 + lane;
       const uint32_t t_conv = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kAccCols;
       uint32_t g = 0;
+      RingPos rc = {0, 0u, 0, 0, 0u};
       bool ok = true;
       WorkIter it = work_begin<PR>(p);
       Unit w;
       while (ok && work_next<PR>(p, BN, it, w)) {
-        for (int i = 0; i < w.nk; ++i, ++g) {
-          const int s = static_cast<int>(g % S);           // int8 ring stage
-          const uint32_t ph = (g / S) & 1u;
+        for (int i = 0; i < w.nk; ++i, ++g, ring_next(rc, S, 1, S)) {
+          const int s = rc.s;                               // int8 ring stage
+          const uint32_t ph = rc.ph;
           const int os = static_cast<int>(g % C::kOpSlots);  // fp16 operand slot
           const uint32_t oph = (g / C::kOpSlots) & 1u;
           if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[os], oph ^ 1u, lim)) {
@@ -1494,7 +1534,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           // P row -> tensor memory (buffer os); Q -> fp16 shared slot os
           convert_row_to_tmem(stage_base(s), t_conv + static_cast<uint32_t>(os) * 64u, conv_row);
           static_assert(BN % 16 == 0, "Q tile rows come in groups of 16");
-          convert_tile<BN / 16>(stage_base(s) + C::kP8Bytes, op_base(g), BN, ct);
+          convert_tile<BN / 16>(stage_base(s) + C::kP8Bytes, op_base(g, s), BN, ct);
           tmem_st_wait();
           tc_fence_before();
           fence_proxy_async_smem();

@@ -657,3 +657,18 @@ def test_wide_tile_split_k(dtype, scale, t, tn):
                             residual=True, seed=45)
     y, _ = run(p, dict(tile_n=tn, stages=4, swap_ab=0, **t))
     assert_close_rms(bits(y), oracle.linear(p))
+
+
+def test_prefill_full_size_sampled():
+    """The bf16 prefill block at its full size (4096^3, bias + residual, then
+    tanh GELU) with the table's tuning (CTA pairs, stages released two per
+    commit), sampled outputs against the oracle, plus the single-CTA tiles
+    with one stage per commit."""
+    p = inputs.workload("prefill_bf16")
+    plan = make_plan(p)
+    assert plan.tuning["cta_pair"] == 1
+    y, _ = run(p, plan=plan)
+    plan.close()
+    _sampled(p, y, npts=2000)
+    y2, _ = run(p, dict(tile_n=256, stages=4, split_k=1, swap_ab=0))
+    _sampled(p, y2, npts=500, seed=1)
