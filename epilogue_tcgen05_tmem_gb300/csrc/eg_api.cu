@@ -112,6 +112,7 @@ struct eg_plan {
   int stall = 0;
   int l2_prefetch = 1;  // EG_PDL_L2_PREFETCH=0 turns the L2 weight prefetch off
   int commit_group = 1; // ring stages released per UMMA commit (see commit_group_for)
+  int acc_release = 0;  // promotion frees stages / INT8 slots by the accumulator commit
   int units = 0, blocks_per_sm = 0, regs = 0, max_contrib = 1;
   uint64_t* trace = nullptr;
   int trace_ctas = 0;
@@ -501,6 +502,7 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.pdl = (p.flags & EG_RUN_PDL) ? 1 : 0;
   k.l2_prefetch = pl->l2_prefetch;
   k.commit_group = pl->commit_group;
+  k.acc_release = pl->acc_release;
   k.trace = pl->trace;
   k.trace_ctas = pl->trace_ctas;
   k.cluster_reduce = pl->tune.cluster_reduce;
@@ -532,6 +534,19 @@ int commit_group_for(const eg_problem& p, const eg_tuning& t) {
     if (v >= 1 && v <= t.stages && t.stages % v == 0) g = v;
   }
   return g;
+}
+
+// Promotion commits each K block's accumulator (4 accumulator buffers); that
+// commit also says the block's UMMAs have read their ring stage (block
+// scales) or fp16 operand slot (INT8), so the stage / slot needs no commit
+// of its own.  A stage is then freed S blocks later, which is safe while S
+// <= 4 (the accumulator buffer's next commit cannot have happened yet).
+int acc_release_for(const eg_problem& p, const eg_tuning& t) {
+  if (const char* e = getenv("EG_ACC_RELEASE"))
+    if (atoi(e) == 0) return 0;
+  if (p.dtype == EG_IN_INT8) return 1;
+  if (p.scale == EG_SCALE_BLOCK) return t.stages <= 4 ? 1 : 0;
+  return 0;
 }
 
 uint32_t epi_flags(uint32_t f) {
@@ -726,6 +741,7 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   pl->wait_limit_ns = default_wait_limit_ns();
   if (const char* e2 = getenv("EG_PDL_L2_PREFETCH")) pl->l2_prefetch = atoi(e2) != 0;
   pl->commit_group = commit_group_for(p, t);
+  pl->acc_release = acc_release_for(p, t);
   auto cleanup = [&](eg_status st) {
     eg_plan_destroy(pl);
     return st;
@@ -1044,6 +1060,7 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   pl.tiles_cols = (pl.cols + t.tile_n - 1) / t.tile_n;
   pl.wait_limit_ns = default_wait_limit_ns();
   pl.commit_group = commit_group_for(p, t);
+  pl.acc_release = acc_release_for(p, t);
   if ((s = validate_args(&pl, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0)) != EG_OK) return s;
   if (p.M == 0 || p.N == 0) return EG_OK;
 

@@ -83,6 +83,9 @@ struct KParams {
   int32_t pdl;                    // launched as a programmatic dependent
   int32_t l2_prefetch;            // ... and prefetches its weight range into L2
   int32_t commit_group;           // ring stages released per UMMA commit (divides stages)
+  int32_t acc_release;            // promotion: the per-K-block accumulator commit also
+                                  // frees the block's ring stage (block scales, stages
+                                  // <= accumulator buffers) or INT8 operand slot
   uint64_t* trace;                // per-CTA timeline (nullable), kTracePoints each
   int32_t trace_ctas;             // CTAs the trace buffer holds
   int32_t stream_k;               // balanced split-K over the grid (else split_k)
@@ -1336,6 +1339,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
         }
       };
       RingPos rp = {0, 0u, 0, 0, 0u};  // ring position across units
+      uint32_t gp = 0;                 // ring iteration (= K block when promoting)
+      // block scales: a stage is free once the accumulator commit of the K
+      // block that used it (S iterations back) has arrived
+      const bool stage_by_acc = C::kPromote && !C::kConvert && p.acc_release;
       bool first = true;
       bool ok = true;
       WorkIter it = work_begin<PR>(p);
@@ -1365,12 +1372,20 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           trace_point(p, TR_FIRST_TMA);
           i0 = pre;
           for (int i = 0; i < pre; ++i) ring_next(rp, S, CG, NG);
+          gp = static_cast<uint32_t>(pre);
         }
         for (int i = i0; i < w.nk; ++i) {
           const int s = rp.s;
           // stages are released in groups of CG by one commit on the
           // group's barrier: wait for the previous use of this group slot
-          if (!mbar_wait(&empty[rp.gs], rp.gph ^ 1u, lim)) {
+          bool free_ok;
+          if (stage_by_acc) {
+            const uint32_t j = gp - static_cast<uint32_t>(S);  // used only when gp >= S
+            free_ok = gp < static_cast<uint32_t>(S) || mbar_wait(&tfull[j % NB], (j / NB) & 1u, lim);
+          } else {
+            free_ok = mbar_wait(&empty[rp.gs], rp.gph ^ 1u, lim);
+          }
+          if (!free_ok) {
             record_status(p.status, ST_TIMEOUT_PRODUCER);
             ok = false;
             break;
@@ -1379,6 +1394,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           load_op(true, w, i, s);
           load_op(false, w, i, s);
           ring_next(rp, S, CG, NG);
+          ++gp;
         }
       }
     }
@@ -1477,7 +1493,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           // pipe a bubble of a few hundred cycles unless enough UMMAs
           // follow it, so every-stage commits of 4 UMMAs run at ~60% rate
           if (C::kConvert) {
-            umma_commit(&bempty[os]);
+            if (!p.acc_release) umma_commit(&bempty[os]);
+          } else if (C::kPromote && p.acc_release) {
+            // the stage is freed by the accumulator commit below
           } else if (rm.gi == CG - 1) {
             uint64_t* eb = &empty[rm.gs];  // the last stage of this group is done
             if constexpr (PR)
@@ -1525,7 +1543,14 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           const uint32_t ph = rc.ph;
           const int os = static_cast<int>(g % C::kOpSlots);  // fp16 operand slot
           const uint32_t oph = (g / C::kOpSlots) & 1u;
-          if (!mbar_wait(&full[s], ph, lim) || !mbar_wait(&bempty[os], oph ^ 1u, lim)) {
+          // the fp16 slot os was last read by the UMMAs of K block g - 2: its
+          // accumulator commit (or the slot's own commit) says they are done
+          const bool slot_ok =
+              p.acc_release
+                  ? (g < static_cast<uint32_t>(C::kOpSlots) ||
+                     mbar_wait(&tfull[(g - C::kOpSlots) % NB], ((g - C::kOpSlots) / NB) & 1u, lim))
+                  : mbar_wait(&bempty[os], oph ^ 1u, lim);
+          if (!mbar_wait(&full[s], ph, lim) || !slot_ok) {
             record_status(p.status, ST_TIMEOUT_CONVERT);
             ok = false;
             break;
