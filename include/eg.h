@@ -212,7 +212,15 @@ typedef struct eg_plan eg_plan;
  * counters and status word on the current device.  Returns
  * EG_ERR_INVALID_ARG for an inconsistent problem, EG_ERR_UNSUPPORTED for an
  * unsupported device or tuning, EG_ERR_NO_MEMORY / EG_ERR_CUDA on device
- * failures.  On success *out owns a new plan. */
+ * failures.  On success *out owns a new plan.
+ *
+ * Environment overrides read at plan creation, for measurements only:
+ * EG_PDL_L2_PREFETCH=0 (no L2 prefetch of the weight range as a programmatic
+ * dependent), EG_COMMIT_GROUP=n (ring stages released per UMMA commit; n must
+ * divide the stages; default two for CTA pairs with 6+ even stages, else
+ * one), EG_ACC_RELEASE=0 (promotion kernels release ring stages / INT8
+ * operand slots with their own commit instead of the K block's accumulator
+ * commit), EG_WAIT_CAP_MS (bound on any in-kernel wait). */
 EG_API eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning,
                          eg_plan** out);
 
