@@ -5,14 +5,22 @@ K=4096, N=12288, per-token activation and per-channel weight scales, + bias,
 SiLU, bf16 out, at every token bucket M in {1, 2, 4, 8, 16, 24, 32}.
 
 One step = one fused call per token bucket on each of NSETS independent
-weight sets (7 x NSETS calls).  The sets rotate so that a weight set is
-touched again only after more than twice the L2 capacity of other weights
-has streamed through; each call therefore reads its weights from HBM.  The
-calls of one step are captured once into a CUDA graph per step and replayed.
+weight sets (7 x NSETS calls), bucket by bucket with the weight set changing
+on every call, so a set is read again only after the other NSETS - 1 sets
+(more than twice the L2 capacity) have streamed through: every call reads
+its weights from HBM.  The calls of one step are captured once into a CUDA
+graph and replayed; each call is a programmatic dependent of the previous
+one.  The timed region (exactly --steps replays) is cut into at least 10
+repeats whose median is reported beside the whole-region value.
 
 value = algorithmic HBM bytes of all calls (each tensor once) / device time,
 in GB/s, summed over ranks (replicas: the layer does not shard across GPUs
-here).  Per-bucket microseconds per call are reported beside it.
+here).  Per token bucket the line also carries the pipelined interval
+between back-to-back calls and the isolated latency of one call (a graph
+holding one call, after an L2 flush).  The same run measures the other
+configurations (W8A8_INT8 and Block_FP8 decode, FP8_Dynamic and Block_FP8
+at 2048 tokens, the bf16 4096^3 prefill fused and unfused) under "configs",
+each with its SM clocks.
 
 ``--impl reference`` times the CPU oracle (plain C, float64) on a bounded
 sample of the same workload instead.
@@ -21,6 +29,8 @@ w8a8_int8, block_fp8, prefill_bf16, prefill_unfused, and fp8_quant_calls /
 int8_quant_calls: bf16 activations quantised per token in the same plan run;
 fp8_swiglu_calls: the gated unit of an MLP, W [2 x 12288, 4096];
 ``--m`` picks token counts) and prints its own line.
+``--trace-timeline`` prints the per-call device timeline of one replayed
+step (first CTA start, first TMA, last CTA end of every call).
 """
 from __future__ import annotations
 
@@ -41,7 +51,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused scaled-GEMM HBM GB/s (FP8_Dynamic decode linear, K=4096 N=12288, M=1..32)"
-NSETS = 6
+NSETS = 7
 
 
 def parse():
@@ -53,6 +63,11 @@ def parse():
     ap.add_argument("--config", default="fp8_dynamic")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--repeats", type=int, default=10,
+                    help="repeats the timed region is cut into (at least 10)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only the default workload (no other configurations)")
+    ap.add_argument("--trace-timeline", action="store_true")
     ap.add_argument("--m", default=None, help="token counts for --config runs, e.g. 1,16")
     ap.add_argument("--tuning", default=None,
                     help="tuning override for --config runs, JSON, e.g. "
@@ -173,6 +188,193 @@ def weight_set(base, seed, torch):
     return W, s_w, b
 
 
+def l2_bytes(torch):
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 129 * 1024 * 1024
+
+
+def time_graph(torch, enqueue, stream, repeats=10, warmup=3):
+    """Capture enqueue(stream) into one CUDA graph and time `repeats`
+    replays of it with CUDA events on `stream`: per-replay milliseconds."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue(stream)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(repeats + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(repeats):
+            g.replay()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    del g
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(repeats)]
+
+
+def time_isolated(torch, enqueue, stream, flush, repeats=30):
+    """Latency of one call on its own: a graph holding that one call,
+    replayed after a write of more than twice the L2 capacity (so neither
+    its weights nor its predecessor's work are in L2, and no call of the
+    same layer runs before it); events around the replay only.  Median
+    microseconds."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue(stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(repeats)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in pairs:
+            flush.zero_()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in pairs)
+
+
+def clocks_during(torch, loop_fn, seconds=0.6):
+    """nvidia-smi SM clocks and throttle reasons while loop_fn() runs
+    repeatedly for about `seconds`."""
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.15)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        loop_fn()
+        torch.cuda.synchronize()
+    return sampler.stop()
+
+
+def weight_copies(W, n, torch):
+    """n device copies of a weight tensor (the first is W itself)."""
+    return [W] + [W.clone() for _ in range(n - 1)]
+
+
+def rotate_count(weight_bytes, l2):
+    """Weight copies for a rotation in which a copy is read again only after
+    more than twice the L2 capacity of other weights went through."""
+    return max(2, math.ceil(2 * l2 / max(weight_bytes, 1)) + 1)
+
+
+def decode_rows(torch, eg, inputs, traffic, base, tokens, peaks, stream, flush, l2):
+    """Per token bucket of one decode workload (`base` holds its largest
+    token count): the pipelined interval (a graph of back-to-back calls, the
+    weight copy changing on every call, each call a programmatic dependent
+    of the previous one), the isolated latency of one call, GB/s and the
+    fraction of the HBM roofline for both, and the SM clocks under the
+    first bucket's load."""
+    d0 = device_problem(base, torch)
+    nw = rotate_count(d0["W"].numel() * d0["W"].element_size(), l2)
+    Ws = weight_copies(d0["W"], nw, torch)
+    rows, clocks = {}, None
+    for M in tokens:
+        p = inputs.take_tokens(base, M)
+        d = device_problem(p, torch)
+        plan = eg.Plan(M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
+                       residual=p.residual is not None, pdl=True)
+        nb = traffic.problem_bytes(p)
+
+        def call(W, s, d=d, plan=plan):
+            plan.run(d["A"], W, d["Y"], d["s_a"], d0["s_w"], d0["bias"], d["residual"],
+                     stream=s.cuda_stream)
+        with torch.cuda.stream(stream):
+            call(Ws[0], stream)
+        torch.cuda.synchronize()
+        R = 4 * nw
+        ms = time_graph(torch, lambda s: [call(Ws[i % nw], s) for i in range(R)], stream)
+        us = statistics.median(ms) * 1e3 / R
+        iso = time_isolated(torch, lambda s: call(Ws[1], s), stream, flush)
+        if clocks is None:
+            def loop():
+                with torch.cuda.stream(stream):
+                    for i in range(R):
+                        call(Ws[i % nw], stream)
+            clocks = clocks_during(torch, loop)
+        gbs = nb / (us * 1e-6) / 1e9
+        rows[str(M)] = {"us_per_call": round(us, 3), "GB_s": round(gbs, 1),
+                        "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "isolated_us": round(iso, 3),
+                        "isolated_hbm_frac": round(nb / (iso * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                        "tuning": plan.tuning}
+        plan.close()
+        del d
+    del Ws, d0
+    return rows, clocks
+
+
+def large_m_row(torch, eg, traffic, p, peaks, stream, l2, unfused=False):
+    """One tensor-bound call (2048 tokens, or the 4096^3 prefill): median of
+    10 timed graphs of 10 back-to-back calls over rotated input copies (A, W
+    and the residual: a copy is read again only after more than the L2
+    capacity of other data); TFLOP/s against the dtype's dense peak (E4M3:
+    twice the measured bf16 figure, the nominal ratio).  With unfused, the
+    same problem through the three-kernel path too."""
+    d = device_problem(p, torch)
+    plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
+                   residual=p.residual is not None, residual_pre_act=p.residual_pre_act, pdl=True)
+    nb = traffic.problem_bytes(p)
+    fl = traffic.flops(p.M, p.N, p.K)
+    nsets = 2 if nb > 2 * l2 else 3
+    sets = [(d["A"], d["W"], d["residual"])]
+    for _ in range(nsets - 1):
+        sets.append((d["A"].clone(), d["W"].clone(),
+                     None if d["residual"] is None else d["residual"].clone()))
+
+    def call(i, s):
+        A, W, R = sets[i % nsets]
+        plan.run(A, W, d["Y"], d["s_a"], d["s_w"], d["bias"], R, stream=s.cuda_stream)
+    with torch.cuda.stream(stream):
+        call(0, stream)
+    torch.cuda.synchronize()
+    R = 10
+    ms = time_graph(torch, lambda s: [call(i, s) for i in range(R)], stream)
+    us = statistics.median(ms) * 1e3 / R
+    peak_tf = peaks["bf16_tflops"] * (2 if p.dtype == "e4m3" else 1)
+    tf = fl / (us * 1e-6) / 1e12
+    row = {"M": p.M, "N": p.N, "K": p.K, "us_per_call": round(us, 3), "TFLOP_s": round(tf, 1),
+           "tensor_frac": round(tf / peak_tf, 4), "peak_TFLOP_s": round(peak_tf, 1),
+           "peak_source": peaks["source"] + (" bf16 x 2" if p.dtype == "e4m3" else " bf16 burst"),
+           "GB_s": round(nb / (us * 1e-6) / 1e9, 1), "tuning": plan.tuning,
+           "repeats_us_per_call": [round(x * 1e3 / R, 2) for x in ms]}
+
+    def loop():
+        with torch.cuda.stream(stream):
+            for i in range(R):
+                call(i, stream)
+    row["clocks"] = clocks_during(torch, loop)
+    if unfused:
+        T1 = torch.empty(p.M, p.N, dtype=torch.bfloat16, device="cuda")
+        T2 = torch.empty_like(T1)
+        uplan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
+                        residual=p.residual is not None, residual_pre_act=p.residual_pre_act)
+
+        def ucall(i, s):
+            A, W, Rr = sets[i % nsets]
+            uplan.run_unfused(A, W, d["Y"], T1, T2, d["s_a"], d["s_w"], d["bias"], Rr,
+                              stream=s.cuda_stream)
+        with torch.cuda.stream(stream):
+            ucall(0, stream)
+        torch.cuda.synchronize()
+        ums = time_graph(torch, lambda s: [ucall(i, s) for i in range(R)], stream)
+        uus = statistics.median(ums) * 1e3 / R
+        row["unfused"] = {"us_per_call": round(uus, 3), "kernels_per_call": 3,
+                          "extra_bytes": traffic.unfused_extra_bytes(p.M, p.N),
+                          "fused_saves_us": round(uus - us, 3),
+                          "fused_speedup": round(uus / us, 4)}
+        uplan.close()
+    plan.close()
+    del sets, d
+    return row
+
+
 def run_native(args):
     import torch
     import epilogue_tcgen05_tmem_gb300 as eg
@@ -187,6 +389,7 @@ def run_native(args):
         pg = dist
     eg.lib()
     peaks = measured_peaks()
+    l2 = l2_bytes(torch)
 
     # ---- workload: token buckets x weight sets -----------------------------
     base = inputs.workload("fp8_dynamic", 32, seed=0)
@@ -196,23 +399,25 @@ def run_native(args):
     for M in tokens:
         p = inputs.take_tokens(base, M)
         plans[M] = eg.Plan(M, p.N, p.K, p.dtype, p.scale, p.act, bias=True, pdl=True)
-        d = device_problem(p, torch)
-        acts[M] = d
+        acts[M] = device_problem(p, torch)
     bytes_per_call = {M: traffic.algorithmic_bytes(M, base.N, base.K, "e4m3", "token_channel",
                                                    bias=True) for M in tokens}
-    calls_per_step = len(tokens) * NSETS
-    bytes_per_step = sum(bytes_per_call.values()) * NSETS
+    # the weight set changes on every call: bucket by bucket, each bucket
+    # over all NSETS sets, so a set is read again only after the other
+    # NSETS - 1 sets (more than twice the L2 capacity) went through
+    order = [(M, j) for M in tokens for j in range(NSETS)]
+    calls_per_step = len(order)
+    bytes_per_step = sum(bytes_per_call[M] for M, _ in order)
     weight_bytes = base.N * base.K
+    assert (NSETS - 1) * weight_bytes > 2 * l2 or l2 > 200e6
     stream = torch.cuda.Stream()
 
     def enqueue_step(s):
-        for j in range(NSETS):
+        for M, j in order:
             W, s_w, b = Wd[j]
-            for M in tokens:
-                d = acts[M]
-                plans[M].run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=s.cuda_stream)
+            d = acts[M]
+            plans[M].run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=s.cuda_stream)
 
-    # graph of one step (all buckets x all weight sets, each set visited once)
     with torch.cuda.stream(stream):
         enqueue_step(stream)  # first calls encode descriptors outside capture
     torch.cuda.synchronize()
@@ -220,63 +425,74 @@ def run_native(args):
     with torch.cuda.graph(g, stream=stream):
         enqueue_step(stream)
     torch.cuda.synchronize()
-
     for _ in range(max(args.warmup, 3)):
         g.replay()
     torch.cuda.synchronize()
 
-    # ---- timed region -------------------------------------------------------
+    # ---- timed region: exactly `steps` replays, cut into >= 10 repeats ------
+    n_rep = min(args.steps, max(10, args.repeats))
+    bounds = [args.steps * i // n_rep for i in range(n_rep + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.3)
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            g.replay()
-        e1.record(stream)
+        ev[0].record(stream)
+        for r in range(n_rep):
+            for _ in range(bounds[r + 1] - bounds[r]):
+                g.replay()
+            ev[r + 1].record(stream)
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    ms, total_bytes = rank_aggregate(e0.elapsed_time(e1), bytes_per_step * args.steps, pg)
+    local_ms = ev[0].elapsed_time(ev[-1])
+    rep_ms = [ev[r].elapsed_time(ev[r + 1]) / (bounds[r + 1] - bounds[r]) for r in range(n_rep)]
+    ms, total_bytes = rank_aggregate(local_ms, bytes_per_step * args.steps, pg)
     ms_per_step = ms / args.steps
     value = total_bytes / (ms * 1e-3) / 1e9
     avg_launch_us = ms * 1e3 / (args.steps * calls_per_step)
     achieved = (bytes_per_step / calls_per_step) / (avg_launch_us * 1e-6) / 1e9
+    del g
 
-    # ---- per-bucket microseconds per call (graph of NSETS*R calls) ---------
+    # ---- per bucket: pipelined interval and isolated latency ----------------
+    flush = torch.empty(int(2.2 * l2), dtype=torch.uint8, device="cuda")
     per_m = {}
     for M in tokens:
-        gm = torch.cuda.CUDAGraph()
-        R = 8
-        with torch.cuda.graph(gm, stream=stream):
-            for _ in range(R):
-                for j in range(NSETS):
-                    W, s_w, b = Wd[j]
-                    d = acts[M]
-                    plans[M].run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=stream.cuda_stream)
-        for _ in range(3):
-            gm.replay()
-        torch.cuda.synchronize()
-        reps = 20
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                gm.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * R * NSETS)
+        d = acts[M]
+
+        def call(j, s, M=M, d=d):
+            W, s_w, b = Wd[j]
+            plans[M].run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=s.cuda_stream)
+        R = 4
+        msr = time_graph(torch, lambda s: [call(j, s) for _ in range(R) for j in range(NSETS)],
+                         stream)
+        us = statistics.median(msr) * 1e3 / (R * NSETS)
+        iso = time_isolated(torch, lambda s: call(1, s), stream, flush)
         per_m[str(M)] = {"us_per_call": round(us, 3),
                          "GB_s": round(bytes_per_call[M] / (us * 1e-6) / 1e9, 1),
                          "hbm_frac": round(bytes_per_call[M] / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                         "isolated_us": round(iso, 3),
+                         "isolated_hbm_frac": round(
+                             bytes_per_call[M] / (iso * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
                          "tuning": plans[M].tuning}
 
     # ---- end to end through host buffers -----------------------------------
-    e2e = run_e2e(args, torch, eg, plans, acts, Wd, tokens, bytes_per_step, stream)
+    e2e = run_e2e(args, torch, eg, plans, acts, Wd, order, bytes_per_step, stream)
+    for pl in plans.values():
+        pl.close()
+    del Wd, acts
+    torch.cuda.empty_cache()
+
+    # ---- the other configurations, under the same clock ---------------------
+    configs = {}
+    if not args.no_configs:
+        configs = other_configs(torch, eg, inputs, traffic, peaks, stream, flush, l2)
+    del flush
+    torch.cuda.empty_cache()
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -285,26 +501,173 @@ def run_native(args):
         "data": "synthetic (seeded SplitMix64 normals; 1% outlier channels x10; e4m3 per-token/per-channel)",
         "config": {"workload": "fp8_dynamic_decode", "M": tokens, "K": base.K, "N": base.N,
                    "epilogue": "scale+bias+SiLU, bf16 out", "weight_sets": NSETS,
+                   "call_order": "bucket by bucket, the weight set changing on every call",
                    "calls_per_step": calls_per_step, "bytes_per_step": bytes_per_step,
                    "l2": f"inputs larger than L2: {NSETS} rotating weight sets "
-                         f"({NSETS * weight_bytes / 1e6:.0f} MB of weights per step)",
-                   "timing": "CUDA events around CUDA-graph replays of whole steps",
+                         f"({NSETS * weight_bytes / 1e6:.0f} MB of weights per step); a set is "
+                         f"read again after {(NSETS - 1) * weight_bytes / 1e6:.0f} MB of other "
+                         f"weights (L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA events around CUDA-graph replays of whole steps; each call "
+                             "a programmatic dependent of the previous one",
                    "parallelism": f"replicas x{world}"},
+        "repeats": {"n": n_rep, "ms_per_step_median": round(statistics.median(rep_ms), 5),
+                    "ms_per_step_min": round(min(rep_ms), 5),
+                    "ms_per_step_max": round(max(rep_ms), 5),
+                    "value_median": round(bytes_per_step / (statistics.median(rep_ms) * 1e-3) / 1e9, 2)},
         "per_m": per_m,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": measured_traffic("fp8_dynamic_decode"), "peak_source": peaks["source"],
-                     "kernel": "fused_linear_kernel<e4m3, token_channel, swap_ab>"},
+                     "kernel": "fused_linear_kernel<e4m3, token_channel, swap_ab>",
+                     "launch_duration": "timed region / launches (back-to-back calls overlap "
+                                        "through programmatic dependent launch)"},
+        "configs": configs,
         "e2e": e2e, "gpu_launches": args.steps * calls_per_step, "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(base)
-    for pl in plans.values():
-        pl.close()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def other_configs(torch, eg, inputs, traffic, peaks, stream, flush, l2):
+    """The other workloads of the measurement table, timed in the same run:
+    W8A8_INT8 and Block_FP8 decode per token bucket (pipelined and
+    isolated), FP8_Dynamic and Block_FP8 at 2048 tokens, and the bf16
+    4096^3 prefill block fused and through the unfused three-kernel path."""
+    cfg = {}
+    base = inputs.workload("w8a8_int8", 32)
+    rows, clocks = decode_rows(torch, eg, inputs, traffic, base, list(inputs.DECODE_TOKENS),
+                               peaks, stream, flush, l2)
+    cfg["w8a8_int8_decode"] = {"K": base.K, "N": base.N, "epilogue": "scale + bf16 residual",
+                               "per_m": rows, "clocks": clocks}
+    del base
+    torch.cuda.empty_cache()
+    # Block_FP8: the 2048-token problem; its first 1, 8 and 32 tokens are
+    # the decode problems (per-token data is row-local)
+    big = inputs.workload("block_fp8", 2048)
+    rows, clocks = decode_rows(torch, eg, inputs, traffic, inputs.take_tokens(big, 32), [1, 8, 32],
+                               peaks, stream, flush, l2)
+    cfg["block_fp8_decode"] = {"K": big.K, "N": big.N, "per_m": rows, "clocks": clocks}
+    torch.cuda.empty_cache()
+    cfg["block_fp8_m2048"] = large_m_row(torch, eg, traffic, big, peaks, stream, l2)
+    del big
+    torch.cuda.empty_cache()
+    cfg["fp8_dynamic_m2048"] = large_m_row(torch, eg, traffic, inputs.workload("fp8_dynamic", 2048),
+                                           peaks, stream, l2)
+    torch.cuda.empty_cache()
+    cfg["prefill_bf16_4096"] = large_m_row(torch, eg, traffic, inputs.workload("prefill_bf16"),
+                                           peaks, stream, l2, unfused=True)
+    torch.cuda.empty_cache()
+    return cfg
+
+
+def run_trace_timeline(args):
+    """Per-call timeline of one replay of the default step (every call with
+    its own plan and trace buffer): for each call, the first CTA start, the
+    first TMA issued after its wait on the previous kernel, and the last CTA
+    end, relative to the step's first CTA start.  Prints one JSON line."""
+    import torch
+    import epilogue_tcgen05_tmem_gb300 as eg
+    from epilogue_tcgen05_tmem_gb300 import inputs
+
+    torch.cuda.set_device(dist_env()[2])
+    eg.lib()
+    base = inputs.workload("fp8_dynamic", 32, seed=0)
+    tokens = list(inputs.DECODE_TOKENS)
+    Wd = [weight_set(base, 0, torch)] + [weight_set(base, 100 + i, torch) for i in range(NSETS - 1)]
+    acts = {M: device_problem(inputs.take_tokens(base, M), torch) for M in tokens}
+    order = [(M, j) for M in tokens for j in range(NSETS)]
+    calls = []
+    for M, j in order:
+        pl = eg.Plan(M, base.N, base.K, "e4m3", "token_channel", "silu", bias=True, pdl=True)
+        ctas = pl.launch_info["grid"]
+        buf = torch.zeros(ctas, eg.EG_TRACE_POINTS, dtype=torch.int64, device="cuda")
+        pl.set_trace(buf)
+        calls.append((M, j, pl, buf))
+    stream = torch.cuda.Stream()
+
+    def enqueue(s):
+        for M, j, pl, _ in calls:
+            W, s_w, b = Wd[j]
+            d = acts[M]
+            pl.run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=s.cuda_stream)
+    with torch.cuda.stream(stream):
+        enqueue(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue(stream)
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    for _, _, _, buf in calls:
+        buf.zero_()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    step_ms = e0.elapsed_time(e1)
+    tr = [buf.cpu().numpy() for _, _, _, buf in calls]
+    t0 = min(int(t[:, 0][t[:, 0] > 0].min()) for t in tr)
+    from epilogue_tcgen05_tmem_gb300 import trace as trace_mod
+    rows = []
+    prev_end = None
+    detail = {}
+    for i in (0, 1, len(calls) // 2, len(calls) - 1):
+        M, j = calls[i][0], calls[i][1]
+        detail[f"call{i}_M{M}_set{j}"] = trace_mod.summarize(tr[i], t0)
+    for (M, j, pl, _), t in zip(calls, tr):
+        st = t[:, 0][t[:, 0] > 0]
+        ft = t[:, 2][t[:, 2] > 0]
+        en = t[:, 7][t[:, 7] > 0]
+        r = {"M": M, "set": j, "ctas": int(st.size),
+             "start_us": round((int(st.min()) - t0) / 1e3, 3),
+             "first_tma_us": round((int(ft.min()) - t0) / 1e3, 3) if ft.size else None,
+             "end_us": round((int(en.max()) - t0) / 1e3, 3)}
+        r["span_us"] = round(r["end_us"] - r["start_us"], 3)
+        r["overlap_prev_us"] = None if prev_end is None else round(prev_end - r["start_us"], 3)
+        prev_end = r["end_us"]
+        rows.append(r)
+    # isolated calls: one call per graph replay after an L2 flush, traced
+    flush = torch.empty(int(2.2 * l2_bytes(torch)), dtype=torch.uint8, device="cuda")
+    iso = {}
+    for i in (0, len(calls) - 1):
+        M, j, pl, buf = calls[i]
+        W, s_w, b = Wd[j]
+        d = acts[M]
+        gi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gi, stream=stream):
+            pl.run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=stream.cuda_stream)
+        for _ in range(3):
+            gi.replay()
+        torch.cuda.synchronize()
+        buf.zero_()
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            gi.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = buf.cpu().numpy()
+        st, en = t[:, 0][t[:, 0] > 0], t[:, 7][t[:, 7] > 0]
+        iso[f"M{M}_set{j}"] = {"event_us": round(e0.elapsed_time(e1) * 1e3, 3),
+                               "trace_span_us": round((int(en.max()) - int(st.min())) / 1e3, 3),
+                               "points": trace_mod.summarize(t)}
+        del gi
+    for _, _, pl, _ in calls:
+        pl.close()
+    spans = [r["span_us"] for r in rows]
+    print(json.dumps({"trace": "fp8_dynamic_decode step", "calls": len(rows),
+                      "step_ms_events": round(step_ms, 4),
+                      "step_us_trace": round(rows[-1]["end_us"] - rows[0]["start_us"], 3),
+                      "sum_of_spans_us": round(sum(spans), 3),
+                      "mean_interval_us": round((rows[-1]["end_us"] - rows[0]["start_us"]) / len(rows), 3),
+                      "points": detail, "isolated": iso, "rows": rows}), flush=True)
 
 
 def kernel_source_sha256():
@@ -332,27 +695,27 @@ def measured_traffic(key):
     return rec["dram_bytes_per_launch"]
 
 
-def run_e2e(args, torch, eg, plans, acts, Wd, tokens, bytes_per_step, stream):
+def run_e2e(args, torch, eg, plans, acts, Wd, order, bytes_per_step, stream):
     """Same metric through the C ABI with host buffers: every call copies its
     activations (A, s_a) from pinned host memory and reads Y back."""
+    tokens = sorted({M for M, _ in order})
     host = {}
     for M in tokens:
         d = acts[M]
         host[M] = {"A": d["A"].cpu().pin_memory(), "s_a": d["s_a"].cpu().pin_memory(),
                    "Y": torch.empty(d["Y"].shape, dtype=torch.bfloat16).pin_memory()}
     steps = args.e2e_steps or max(3, min(args.steps, 50))
-    h2d = sum(host[M]["A"].numel() + 4 * host[M]["s_a"].numel() for M in tokens) * NSETS
-    d2h = sum(host[M]["Y"].numel() * 2 for M in tokens) * NSETS
+    h2d = sum(host[M]["A"].numel() + 4 * host[M]["s_a"].numel() for M, _ in order)
+    d2h = sum(host[M]["Y"].numel() * 2 for M, _ in order)
 
     def one_step():
-        for j in range(NSETS):
+        for M, j in order:
             W, s_w, b = Wd[j]
-            for M in tokens:
-                d, h = acts[M], host[M]
-                d["A"].copy_(h["A"], non_blocking=True)
-                d["s_a"].copy_(h["s_a"], non_blocking=True)
-                plans[M].run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=stream.cuda_stream)
-                h["Y"].copy_(d["Y"], non_blocking=True)
+            d, h = acts[M], host[M]
+            d["A"].copy_(h["A"], non_blocking=True)
+            d["s_a"].copy_(h["s_a"], non_blocking=True)
+            plans[M].run(d["A"], W, d["Y"], d["s_a"], s_w, b, None, stream=stream.cuda_stream)
+            h["Y"].copy_(d["Y"], non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(2):
@@ -552,6 +915,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.trace_timeline:
+        run_trace_timeline(args)
     elif args.config != "fp8_dynamic":
         run_config(args)
     else:

@@ -220,8 +220,9 @@ def eg_plan_last_launch_count(plan) -> int:
     return lib().eg_plan_last_launch_count(plan)
 
 
-def eg_plan_set_test_stall(plan, wait_limit_ns: int, stall_producer: bool) -> int:
-    return lib().eg_plan_set_test_stall(plan, wait_limit_ns, int(bool(stall_producer)))
+def eg_plan_set_test_stall(plan, wait_limit_ns: int, stall_producer: int) -> int:
+    """stall_producer: 0 off, 1 (or True) every CTA, 2 odd-numbered CTAs only."""
+    return lib().eg_plan_set_test_stall(plan, wait_limit_ns, int(stall_producer))
 
 
 # -------------------------------------------------------------- Plan -------
@@ -324,7 +325,7 @@ class Plan:
     def last_launch_count(self) -> int:
         return eg_plan_last_launch_count(self.handle)
 
-    def set_test_stall(self, wait_limit_ns: int, stall_producer: bool):
+    def set_test_stall(self, wait_limit_ns: int, stall_producer: int):
         _check(eg_plan_set_test_stall(self.handle, wait_limit_ns, stall_producer))
 
     def close(self):

@@ -92,6 +92,10 @@ struct GraphEntry {
   cudaGraphExec_t exec;
 };
 
+// Captured graphs a plan keeps in EG_RUN_GRAPH mode (one per argument set,
+// least recently used dropped first).
+constexpr size_t kGraphCache = 8;
+
 struct eg_plan {
   eg_problem prob{};
   eg_tuning tune{};
@@ -240,6 +244,9 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
     return fail(EG_ERR_INVALID_ARG, "cluster_reduce must be 0 or 1");
   if (t.cluster_reduce && (p.flags & EG_EPI_GATED))
     return fail(EG_ERR_UNSUPPORTED, "gated units reduce split-K through the workspace (cluster_reduce 0)");
+  if (t.cluster_reduce && p.scale == EG_SCALE_BLOCK && !t.swap_ab && t.tile_n > 128)
+    return fail(EG_ERR_UNSUPPORTED,
+                "block-scale tiles wider than 128 reduce split-K through the workspace (cluster_reduce 0)");
   if (t.cluster_reduce) {
     if (t.split_k != 2 && t.split_k != 4 && t.split_k != 8)
       return fail(EG_ERR_UNSUPPORTED, "cluster_reduce needs split_k in {2, 4, 8} (got %d)", t.split_k);
@@ -309,6 +316,12 @@ eg_status residency(eg_plan* pl, int dev, int* per_sm_out) {
   per_sm = std::min(per_sm, sm_blocks);
   per_sm = std::min(per_sm, 512 / pl->ke.tmem_cols);
   if (per_sm < 1) return fail(EG_ERR_UNSUPPORTED, "the kernel does not fit on an SM");
+  // a setmaxnreg split draws on the block's launch allocation (threads x
+  // registers per thread): one that does not fit would wait forever
+  if (pl->ke.regsplit_need > 0 && fa.numRegs * pl->ke.threads < pl->ke.regsplit_need)
+    return fail(EG_ERR_UNSUPPORTED,
+                "the kernel's register split needs %d registers; it was built with %d x %d",
+                pl->ke.regsplit_need, fa.numRegs, pl->ke.threads);
   *per_sm_out = per_sm;
   return EG_OK;
 }
@@ -545,7 +558,9 @@ int acc_release_for(const eg_problem& p, const eg_tuning& t) {
   if (const char* e = getenv("EG_ACC_RELEASE"))
     if (atoi(e) == 0) return 0;
   if (p.dtype == EG_IN_INT8) return 1;
-  if (p.scale == EG_SCALE_BLOCK) return t.stages <= 4 ? 1 : 0;
+  // (a stage may wait for the commit of the K block S blocks back only while
+  // S is at most the accumulator buffers: four, or two for 256-wide tiles)
+  if (p.scale == EG_SCALE_BLOCK) return t.stages <= (!t.swap_ab && t.tile_n > 128 ? 2 : 4) ? 1 : 0;
   return 0;
 }
 
@@ -828,7 +843,9 @@ eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace_ctas) 
 eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns, int32_t stall_producer) {
   if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
   plan->wait_limit_ns = wait_limit_ns ? wait_limit_ns : default_wait_limit_ns();
-  plan->stall = stall_producer ? 1 : 0;
+  if (stall_producer < 0 || stall_producer > 2)
+    return fail(EG_ERR_INVALID_ARG, "stall_producer must be 0, 1 or 2 (got %d)", stall_producer);
+  plan->stall = stall_producer;
   return EG_OK;
 }
 
@@ -868,10 +885,12 @@ eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream) {
     plan->last_launches = launches;
     return EG_OK;
   }
-  // graph mode: one captured graph per distinct argument set
-  for (auto& g : plan->graphs) {
-    if (memcmp(&g.args, args, sizeof(eg_args)) == 0) {
-      EG_CUDA(cudaGraphLaunch(g.exec, st), "cudaGraphLaunch");
+  // graph mode: one captured graph per distinct argument set, the most
+  // recently used first; at most kGraphCache of them are kept
+  for (size_t i = 0; i < plan->graphs.size(); ++i) {
+    if (memcmp(&plan->graphs[i].args, args, sizeof(eg_args)) == 0) {
+      if (i > 0) std::rotate(plan->graphs.begin(), plan->graphs.begin() + i, plan->graphs.begin() + i + 1);
+      EG_CUDA(cudaGraphLaunch(plan->graphs[0].exec, st), "cudaGraphLaunch");
       plan->last_launches = launches;
       return EG_OK;
     }
@@ -891,7 +910,13 @@ eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream) {
   e = cudaGraphInstantiate(&exec, graph, 0);
   cudaGraphDestroy(graph);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
-  plan->graphs.push_back(GraphEntry{*args, exec});
+  if (plan->graphs.size() >= kGraphCache) {
+    // the least recently used graph goes; work it queued earlier keeps
+    // running (a graph exec may be destroyed while its launches are pending)
+    cudaGraphExecDestroy(plan->graphs.back().exec);
+    plan->graphs.pop_back();
+  }
+  plan->graphs.insert(plan->graphs.begin(), GraphEntry{*args, exec});
   EG_CUDA(cudaGraphLaunch(exec, st), "cudaGraphLaunch");
   plan->last_launches = launches;
   return EG_OK;
@@ -947,6 +972,14 @@ eg_status eg_plan_device_status(eg_plan* plan) {
   int st = 0;
   EG_CUDA(cudaMemcpy(&st, plan->status, sizeof(int), cudaMemcpyDeviceToHost), "reading the status word");
   if (st != 0) {
+    // A CTA that gave up on a wait left its split-K tiles unfinished: their
+    // arrival counters hold partial counts (the last arriver resets a
+    // counter, and it never came) and, for INT8, slot 0 of the workspace
+    // holds partial sums (the last arriver re-zeroes it).  Reset both so the
+    // plan's next run starts from the state eg_plan_create left.
+    const size_t tiles = size_t(plan->tiles_rows) * plan->tiles_cols;
+    EG_CUDA(cudaMemset(plan->counters, 0, (tiles + 1) * sizeof(int)), "resetting the tile counters");
+    if (plan->ws) EG_CUDA(cudaMemset(plan->ws, 0, plan->ws_bytes), "resetting the split-K workspace");
     EG_CUDA(cudaMemset(plan->status, 0, sizeof(int)), "clearing the status word");
     EG_CUDA(cudaDeviceSynchronize(), "synchronising");
     static const char* where[] = {"", "load warp", "UMMA warp", "epilogue warps", "transform warps",
@@ -1087,6 +1120,11 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   EG_CUDA(cudaFuncSetAttribute(pl.ke.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kMaxSmem)),
           "cudaFuncSetAttribute");
+  // as eg_plan_create does: the grid above counts on the largest
+  // shared-memory carveout
+  EG_CUDA(cudaFuncSetAttribute(pl.ke.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared),
+          "setting the shared-memory carveout");
   // the arrival counters and the status word start every call at zero (the
   // array keeps whatever the previous call left)
   EG_CUDA(cudaMemsetAsync(counters, 0, (tiles + 1) * sizeof(int), st), "clearing tile counters");

@@ -76,7 +76,10 @@ struct KParams {
   int* counters;                  // per-tile arrival counters
   int* status;                    // device status word
   uint64_t wait_limit_ns;
-  int32_t stall_producer;         // failure-detection test hook
+  int32_t stall_producer;         // failure-detection test hook: 1 every CTA's load
+                                  // warp issues nothing, 2 only odd-numbered CTAs'
+                                  // (the others finish and count their split-K
+                                  // arrivals)
   int32_t evict_first_p;          // L2 evict-first hint on the P operand
   int32_t evict_first_q;          // ... on the Q operand
   int32_t vec_ok;                 // Y (and R) rows 16-byte aligned: vector path
@@ -144,7 +147,17 @@ struct Cfg {
       ((kPromote && !kConvert && BN >= 64) || (!SWAP && !kPromote && !G && BN >= 128)) ? 8 : 4;
   static constexpr int kEpiThreads = kEpiWarps * 32;
   static constexpr int kColsPerThread = BN / (kEpiWarps / 4);
-  static constexpr int kThreads = 64 + kEpiThreads + (kConvert ? 128 : 0);
+  // Wide block-scale promotion (tile_n above 128): each epilogue thread
+  // keeps 128 running sums.  The epilogue warps then form their own two
+  // warpgroups (warps 4..11; warps 2 and 3 stay idle) so that the first
+  // warpgroup (producer, UMMA issuer) can hand registers over to them with
+  // setmaxnreg: kRegsLow per thread there, kRegsHigh in the epilogue.
+  static constexpr bool kWidePromote = kPromote && !kConvert && BN > 128;
+  static constexpr int kEpiWarp0 = kWidePromote ? 4 : 2;   // first epilogue warp
+  static constexpr int kThreads = 32 * kEpiWarp0 + kEpiThreads + (kConvert ? 128 : 0);
+  static constexpr int kRegsLow = 64, kRegsHigh = 216;
+  // registers the split needs from the block's launch allocation
+  static constexpr int kRegSplitNeed = kWidePromote ? 128 * kRegsLow + kEpiThreads * kRegsHigh : 0;
   // Small tiles (decode) are meant to run two CTAs per SM; cap registers so
   // two fit.  Promotion with wide tiles keeps BN accumulators per thread.
   // Decode tiles (BN 16) keep a third slot per SM free so that the next
@@ -185,7 +198,11 @@ struct Cfg {
       (IN == IN_BF16) ? idesc_f32acc(1, 1, kUmmaM, BN)
                       : idesc_f32acc(0, 0, kUmmaM, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
-  static_assert(!kPromote || BN <= 128, "promotion keeps BN fp32 values per thread");
+  static_assert(!kPromote || BN <= 128 || (kWidePromote && BN == 256 && !SWAP && !G && !PR),
+                "wide promotion: block scales, tile_n 256, rows over M");
+  static_assert(!kWidePromote || kColsPerThread == 128, "128 running sums per epilogue thread");
+  static_assert(!kWidePromote || 128 * kRegsLow + kEpiThreads * kRegsHigh <= kThreads * kMaxRegs,
+                "register split within the launch allocation");
   static_assert(kTmemUsed <= 512, "tensor memory holds 512 columns");
   static_assert(!G || !kPromote, "gated units use the tensor-memory accumulator path");
   static_assert(!PR || (!SWAP && !kPromote && !G && (BN == 128 || BN == 256)),
@@ -606,6 +623,22 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
   EG_ACT_DISPATCH(p.act, (epilogue_chunk_a<IN, SC, SWAP, CW, A_>(p, row, col0, vals)))
 }
 
+// The epilogue of a thread's CPT promoted accumulators (columns col0 ..
+// col0 + CPT - 1 of its row), CW columns at a time, with the activation a
+// compile-time choice made once for all of them (the chunk loop unrolls and
+// the accumulators stay in registers).
+template <int IN, int SC, bool SWAP, int CW, int CPT, int ACT>
+__device__ __forceinline__ void promoted_store(const KParams& p, int row, int col0,
+                                               const uint32_t (&acc)[CPT]) {
+#pragma unroll
+  for (int c = 0; c < CPT; c += CW) {
+    uint32_t r[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
+    epilogue_chunk_a<IN, SC, SWAP, CW, ACT>(p, row, col0 + c, r);
+  }
+}
+
 // Gated unit epilogue of CW consecutive accumulator columns of one TMEM lane:
 // gate values g and up values u (fp32 bits).  Per output (m, n):
 // gate = scale(g) + bias[n], up = scale(u) + bias[N + n] (scale: s_a[m] *
@@ -694,6 +727,16 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[CW
   } else {
     tmem_ld16(taddr, r);
   }
+}
+
+// Promotion of one 32-column piece of a K block: acc[C0 + j] += s * r[j]
+// (float32 bits), with C0 known at compile time so the accumulator array
+// stays in registers.
+template <int C0, int N>
+__device__ __forceinline__ void fma_piece(uint32_t (&acc)[N], const uint32_t (&r)[32], float s) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    acc[C0 + j] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[j]), __uint_as_float(acc[C0 + j])));
 }
 
 // Split-K: store this split's partial for (tile, split); valid entries only.
@@ -1298,9 +1341,20 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
   if (p.pdl && threadIdx.x == 0) griddep_launch_dependents();
   if (threadIdx.x == 0) trace_point(p, TR_SETUP);
 
+  // Roles: producer (warp 0), UMMA issuer (warp 1), INT8 converters (the
+  // last four warps), epilogue (the rest from kEpiWarp0 on).  Wide
+  // promotion tiles: warpgroup 0 (producer, issuer and two idle warps) hands
+  // registers to the two epilogue warpgroups with setmaxnreg, each
+  // warpgroup executing one and the same instruction at the top of its
+  // branch (the host checked that the split fits the launch allocation).
+  const bool epi_warp =
+      warp >= C::kEpiWarp0 && !(C::kConvert && warp >= C::kEpiWarp0 + C::kEpiWarps);
+  if (!epi_warp) {
+  if constexpr (C::kWidePromote) setmaxnreg_dec<C::kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    if (lane == 0 && !p.stall_producer && has_work) {
+    const bool stalled = p.stall_producer == 1 || (p.stall_producer == 2 && (blockIdx.x & 1u));
+    if (lane == 0 && !stalled && has_work) {
       const uint64_t pol_first = policy_evict_first();
       // The weight operand (P with swap-AB, else Q) is constant across calls;
       // the activation operand may be written by the previous kernel.
@@ -1395,6 +1449,26 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           load_op(false, w, i, s);
           ring_next(rp, S, CG, NG);
           ++gp;
+        }
+      }
+      // Wind-down: wait (bounded) until every stage this thread armed has
+      // received all of its bytes, so that no bulk copy is still landing in
+      // shared memory when the CTA leaves after some role gave up on a wait.
+      // Stage s was armed n_s times; its last armed phase is n_s - 1, and a
+      // phase is only armed once the one before it has completed, so its
+      // parity identifies it.  On the normal path the UMMA issuer (or the
+      // INT8 converters) already consumed every phase and these return at
+      // once.  CTA pairs: the even CTA's stage barriers count both CTAs'
+      // bytes, and the odd CTA leaves only after the cluster barrier of the
+      // teardown, which the even CTA reaches after this wait.
+      if (pair_leader) {
+        const uint32_t su = static_cast<uint32_t>(S);
+        for (int s = 0; s < S; ++s) {
+          const uint32_t n = gp / su + (static_cast<uint32_t>(s) < gp % su ? 1u : 0u);
+          if (n > 0 && !mbar_wait(&full[s], (n - 1u) & 1u, lim)) {
+            record_status(p.status, ST_TIMEOUT_PRODUCER);
+            break;
+          }
         }
       }
     }
@@ -1524,7 +1598,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
       else
         umma_commit(mma_done);
     }
-  } else if (C::kConvert && warp >= 6) {
+  } else if (C::kConvert && warp >= C::kEpiWarp0 + C::kEpiWarps) {
     // ---------------------------------- INT8 -> fp16 prologue transform ----
     if constexpr (C::kConvert) {
       const int ct = threadIdx.x - 192;  // 0..127
@@ -1568,18 +1642,20 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
         }
       }
     }
+  }
   } else {
     // ----------------------------------------------------- epilogue ----
+    if constexpr (C::kWidePromote) setmaxnreg_inc<C::kRegsHigh>();
     const int quarter = warp & 3;
     const int lane_row = quarter * 32 + lane;
     constexpr int CPT = C::kColsPerThread;
     static_assert(CPT % C::kCW == 0, "whole TMEM load chunks per thread");
     static_assert(!G || CPT == BN, "gated units use 4 epilogue warps");
     // this thread's first column in the tile
-    const int cbeg = (C::kEpiWarps == 4) ? 0 : ((warp - 2) >> 2) * CPT;
+    const int cbeg = (C::kEpiWarps == 4) ? 0 : ((warp - C::kEpiWarp0) >> 2) * CPT;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                             static_cast<uint32_t>(cbeg);
-    const int ept = threadIdx.x - 64;  // 0 .. kEpiThreads-1
+    const int ept = threadIdx.x - 32 * C::kEpiWarp0;  // 0 .. kEpiThreads-1
     griddep_wait();
     uint32_t blk = 0;
     bool ok = true;
@@ -1589,8 +1665,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     // staged one unit ahead, into the other of two buffers, so their global
     // latency overlaps the current unit; with swap-AB (decode, about one unit
     // per CTA) each unit stages its own, all copies in flight at once.
+    // Wide promotion tiles read their two scales per K block straight from
+    // global memory, one block ahead, into registers (no staging buffer).
     constexpr int kScaleRows = SWAP ? BN : 128;
-    constexpr bool kAhead = (SC == SC_BLOCK) && !SWAP;
+    constexpr bool kAhead = (SC == SC_BLOCK) && !SWAP && !C::kWidePromote;
     const int scale_buf_floats = (kScaleRows + 1) * scale_row_stride(p.k_tiles);
     WorkIter it_pf = it;
     uint32_t su = 0;
@@ -1623,13 +1701,63 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           cp_async_commit();
           cp_async_wait<1>();            // this thread's copies for this unit landed
           epi_bar_sync(C::kEpiThreads);  // ... and every thread's
-        } else if constexpr (SC == SC_BLOCK) {
+        } else if constexpr (SC == SC_BLOCK && !C::kWidePromote) {
           epi_bar_sync(C::kEpiThreads);  // the previous unit's reads of this buffer are done
           stage_block_scales<SWAP, BN, C::kEpiThreads>(p, w, sc_a, ept);
           cp_async_commit();
           cp_async_wait<0>();
           epi_bar_sync(C::kEpiThreads);
         }
+        if constexpr (C::kWidePromote) {
+          // 128 running sums per thread: one row (m) and the 128 columns of
+          // one weight block (n / 128), so one s_a and one s_w per K block,
+          // loaded a block ahead.  Per K block the buffer is read in four
+          // 32-column pieces, each piece's load in flight while the previous
+          // piece is added (two pieces in registers at a time).
+          const int nbw = (w.col0 + cbeg) >> 7;
+          const bool rv = row < p.M;
+          const bool wv = nbw < (p.N + 127) / 128;
+          const float* sa = p.s_a + (rv ? static_cast<int64_t>(row) * p.kb_count + w.kt0 : 0);
+          const float* sw = p.s_w + (wv ? static_cast<int64_t>(nbw) * p.kb_count + w.kt0 : 0);
+          float sa_n = (rv && w.nk > 0) ? __ldg(sa) : 0.0f;
+          float sw_n = (wv && w.nk > 0) ? __ldg(sw) : 0.0f;
+          for (int i = 0; i < w.nk; ++i, ++blk) {
+            const int b = blk % NB;
+            const uint32_t bph = (blk / NB) & 1u;
+            const float srow = sa_n * sw_n;
+            if (i + 1 < w.nk) {
+              sa_n = rv ? __ldg(sa + i + 1) : 0.0f;
+              sw_n = wv ? __ldg(sw + i + 1) : 0.0f;
+            }
+            if (!mbar_wait(&tfull[b], bph, lim)) {
+              record_status(p.status, ST_TIMEOUT_EPILOGUE);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
+            const uint32_t tb = t_lane + static_cast<uint32_t>(b * BN);
+            uint32_t ra[32], rb[32];
+            tmem_ld32(tb, ra);
+            tmem_ld_wait();
+            reg_fence<32>(ra);
+            tmem_ld32(tb + 32u, rb);
+            fma_piece<0, CPT>(acc, ra, srow);
+            tmem_ld_wait();
+            reg_fence<32>(rb);
+            tmem_ld32(tb + 64u, ra);
+            fma_piece<32, CPT>(acc, rb, srow);
+            tmem_ld_wait();
+            reg_fence<32>(ra);
+            tmem_ld32(tb + 96u, rb);
+            fma_piece<64, CPT>(acc, ra, srow);
+            tmem_ld_wait();
+            reg_fence<32>(rb);
+            tc_fence_before();
+            mbar_arrive(&tempty[b]);  // the buffer is free once all of it is in registers
+            fma_piece<96, CPT>(acc, rb, srow);
+          }
+        } else
         for (int i = 0; i < w.nk; ++i, ++blk) {
           const int b = blk % NB;
           const uint32_t bph = (blk / NB) & 1u;
@@ -1665,6 +1793,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           }
         }
         if (!ok) break;
+        // (wide tiles take split-K through the workspace only)
+        if constexpr (!C::kWidePromote) {
         if (p.cluster_reduce) {
           // every UMMA of the unit has completed (its last buffer was full),
           // so this CTA's operand ring is idle
@@ -1688,6 +1818,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             break;
           }
           continue;
+        }
         }
         bool do_epi = true;
         if (w.contrib > 1) {
@@ -1718,19 +1849,27 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
               if (row < p.rows && w.col0 + cbeg + c < p.cols) __stcg(wsb + c * 128, acc[c]);
             do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
             if (do_epi) {
-              reduce_partials<IN, BN, CPT>(p, w.tile, w.contrib, cbeg, lane_row, row < p.rows,
-                                           p.cols - (w.col0 + cbeg), acc);
+              if constexpr (CPT > 64) {
+                // 32 columns at a time, so the partials in flight stay small
+#pragma unroll
+                for (int c = 0; c < CPT; c += 32) {
+                  uint32_t part[32];
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) part[j] = acc[c + j];
+                  reduce_partials<IN, BN, 32>(p, w.tile, w.contrib, cbeg + c, lane_row, row < p.rows,
+                                              p.cols - (w.col0 + cbeg + c), part);
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) acc[c + j] = part[j];
+                }
+              } else {
+                reduce_partials<IN, BN, CPT>(p, w.tile, w.contrib, cbeg, lane_row, row < p.rows,
+                                             p.cols - (w.col0 + cbeg), acc);
+              }
             }
           }
         }
         if (do_epi) {
-#pragma unroll
-          for (int c = 0; c < CPT; c += CW) {
-            uint32_t r[CW];
-#pragma unroll
-            for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
-            epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + cbeg + c, r);
-          }
+          EG_ACT_DISPATCH(p.act, (promoted_store<IN, SC, SWAP, CW, CPT, A_>(p, row, w.col0 + cbeg, acc)))
         }
       } else {
         // ---- accumulator in TMEM buffer blk&1 until the unit is done ----
@@ -1859,6 +1998,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
         ++blk;
       }
     }
+    // block scales: no copy of this thread may still be landing in shared
+    // memory when the CTA leaves (the loop can end early on a timeout)
+    if constexpr (SC == SC_BLOCK) cp_async_wait<0>();
     if (ept == 0) trace_point(p, TR_EPI_DONE);
   }
 
@@ -1872,11 +2014,16 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
   if (warp == 1) {
     tc_fence_after();
     if (has_work) {
-      // every UMMA this CTA issued has completed before TMEM is released
-      bool done = true;
-      if (lane == 0) done = mbar_wait(mma_done, 0, lim);
-      done = __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
-      if (!done && lane == 0) record_status(p.status, ST_TIMEOUT_TEARDOWN);
+      // every UMMA this CTA issued has completed before TMEM is released.
+      // The issuer commits mma_done on every exit path, timeouts included,
+      // and UMMAs read only shared and tensor memory, so the commit always
+      // arrives; a wait that runs out is recorded and waited again with a
+      // limit eight times longer before the columns are freed.
+      if (lane == 0 && !mbar_wait(mma_done, 0, lim)) {
+        record_status(p.status, ST_TIMEOUT_TEARDOWN);
+        (void)mbar_wait(mma_done, 0, 8 * lim);
+      }
+      __syncwarp();
     }
     __syncwarp();
     if constexpr (PR)

@@ -11,6 +11,7 @@ bool lookup_e4m3_block_noswap(int bn, KernelEntry* out) {
     case 32: EG_KERNEL_ENTRY(IN_E4M3, SC_BLOCK, false, 32);
     case 64: EG_KERNEL_ENTRY(IN_E4M3, SC_BLOCK, false, 64);
     case 128: EG_KERNEL_ENTRY(IN_E4M3, SC_BLOCK, false, 128);
+    case 256: EG_KERNEL_ENTRY(IN_E4M3, SC_BLOCK, false, 256);
     default: return false;
   }
 }

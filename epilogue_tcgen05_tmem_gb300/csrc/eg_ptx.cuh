@@ -261,6 +261,28 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------- register split ----
+// Per-warp register reallocation: every warp of a warpgroup executes the
+// same form; `dec` returns registers to the block's pool, `inc` waits until
+// the pool can grant the new count.  The counts the warpgroups settle on
+// must fit within the registers the block was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
+// Make later uses of r[0..N) depend on this point: after tcgen05.wait::ld
+// the compiler must not read the registers a tcgen05.ld wrote any earlier.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t* r) {
+#pragma unroll
+  for (int j = 0; j < N; ++j) asm volatile("" : "+r"(r[j])::"memory");
+}
+
 // ------------------------------------------------------------- tcgen05 ----
 
 // Allocate `ncols` TMEM columns (power of two, >= 32); the warp executes this

@@ -13,6 +13,7 @@ struct KernelEntry {
   int elems_per_stage = 0;       // K elements one stage covers
   int tmem_cols = 0;             // TMEM columns one CTA allocates
   int acc_n = 0;                 // accumulator columns per unit (gated: 2 tile_n)
+  int regsplit_need = 0;         // registers a setmaxnreg split needs (0: none)
 };
 
 // Each returns false when bn has no instantiation for that kind and swap.
@@ -49,5 +50,6 @@ bool lookup_e4m3_tc_pair(int bn, KernelEntry* out);
     out->elems_per_stage = C_::kElemsPerStage;                                         \
     out->tmem_cols = static_cast<int>(C_::kTmemCols);                                  \
     out->acc_n = C_::kAccN;                                                            \
+    out->regsplit_need = C_::kRegSplitNeed;                                            \
     return true;                                                                       \
   } while (0)

@@ -37,8 +37,8 @@ L2_BYTES = 129 * 2 ** 20
 
 
 def candidates(p, swaps=(0, 1)):
-    promote = p.scale == "block" or p.dtype == "int8"
-    max_bn = 64 if p.dtype == "int8" else (128 if promote else 256)
+    # block scales: tiles up to 128 wide, and 256 wide with rows over M
+    max_bn = 64 if p.dtype == "int8" else 256
     elems = 64 if p.dtype == "bf16" else 128
     k_tiles = -(-p.K // elems)
     if p.M > 32:
@@ -50,6 +50,8 @@ def candidates(p, swaps=(0, 1)):
             if bn > max_bn:
                 continue
             if bn > 16 and bn // 2 >= cols:          # a smaller tile already covers cols
+                continue
+            if p.scale == "block" and bn > 128 and swap:
                 continue
             for stages in (2, 3, 4, 6, 8):
                 for s in SPLITS:
@@ -80,6 +82,8 @@ def _midrange_candidates(p, swaps, max_bn, k_tiles):
             # tile_n 192 and 224 (whole waves for some N) exist without
             # swap-AB for bf16 and per-token/channel FP8
             if bn in (192, 224) and (swap or p.scale == "block" or p.dtype == "int8"):
+                continue
+            if p.scale == "block" and bn > 128 and swap:
                 continue
             for stages in (3, 4, 6):
                 for s in (1, 2, 4):

@@ -232,7 +232,8 @@ EG_API eg_status eg_plan_get_tuning(const eg_plan* plan, eg_tuning* out);
 
 /* Queue one fused linear-layer call on `stream` (a cudaStream_t; NULL is the
  * legacy default stream).  With EG_RUN_GRAPH the call is captured once per
- * distinct argument set into a CUDA graph and replayed on later calls. */
+ * distinct argument set into a CUDA graph and replayed on later calls; the
+ * plan keeps the 8 most recently used graphs and destroys older ones. */
 EG_API eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream);
 
 /* The unfused comparison path of the same problem: the same GEMM kernel
@@ -244,7 +245,10 @@ EG_API eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T
                               void* T2, void* stream);
 
 /* Synchronise the plan's last queued work and report a device-side wait
- * timeout recorded by its kernels (EG_ERR_DEVICE_TIMEOUT, then cleared). */
+ * timeout recorded by its kernels (EG_ERR_DEVICE_TIMEOUT, then cleared).
+ * After a timeout the plan's split-K arrival counters and workspace are
+ * reset as well (a CTA that gave up leaves its tiles half counted), so the
+ * plan's next run is correct. */
 EG_API eg_status eg_plan_device_status(eg_plan* plan);
 
 /* Free everything the plan owns.  NULL is accepted. */
@@ -256,9 +260,12 @@ EG_API int32_t eg_plan_last_launch_count(const eg_plan* plan);
 
 /* Testing hook for failure detection: limit every device pipeline wait of
  * this plan to `wait_limit_ns` nanoseconds (0 restores the default of
- * 2 s), and, when `stall_producer` is non-zero, have the load warp issue no
- * loads so that the first wait runs out.  No fault, trap or hang results:
- * the kernel records EG_ERR_DEVICE_TIMEOUT and returns. */
+ * 2 s), and have the load warp issue no loads so that the first wait runs
+ * out: `stall_producer` 1 in every CTA, 2 in odd-numbered CTAs only (the
+ * others finish their work and count their split-K arrivals, leaving tiles
+ * half counted), 0 off; other values are EG_ERR_INVALID_ARG.  No fault,
+ * trap or hang results: the kernel records EG_ERR_DEVICE_TIMEOUT and
+ * returns. */
 EG_API eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns,
                                  int32_t stall_producer);
 
@@ -297,7 +304,9 @@ EG_API eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace
  * eg_plan_run.  EG_RUN_GRAPH is rejected.
  *
  * The first call on each device looks up the array's device address; make
- * that first call before any stream capture.  Every call clears the tile
+ * that first call before any stream capture.  The address is kept for the
+ * life of the process, so a device reset (cudaDeviceReset) after the first
+ * call on that device is not supported.  Every call clears the tile
  * counters and the status word on `stream` before its kernel; the split-K
  * partial sums are written before they are read.  All calls share the one
  * array: calls that overlap on the GPU (other streams, other threads) race

@@ -158,3 +158,12 @@ def test_sweep_pair_candidates():
                and c["cluster_reduce"] == 0 and c["tile_n"] in (128, 256) for c in pairs)
     pb = inputs.make_problem(256, 512, 256, "e4m3", "block", seed=0)
     assert not [c for c in sweep.candidates(pb, swaps=(0,)) if c["cta_pair"]]
+
+
+def test_sweep_block_wide_tiles_only_over_m():
+    """Block-scale tiles 256 wide exist with rows over M only."""
+    from epilogue_tcgen05_tmem_gb300 import inputs, sweep
+    pb = inputs.make_problem(512, 1024, 512, "e4m3", "block", seed=0)
+    cands = list(sweep.candidates(pb, swaps=(0, 1)))
+    wide = [c for c in cands if c["tile_n"] > 128]
+    assert wide and all(c["swap_ab"] == 0 and c["tile_n"] == 256 for c in wide)

@@ -144,6 +144,13 @@ def test_fp8_dynamic_full_size_sampled(M):
     _sampled(p, y)
 
 
+def test_fp8_dynamic_m2048_full_size_sampled():
+    """K=4096 N=12288 at 2048 tokens (the table's large-M row), sampled."""
+    p = inputs.workload("fp8_dynamic", 2048)
+    y, _ = run(p)
+    _sampled(p, y, npts=1500)
+
+
 # ------------------------------------------------------------ INT8 ------
 
 @pytest.mark.parametrize("M,N,K", [(1, 136, 384), (7, 256, 1024), (32, 384, 2048), (130, 200, 640)])
@@ -183,11 +190,45 @@ def test_block_fp8_small(M, N, K):
     check_full(p, dict(tile_n=128, stages=4, split_k=1, swap_ab=0))
 
 
-@pytest.mark.parametrize("M", [1, 32])
+@pytest.mark.parametrize("M", [1, 32, 2048])
 def test_block_fp8_full_size_sampled(M):
     p = inputs.workload("block_fp8", M)
     y, _ = run(p)
-    _sampled(p, y)
+    _sampled(p, y, npts=1500 if M > 32 else 600)
+
+
+WIDE_BLOCK = [
+    dict(tile_n=256, stages=4, split_k=1, swap_ab=0),
+    dict(tile_n=256, stages=3, split_k=1, swap_ab=0, stream_k=1),
+    dict(tile_n=256, stages=2, split_k=2, swap_ab=0),          # accumulator-commit release
+]
+
+
+@pytest.mark.parametrize("tuning", WIDE_BLOCK)
+@pytest.mark.parametrize("M,N,K", [(300, 640, 1024), (130, 512, 2048), (17, 256, 384)])
+def test_block_fp8_wide_tiles(M, N, K, tuning):
+    """256-wide promotion tiles (two weight blocks per tile, 128 running sums
+    per epilogue thread, scales read per K block into registers): ragged M,
+    N not a multiple of 256 (the second weight block of the last tile lies
+    past N), several K splits."""
+    p = inputs.make_problem(M, N, K, "e4m3", "block", act="gelu_erf", bias=True,
+                            residual=True, seed=17)
+    check_full(p, tuning)
+
+
+def test_block_fp8_wide_tiles_debug_accumulators():
+    p = inputs.make_problem(140, 384, 640, "e4m3", "block", seed=19)
+    yacc, _ = run(p, dict(tile_n=256, stages=4, split_k=1, swap_ab=0), debug=True)
+    _, acc, _ = oracle.linear(p, want_acc=True)
+    rms = float(np.sqrt(np.mean(acc ** 2)))
+    assert float(np.max(np.abs(yacc.numpy().astype(np.float64) - acc))) <= 1e-4 * rms
+
+
+def test_block_fp8_wide_tiles_reject_cluster_reduce():
+    with pytest.raises(eg.EgError) as ei:
+        eg.Plan(256, 512, 1024, "e4m3", "block",
+                tuning=dict(tile_n=256, stages=3, split_k=2, swap_ab=0, cluster_reduce=1))
+    assert ei.value.status == eg.EG_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------- debug accumulators ---
@@ -215,6 +256,22 @@ def test_graph_mode_matches_direct_and_recaptures():
     y2, _ = run(p, plan=plan, d=d2)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert_close_rms(bits(y2), ref)
+    plan.close()
+
+
+def test_graph_cache_evicts_and_recaptures():
+    """More distinct argument sets than the plan keeps graphs for: every
+    call is still right, also when an evicted set comes back."""
+    p = inputs.make_problem(8, 256, 512, "e4m3", "token_channel", act="silu", bias=True, seed=4)
+    ref = oracle.linear(p)
+    plan = make_plan(p, graph=True)
+    ds = [to_device(p) for _ in range(11)]
+    for rnd in range(2):
+        for d in ds:
+            d["Y"].fill_(0)
+            y, _ = run(p, plan=plan, d=d)
+            assert plan.last_launch_count() == 1
+            assert_close_rms(bits(y), ref)
     plan.close()
 
 
@@ -250,6 +307,40 @@ def test_device_wait_timeout_reported_without_hang():
     plan.set_test_stall(0, False)
     y, _ = run(p, plan=plan, d=d)
     assert_close_rms(bits(y), oracle.linear(p))
+    plan.close()
+
+
+@pytest.mark.parametrize("dtype,M,N,K,tuning", [
+    ("e4m3", 8, 1024, 4096, dict(tile_n=16, stages=4, split_k=4, swap_ab=1)),
+    ("int8", 4, 1024, 8192, dict(tile_n=16, stages=3, split_k=8, swap_ab=1)),
+])
+def test_timeout_in_some_ctas_then_split_k_plan_recovers(dtype, M, N, K, tuning):
+    """Odd-numbered CTAs stall: the others finish their splits and count
+    their arrivals, so every tile is left half counted (and, for INT8, slot
+    0 of the workspace holds partial sums).  After the timeout is reported
+    the plan's next run must match the oracle."""
+    p = inputs.make_problem(M, N, K, dtype, "token_channel", act="silu", bias=dtype == "e4m3",
+                            residual=dtype == "int8", seed=7)
+    plan = make_plan(p, tuning)
+    d = to_device(p)
+    plan.set_test_stall(5_000_000, 2)              # 5 ms, odd CTAs' load warps idle
+    plan.run(d["A"], d["W"], d["Y"], d["s_a"], d["s_w"], d["bias"], d["residual"])
+    assert plan.device_status() == eg.EG_ERR_DEVICE_TIMEOUT
+    plan.set_test_stall(0, 0)
+    for _ in range(2):
+        y, _ = run(p, plan=plan, d=d)
+        ref = oracle.linear(p)
+        if dtype == "int8":
+            assert ulp_dist(bits(y), ref).max() <= 1
+        else:
+            assert_close_rms(bits(y), ref)
+    plan.close()
+
+
+def test_test_stall_rejects_unknown_modes():
+    p = inputs.make_problem(8, 256, 512, "bf16", seed=1)
+    plan = make_plan(p)
+    assert eg.eg_plan_set_test_stall(plan.handle, 0, 3) == eg.EG_ERR_INVALID_ARG
     plan.close()
 
 

@@ -4,10 +4,15 @@ Callers such as code running inside a memory pool or arena that owns the
 whole device, or runtimes that forbid cudaMalloc once they are running,
 cannot let the library allocate its split-K scratch.  eg_linear_noalloc
 runs the same kernel with that scratch in a fixed array compiled into the
-library.  These tests call it through the C ABI on split-K problems and
-compare its output with the plan-based entry point's (eg_plan_create +
-eg_plan_run) under the tolerance the parity tests use, on two calls in a
-row: the second call finds the array holding the first call's leftovers.
+library.  These tests call it through the C ABI on split-K problems, on two
+calls in a row (the second call finds the array holding the first call's
+leftovers), and check that:
+
+* its output is bit-identical to the plan-based entry point's
+  (eg_plan_create + eg_plan_run): both run the same kernel with the same
+  split order;
+* both meet the parity bound against the oracle;
+* the device's free memory does not change across a call.
 
 This file is collected last on purpose; it also passes on its own in a
 fresh process.
@@ -20,7 +25,8 @@ import torch
 
 import epilogue_tcgen05_tmem_gb300 as eg
 from epilogue_tcgen05_tmem_gb300 import inputs
-from tests._gpu_helpers import assert_close_rms, bits, make_plan, to_device
+import oracle
+from tests._gpu_helpers import assert_close_rms, bits, make_plan, to_device, ulp_dist
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +49,7 @@ def _plan_output(p, tuning):
     return y
 
 
-def _noalloc_output(p, tuning):
+def _noalloc_call(p, tuning, d):
     flags = 0
     if p.bias is not None:
         flags |= eg.EG_EPI_BIAS
@@ -51,7 +57,6 @@ def _noalloc_output(p, tuning):
         flags |= eg.EG_EPI_RESIDUAL_PRE_ACT if p.residual_pre_act else eg.EG_EPI_RESIDUAL
     prob = eg.make_problem(p.M, p.N, p.K, p.dtype, p.scale, p.act, flags)
     t = eg.make_tuning(**tuning)
-    d = to_device(p)
     args = eg.eg_args(d["A"].data_ptr(), d["W"].data_ptr(),
                       None if d["s_a"] is None else d["s_a"].data_ptr(),
                       None if d["s_w"] is None else d["s_w"].data_ptr(),
@@ -60,8 +65,24 @@ def _noalloc_output(p, tuning):
                       d["Y"].data_ptr(), p.K, p.K, p.N, p.N)
     s = eg.eg_linear_noalloc(prob, t, args, torch.cuda.current_stream().cuda_stream)
     assert s == eg.EG_OK, eg.last_error_detail()
+
+
+def _noalloc_output(p, tuning):
+    d = to_device(p)
+    _noalloc_call(p, tuning, d)
     torch.cuda.synchronize()
     return d["Y"].cpu()
+
+
+def _check_pair(p, tuning):
+    ref = oracle.linear(p)
+    want = bits(_plan_output(p, tuning))
+    got = bits(_noalloc_output(p, tuning))
+    assert np.array_equal(got, want), "no-alloc output differs from the plan path's"
+    if p.dtype == "int8":
+        assert ulp_dist(got, ref).max() <= 1
+    else:
+        assert_close_rms(got, ref)
 
 
 @pytest.mark.parametrize("tuning", [
@@ -74,23 +95,39 @@ def test_noalloc_matches_plan_entry_two_calls(tuning):
     second = inputs.make_problem(8, 2048, 4096, "e4m3", "token_channel", act="silu", bias=True,
                                  outlier_frac=0.01, seed=32)
     for p in (first, second):
-        ref = _plan_output(p, tuning)
-        got = _noalloc_output(p, tuning)
-        assert_close_rms(bits(got), bits(ref))
+        _check_pair(p, tuning)
 
 
 def test_noalloc_int8_split_k_two_calls():
     t = dict(tile_n=16, stages=3, split_k=8, swap_ab=1)
     for seed in (41, 42):
         p = inputs.make_problem(4, 1024, 8192, "int8", "token_channel", residual=True, seed=seed)
-        ref = _plan_output(p, t)
-        got = _noalloc_output(p, t)
-        assert np.array_equal(bits(got), bits(ref))
+        _check_pair(p, t)
+
+
+def test_noalloc_leaves_free_device_memory_unchanged():
+    """The call's whole contract: no device allocation.  The first call on
+    the device may load the library's module (and with it the scratch
+    array); across every later call the device's free memory must not
+    move."""
+    t = dict(tile_n=16, stages=4, split_k=4, swap_ab=1)
+    p = inputs.make_problem(8, 2048, 4096, "e4m3", "token_channel", act="silu", bias=True,
+                            outlier_frac=0.01, seed=33)
+    d = to_device(p)
+    _noalloc_call(p, t, d)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc_call(p, t, d)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory moved by {free0 - free1} bytes"
+    assert_close_rms(bits(d["Y"].cpu()), oracle.linear(p))
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    # 64-way split of a 12288 x 4096 FP8 layer at tile_n 32 needs far more
-    # than the fixed array holds
+    # a 32-way split of a 12288 x 4096 FP8 layer at tile_n 32 needs far
+    # more split-K scratch than the fixed array holds
     p = inputs.make_problem(32, 12288, 4096, "e4m3", "token_channel", seed=1)
     prob = eg.make_problem(p.M, p.N, p.K, "e4m3", "token_channel")
     t = eg.make_tuning(tile_n=32, stages=4, split_k=32, swap_ab=1)
