@@ -655,8 +655,20 @@ def run_trace_timeline(args):
         torch.cuda.synchronize()
         t = buf.cpu().numpy()
         st, en = t[:, 0][t[:, 0] > 0], t[:, 7][t[:, 7] > 0]
+        # the split-K last arrivers' reduction and store (store_begin ->
+        # epilogue done) and everyone else's arrival -> epilogue done
+        last = t[:, 14] > 0
+        red = (t[last, 6] - t[last, 14]) / 1e3
+        red_only = (t[last & (t[:, 13] > 0), 13] - t[last & (t[:, 13] > 0), 14]) / 1e3
+        rest = (t[~last & (t[:, 12] > 0), 6] - t[~last & (t[:, 12] > 0), 12]) / 1e3
         iso[f"M{M}_set{j}"] = {"event_us": round(e0.elapsed_time(e1) * 1e3, 3),
                                "trace_span_us": round((int(en.max()) - int(st.min())) / 1e3, 3),
+                               "last_arriver_reduce_store_us": [round(float(np.percentile(red, q)), 3)
+                                                                for q in (0, 50, 90, 100)] if red.size else None,
+                               "last_arriver_reduce_first_chunk_us": [round(float(np.percentile(red_only, q)), 3)
+                                                                      for q in (0, 50, 90, 100)] if red_only.size else None,
+                               "others_arrived_to_done_us": [round(float(np.percentile(rest, q)), 3)
+                                                             for q in (0, 50, 90, 100)] if rest.size else None,
                                "points": trace_mod.summarize(t)}
         del gi
     for _, _, pl, _ in calls:

@@ -36,9 +36,11 @@ EXPORTED = ("eg_plan_create", "eg_plan_workspace_bytes", "eg_plan_get_tuning", "
             "eg_plan_last_launch_count", "eg_plan_set_test_stall", "eg_plan_get_launch",
             "eg_plan_set_trace", "eg_status_string", "eg_last_error_detail",
             "eg_linear_noalloc", "eg_quantize_rows")
-EG_TRACE_POINTS = 8
+EG_TRACE_POINTS = 16
 TRACE_POINT_NAMES = ("start", "setup", "first_tma", "first_operands", "last_commit",
-                     "first_acc", "epilogue_done", "end")
+                     "first_acc", "epilogue_done", "end", "pre_issued", "last_load",
+                     "last_acc", "partial_out", "arrived", "reduced", "store_begin",
+                     "unused15")
 
 
 class eg_problem(ctypes.Structure):

@@ -126,6 +126,14 @@ struct eg_plan {
   const void* mapW = nullptr;
   int64_t map_lda = 0, map_ldw = 0;
   CUtensorMap tmP{}, tmQ{};
+  // staged TMA stores of Y (rows over M, 2-byte outputs): shared-memory
+  // offset of the epilogue warps' staging boxes, and the cached tensor map
+  // of the Y the last run wrote
+  bool stage_ok = false;
+  uint32_t out_stage_off = 0;
+  CUtensorMap tmY{};
+  const void* mapY = nullptr;
+  int64_t map_ldy = 0;
   std::vector<GraphEntry> graphs;
   cudaStream_t cap_stream = nullptr;
   int last_launches = 0;
@@ -286,6 +294,37 @@ eg_status validate_tuning(const eg_problem& p, const eg_tuning& t, eg::KernelEnt
   return EG_OK;
 }
 
+// Reserve the epilogue warps' staging boxes for staged TMA stores of Y
+// (rows over M, bf16 / fp16 output) when the epilogue can use them and the
+// shared memory they take neither exceeds the per-block limit nor lowers the
+// number of CTAs an SM holds.  EG_STAGED_STORE=0 turns them off.
+void plan_staging(eg_plan* pl, int dev) {
+  const eg_problem& p = pl->prob;
+  const eg_tuning& t = pl->tune;
+  pl->stage_ok = false;
+  pl->out_stage_off = 0;
+  if (const char* e = getenv("EG_STAGED_STORE"))
+    if (atoi(e) == 0) return;
+  if (t.swap_ab || t.cluster_reduce || (p.flags & (EG_EPI_GATED | EG_OUT_E4M3 | EG_OUT_DEBUG_ACCUM)))
+    return;
+  if (pl->ke.cw != 32 && pl->ke.cw != 16) return;
+  // boxes after the ring, barriers and block scales, on a 1 KB boundary of
+  // the kernel's aligned shared-memory base (pl->smem counts 1 KB of slack)
+  const uint32_t off = (pl->smem - 1024u + 1023u) & ~1023u;
+  const uint32_t total =
+      1024u + off + static_cast<uint32_t>(pl->ke.epi_warps) * 2u * 32u * static_cast<uint32_t>(pl->ke.cw) * 2u;
+  if (total > kMaxSmem) return;
+  int sm_smem = 0, reserved = 0;
+  if (cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+    return;
+  if (sm_smem / static_cast<int>(total + reserved) < sm_smem / static_cast<int>(pl->smem + reserved))
+    return;
+  pl->stage_ok = true;
+  pl->out_stage_off = off;
+  pl->smem = total;
+}
+
 int sm_count_of(int dev) {
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
@@ -390,6 +429,26 @@ eg_status encode_map(CUtensorMap* m, const void* base, int dtype, int64_t rows, 
   return EG_OK;
 }
 
+// Tensor map of a 2-byte output Y [M][ldy] for the epilogue's staged
+// stores: boxes of `cw` columns x 32 rows, swizzled as the kernel writes its
+// staging boxes (64-byte rows for 32 columns, 32-byte rows for 16).
+eg_status encode_ymap(CUtensorMap* m, const void* Y, int64_t M, int64_t N, int64_t ldy, int cw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(EG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldy * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(cw), 32u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(Y), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  cw == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(EG_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for Y (M=%lld N=%lld ldy=%lld)",
+                static_cast<int>(r), (long long)M, (long long)N, (long long)ldy);
+  return EG_OK;
+}
+
 bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   if (!a || !b || an == 0 || bn == 0) return false;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -475,6 +534,22 @@ eg_status ensure_maps(eg_plan* pl, const eg_args* a) {
   return EG_OK;
 }
 
+// Staged TMA stores for this run's Y: the plan reserved the staging boxes,
+// the output is bf16 / fp16 (not the debug accumulators) and Y and its row
+// stride are 16-byte aligned.  Encodes (and caches) Y's tensor map.
+eg_status ensure_ymap(eg_plan* pl, void* Y, int64_t ldy, uint32_t kflags, bool* use) {
+  const eg_problem& p = pl->prob;
+  *use = pl->stage_ok && !(kflags & eg::F_DEBUG) && !(p.flags & EG_OUT_E4M3) && aligned16(Y) &&
+         (ldy * 2) % 16 == 0;
+  if (!*use) return EG_OK;
+  if (pl->mapY == Y && pl->map_ldy == ldy) return EG_OK;
+  eg_status s = encode_ymap(&pl->tmY, Y, p.M, p.N, ldy, pl->ke.cw);
+  if (s != EG_OK) return s;
+  pl->mapY = Y;
+  pl->map_ldy = ldy;
+  return EG_OK;
+}
+
 eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t flags, void* Y,
                         int64_t ldy) {
   const eg_problem& p = pl->prob;
@@ -519,6 +594,7 @@ eg::KParams make_params(const eg_plan* pl, const eg_args* a, int act, uint32_t f
   k.trace = pl->trace;
   k.trace_ctas = pl->trace_ctas;
   k.cluster_reduce = pl->tune.cluster_reduce;
+  k.out_stage_off = pl->out_stage_off;
   // streamed weights: hint L2 to evict them first when the grid reads each
   // weight tile once (one tile column / row over the tokens)
   const bool w_once = pl->tune.swap_ab ? (pl->tiles_cols == 1) : (pl->tiles_rows == 1);
@@ -597,8 +673,8 @@ eg_status launch_fused(eg_plan* pl, const eg::KParams& kp, cudaStream_t st) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  void* args[3] = {const_cast<CUtensorMap*>(&pl->tmP), const_cast<CUtensorMap*>(&pl->tmQ),
-                   const_cast<eg::KParams*>(&kp)};
+  void* args[4] = {const_cast<CUtensorMap*>(&pl->tmP), const_cast<CUtensorMap*>(&pl->tmQ),
+                   const_cast<CUtensorMap*>(&pl->tmY), const_cast<eg::KParams*>(&kp)};
   EG_CUDA(cudaLaunchKernelExC(&cfg, pl->ke.fn, args), "launching the fused kernel");
   return EG_OK;
 }
@@ -772,6 +848,7 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   e = cudaFuncSetAttribute(ke.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "setting the shared-memory carveout"));
+  plan_staging(pl, dev);
   int per_sm = 0;
   if ((s = residency(pl, dev, &per_sm)) != EG_OK) return cleanup(s);
   plan_grid(pl, sm_count_of(dev), per_sm);
@@ -866,7 +943,10 @@ static eg_status run_direct(eg_plan* pl, const eg_args* a, cudaStream_t st) {
   }
   eg_status s = ensure_maps(pl, a);
   if (s != EG_OK) return s;
+  bool ts = false;
+  if ((s = ensure_ymap(pl, a->Y, a->ldy, epi_flags(p.flags), &ts)) != EG_OK) return s;
   eg::KParams kp = make_params(pl, a, p.act, epi_flags(p.flags), a->Y, a->ldy);
+  kp.tma_store = ts ? 1 : 0;
   if (p.flags & EG_RUN_QUANT_A) kp.pdl = 1;
   return launch_fused(pl, kp, st);
 }
@@ -944,7 +1024,10 @@ eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1, void
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((s = ensure_maps(plan, args)) != EG_OK) return s;
   // 1) the same GEMM kernel with no epilogue terms: T1 = bf16(scaled acc)
-  const eg::KParams kp = make_params(plan, args, eg::ACT_NONE, 0u, T1, p.N);
+  bool ts = false;
+  if ((s = ensure_ymap(plan, T1, p.N, 0u, &ts)) != EG_OK) return s;
+  eg::KParams kp = make_params(plan, args, eg::ACT_NONE, 0u, T1, p.N);
+  kp.tma_store = ts ? 1 : 0;
   if ((s = launch_fused(plan, kp, st)) != EG_OK) return s;
   const int64_t nv = p.M * (p.N / 8);
   const int threads = 256;
@@ -1099,6 +1182,7 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
 
   // work decomposition and scratch needs
   const size_t tiles = size_t(pl.tiles_rows) * pl.tiles_cols;
+  plan_staging(&pl, dev);
   int per_sm = 0;
   if ((s = residency(&pl, dev, &per_sm)) != EG_OK) return s;
   plan_grid(&pl, sm_count_of(dev), per_sm);
@@ -1134,7 +1218,10 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
     EG_CUDA(cudaMemsetAsync(pl.ws, 0, tiles * size_t(pl.ke.acc_n) * 128 * 4, st),
             "clearing the INT8 split-K sums");
   if ((s = ensure_maps(&pl, args)) != EG_OK) return s;
-  const eg::KParams kp = make_params(&pl, args, p.act, epi_flags(p.flags), args->Y, args->ldy);
+  bool ts = false;
+  if ((s = ensure_ymap(&pl, args->Y, args->ldy, epi_flags(p.flags), &ts)) != EG_OK) return s;
+  eg::KParams kp = make_params(&pl, args, p.act, epi_flags(p.flags), args->Y, args->ldy);
+  kp.tma_store = ts ? 1 : 0;
   return launch_fused(&pl, kp, st);
 }
 

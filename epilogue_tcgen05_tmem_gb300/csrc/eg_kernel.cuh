@@ -96,11 +96,23 @@ struct KParams {
   int32_t cluster_reduce;         // split-K through distributed shared memory
   int32_t out;                    // OUT_BF16 / OUT_F16 / OUT_E4M3
   const float* s_y;               // per-tensor output scale (OUT_E4M3)
+  int32_t tma_store;              // rows over M, 2-byte outputs: staged TMA stores of Y
+  uint32_t out_stage_off;         // shared-memory offset of the staging boxes
 };
 
-constexpr int kTracePoints = 8;
+constexpr int kTracePoints = 16;
 enum : int { TR_START = 0, TR_SETUP = 1, TR_FIRST_TMA = 2, TR_FIRST_OPERANDS = 3,
-             TR_LAST_COMMIT = 4, TR_FIRST_ACC = 5, TR_EPI_DONE = 6, TR_END = 7 };
+             TR_LAST_COMMIT = 4, TR_FIRST_ACC = 5, TR_EPI_DONE = 6, TR_END = 7,
+             // producer: first-unit weight loads (and L2 prefetches) issued,
+             // before the wait on the previous kernel; last load issued
+             TR_PRE_ISSUED = 8, TR_LAST_LOAD = 9,
+             // epilogue (first epilogue thread, the CTA's last unit):
+             // accumulator final; split-K partial stored or sent; arrival
+             // counted (workspace) or all partials received (cluster); the
+             // last arriver's first chunk reduced (tensor-memory accumulator
+             // path); output stores begin.  Point 15 is not recorded.
+             TR_LAST_ACC = 10, TR_PARTIAL_OUT = 11, TR_ARRIVED = 12, TR_REDUCED = 13,
+             TR_STORE_BEGIN = 14 };
 
 __device__ __forceinline__ void trace_point(const KParams& p, int point) {
   if (p.trace != nullptr && static_cast<int>(blockIdx.x) < p.trace_ctas)
@@ -133,7 +145,12 @@ struct Cfg {
   static constexpr uint32_t kWBytes = SWAP ? kPBytes : kQBytes;  // one weight operand tile
   static constexpr uint32_t kStageBytes =
       kConvert ? kP8Bytes + kQ8Bytes : kPBytes + kQBytes + (G ? kWBytes : 0u);
-  static constexpr int kOpSlots = 2;
+  // INT8 fp16 operand slots (P in tensor memory, Q in shared memory): the
+  // transform of K tile g waits for the UMMAs of tile g - kOpSlots, so
+  // three slots keep two tiles of slack between the transform warps and the
+  // UMMA issuer (at most the accumulator buffers, for the release by the
+  // accumulator commit; 64 + 64 x 3 tensor-memory columns at tile_n 16)
+  static constexpr int kOpSlots = kConvert ? 3 : 2;
   static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * kQBytes : 0u;
   static constexpr uint32_t kTxBytes =  // bytes one stage's TMA delivers (PR: to both CTAs)
       PR ? 2u * (128u + BN / 2) * 128u
@@ -204,6 +221,8 @@ struct Cfg {
   static_assert(!kWidePromote || 128 * kRegsLow + kEpiThreads * kRegsHigh <= kThreads * kMaxRegs,
                 "register split within the launch allocation");
   static_assert(kTmemUsed <= 512, "tensor memory holds 512 columns");
+  static_assert(!kConvert || kOpSlots <= kAccBufs,
+                "an operand slot is released by the accumulator commit of its K tile");
   static_assert(!G || !kPromote, "gated units use the tensor-memory accumulator path");
   static_assert(!PR || (!SWAP && !kPromote && !G && (BN == 128 || BN == 256)),
                 "CTA pairs: tiles of 256 x 128 or 256 x 256, per-token/channel or bf16");
@@ -356,16 +375,6 @@ __device__ __forceinline__ uint16_t out_bits(float v, int out, float inv_sy) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// The same with the format known at compile time (the decode store loop).
-template <int OUT>
-__device__ __forceinline__ uint16_t out_bits_c(float v, float inv_sy) {
-  if constexpr (OUT == OUT_F16) return __half_as_ushort(__float2half_rn(v));
-  if constexpr (OUT == OUT_E4M3)
-    return static_cast<uint16_t>(
-        __nv_cvt_float_to_fp8(__fmul_rn(v, inv_sy), __NV_SATFINITE, __NV_E4M3));
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-
 // 1 / s_y for E4M3 outputs (the multiply may differ from the division by
 // one float32 ulp of v / s_y, far below the E4M3 step).
 __device__ __forceinline__ float out_scale(const KParams& p) {
@@ -462,54 +471,116 @@ __device__ __forceinline__ void load_swap_inputs(const KParams& p, int n, int co
 
 // Swap-AB epilogue compute and store: lanes of a warp hold consecutive n, so
 // each token's residual loads and Y stores are coalesced across the warp.
-// The output format is a compile-time choice here (store_swap picks it once).
-template <int IN, int SC, int CW, int ACT, int OUT>
-__device__ __forceinline__ void store_swap_o(const KParams& p, int n, int col0,
-                                             const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
-  if (n >= p.N) return;
-  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
-  const float sy = out_scale(p);
-  // groups of 8 tokens: the group's loads first, then its arithmetic
-  constexpr int G = CW < 8 ? CW : 8;
+// This path runs once per output tile, in split-K by whichever CTA of the
+// tile arrives last, so its code is usually not in that SM's instruction
+// cache (nor, for a call on its own, in L2): it is kept compact.  A runtime
+// loop walks the chunk's valid tokens four at a time (their loads first,
+// then their arithmetic), the activation is a compile-time choice made once
+// per chunk, and the output format is chosen per element.
+template <int CW>
+__device__ __forceinline__ uint32_t pick(const uint32_t (&v)[CW], int j) {
+  uint32_t x = v[0];
 #pragma unroll
-  for (int g = 0; g < CW; g += G) {
-    float r[G], sa[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const int m = col0 + g + j;
-      r[j] = (has_res && m < p.M) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
-      sa[j] = (SC == SC_TC && m < p.M) ? __ldg(p.s_a + m) : 1.0f;
-    }
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const int m = col0 + g + j;
-      if (m < p.M) {
-        uint16_t o;
-        if (IN == IN_INT8)
-          o = epi_int8<ACT>(static_cast<int32_t>(vals[g + j]), sa[j], in.sw, in.b, r[j], p.flags, OUT, sy);
-        else
-          o = out_bits_c<OUT>(epi_value<ACT>(__uint_as_float(vals[g + j]),
-                                             (SC == SC_TC) ? sa[j] * in.sw : 1.0f, in.b, r[j], p.flags),
-                              sy);
-        const int64_t at = static_cast<int64_t>(m) * p.ldy + n;
-        if constexpr (OUT == OUT_E4M3)
-          reinterpret_cast<uint8_t*>(p.Y)[at] = static_cast<uint8_t>(o);
-        else
-          reinterpret_cast<uint16_t*>(p.Y)[at] = o;
-      }
-    }
-  }
+  for (int k = 1; k < CW; ++k) x = (j == k) ? v[k] : x;
+  return x;
 }
 
 template <int IN, int SC, int CW, int ACT>
 __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
                                            const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
-  if (p.out == OUT_F16)
-    store_swap_o<IN, SC, CW, ACT, OUT_F16>(p, n, col0, vals, in);
-  else if (p.out == OUT_E4M3)
-    store_swap_o<IN, SC, CW, ACT, OUT_E4M3>(p, n, col0, vals, in);
-  else
-    store_swap_o<IN, SC, CW, ACT, OUT_BF16>(p, n, col0, vals, in);
+  if (n >= p.N) return;
+  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
+  const float sy = out_scale(p);
+  const int count = min(CW, p.M - col0);
+#pragma unroll 1
+  for (int j0 = 0; j0 < count; j0 += 4) {
+    float r[4], sa[4];
+    uint32_t v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int m = col0 + j0 + q;
+      const bool ok = j0 + q < count;
+      v[q] = pick<CW>(vals, j0 + q);
+      r[q] = (has_res && ok) ? __bfloat162float(p.R[static_cast<int64_t>(m) * p.ldr + n]) : 0.0f;
+      sa[q] = (SC == SC_TC && ok) ? __ldg(p.s_a + m) : 1.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (j0 + q < count) {
+        uint16_t o;
+        if (IN == IN_INT8)
+          o = epi_int8<ACT>(static_cast<int32_t>(v[q]), sa[q], in.sw, in.b, r[q], p.flags, p.out, sy);
+        else
+          o = out_bits(epi_value<ACT>(__uint_as_float(v[q]), (SC == SC_TC) ? sa[q] * in.sw : 1.0f,
+                                      in.b, r[q], p.flags),
+                       p.out, sy);
+        store_out(p, static_cast<int64_t>(col0 + j0 + q) * p.ldy + n, o);
+      }
+    }
+  }
+}
+
+// Output bits of CW consecutive columns col0 .. col0 + CW - 1 of row m (rows
+// over M, m < M), the fused epilogue applied to the accumulator values
+// `vals` (fp32 bits, or int32 for INT8); columns at or beyond N give 0.
+template <int IN, int SC, int CW, int ACT>
+__device__ __forceinline__ void epi_row_values(const KParams& p, int m, int col0,
+                                               const uint32_t (&vals)[CW], uint16_t (&out)[CW]) {
+  const bool has_bias = (p.flags & F_BIAS) != 0;
+  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
+  const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
+  const float sy = out_scale(p);
+  const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
+  if (p.vec_ok && col0 + CW <= p.N) {
+    // full chunk: 16-byte vector loads of bias / R / s_w
+#pragma unroll
+    for (int g = 0; g < CW / 8; ++g) {
+      uint4 bv = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+      if (has_bias) bv = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + g);
+      if (has_res) rv = __ldg(reinterpret_cast<const uint4*>(rrow + col0) + g);
+      float4 sw0 = make_float4(1, 1, 1, 1), sw1 = make_float4(1, 1, 1, 1);
+      if (SC == SC_TC) {
+        sw0 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g);
+        sw1 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g + 1);
+      }
+      const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+      const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+      const float sws[8] = {sw0.x, sw0.y, sw0.z, sw0.w, sw1.x, sw1.y, sw1.z, sw1.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = g * 8 + h * 2 + e;
+          const float b = bf16_to_f(static_cast<uint16_t>(bw[h] >> (16 * e)));
+          const float r = bf16_to_f(static_cast<uint16_t>(rw[h] >> (16 * e)));
+          if (IN == IN_INT8) {
+            out[j] = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.flags,
+                                   p.out, sy);
+          } else {
+            const float sc = (SC == SC_TC) ? sa * sws[h * 2 + e] : 1.0f;
+            out[j] = out_bits(epi_value<ACT>(__uint_as_float(vals[j]), sc, b, r, p.flags), p.out, sy);
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < CW; ++j) {
+      const int n = col0 + j;
+      out[j] = 0;
+      if (n < p.N) {
+        const float b = has_bias ? __bfloat162float(p.bias[n]) : 0.0f;
+        const float r = has_res ? __bfloat162float(rrow[n]) : 0.0f;
+        const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
+        if (IN == IN_INT8)
+          out[j] = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.flags, p.out, sy);
+        else
+          out[j] = out_bits(epi_value<ACT>(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f,
+                                           b, r, p.flags),
+                            p.out, sy);
+      }
+    }
+  }
 }
 
 // Apply the epilogue to CW consecutive accumulator columns of one TMEM lane
@@ -519,8 +590,6 @@ template <int IN, int SC, bool SWAP, int CW, int ACT>
 __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int col0,
                                                  const uint32_t (&vals)[CW]) {
   const bool debug = (p.flags & F_DEBUG) != 0;
-  const bool has_bias = (p.flags & F_BIAS) != 0;
-  const bool has_res = (p.flags & (F_RES | F_RES_PRE)) != 0;
   if (!SWAP) {
     // row = m, columns = n: a thread owns CW consecutive outputs of one row.
     const int m = row;
@@ -532,46 +601,10 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
         if (col0 + j < p.N) y[col0 + j] = vals[j];
       return;
     }
-    const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
-    const float sy = out_scale(p);
+    uint16_t out[CW];
+    epi_row_values<IN, SC, CW, ACT>(p, m, col0, vals, out);
     const int64_t yrow = static_cast<int64_t>(m) * p.ldy;  // element index of row m
-    const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
     if (p.vec_ok && col0 + CW <= p.N) {
-      // full chunk: 16-byte vector loads of bias / R and vector stores of Y
-      uint16_t out[CW];
-#pragma unroll
-      for (int g = 0; g < CW / 8; ++g) {
-        uint4 bv = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
-        if (has_bias) bv = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + g);
-        if (has_res) rv = __ldg(reinterpret_cast<const uint4*>(rrow + col0) + g);
-        float4 sw0 = make_float4(1, 1, 1, 1), sw1 = make_float4(1, 1, 1, 1);
-        if (SC == SC_TC) {
-          sw0 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g);
-          sw1 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g + 1);
-        }
-        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-        const float sws[8] = {sw0.x, sw0.y, sw0.z, sw0.w, sw1.x, sw1.y, sw1.z, sw1.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint16_t o[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = g * 8 + h * 2 + e;
-            const float b = bf16_to_f(static_cast<uint16_t>(bw[h] >> (16 * e)));
-            const float r = bf16_to_f(static_cast<uint16_t>(rw[h] >> (16 * e)));
-            if (IN == IN_INT8) {
-              o[e] = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sws[h * 2 + e], b, r, p.flags,
-                                   p.out, sy);
-            } else {
-              const float s = (SC == SC_TC) ? sa * sws[h * 2 + e] : 1.0f;
-              o[e] = out_bits(epi_value<ACT>(__uint_as_float(vals[j]), s, b, r, p.flags), p.out, sy);
-            }
-          }
-          out[g * 8 + h * 2] = o[0];
-          out[g * 8 + h * 2 + 1] = o[1];
-        }
-      }
 #pragma unroll
       for (int g = 0; g < CW / 8; ++g) {
         uint16_t o8[8];
@@ -581,21 +614,8 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < CW; ++j) {
-        const int n = col0 + j;
-        if (n >= p.N) break;
-        const float b = has_bias ? __bfloat162float(p.bias[n]) : 0.0f;
-        const float r = has_res ? __bfloat162float(rrow[n]) : 0.0f;
-        const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
-        uint16_t o;
-        if (IN == IN_INT8)
-          o = epi_int8<ACT>(static_cast<int32_t>(vals[j]), sa, sw, b, r, p.flags, p.out, sy);
-        else
-          o = out_bits(epi_value<ACT>(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b,
-                                      r, p.flags),
-                       p.out, sy);
-        store_out(p, yrow + n, o);
-      }
+      for (int j = 0; j < CW; ++j)
+        if (col0 + j < p.N) store_out(p, yrow + col0 + j, out[j]);
     }
   } else {
     // row = n, columns = m: lanes of a warp hold consecutive n, so each
@@ -614,6 +634,63 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
     SwapIn<CW> in;
     load_swap_inputs<SC, CW>(p, n, col0, in);
     store_swap<IN, SC, CW, ACT>(p, n, col0, vals, in);
+  }
+}
+
+// ---------------------------------------------------- staged TMA stores ----
+//
+// Rows over M: a thread holds CW consecutive outputs of one row, so a warp's
+// direct stores touch 32 rows per instruction.  Instead each warp writes its
+// 32 rows x CW columns (2-byte outputs) into a shared-memory staging box in
+// the layout a bulk-tensor store with 64-byte (CW = 32) or 32-byte (CW = 16)
+// swizzle reads, and one lane stores the box with one TMA store (rows and
+// columns outside Y are not written).  Two boxes per warp alternate, so the
+// next chunk is computed while the previous box is read out.
+
+// Bytes of one warp's staging box.
+template <int CW>
+__host__ __device__ constexpr uint32_t stage_box_bytes() { return 32u * CW * 2u; }
+
+// Write row r's CW output bits (2 bytes each) into the swizzled box.
+template <int CW>
+__device__ __forceinline__ void stage_row(uint8_t* box, int r, const uint16_t (&o)[CW]) {
+  static_assert(CW == 32 || CW == 16, "64- or 32-byte box rows");
+#pragma unroll
+  for (int c = 0; c < CW / 8; ++c) {
+    const int pc = (CW == 32) ? (c ^ ((r >> 1) & 3)) : (c ^ ((r >> 2) & 1));
+    uint4 v;
+    v.x = static_cast<uint32_t>(o[8 * c + 0]) | (static_cast<uint32_t>(o[8 * c + 1]) << 16);
+    v.y = static_cast<uint32_t>(o[8 * c + 2]) | (static_cast<uint32_t>(o[8 * c + 3]) << 16);
+    v.z = static_cast<uint32_t>(o[8 * c + 4]) | (static_cast<uint32_t>(o[8 * c + 5]) << 16);
+    v.w = static_cast<uint32_t>(o[8 * c + 6]) | (static_cast<uint32_t>(o[8 * c + 7]) << 16);
+    *reinterpret_cast<uint4*>(box + r * (CW * 2) + pc * 16) = v;
+  }
+}
+
+// The epilogue of one chunk through a staging box: every lane of the warp
+// calls this (row = the lane's row, row_base = the warp's first row).  The
+// box was last used two chunks ago; lane 0 waits until that store has read
+// it.
+template <int IN, int SC, int CW, int ACT>
+__device__ __forceinline__ void epilogue_chunk_staged(const KParams& p, const CUtensorMap* tmY, int row,
+                                                      int row_base, int col0,
+                                                      const uint32_t (&vals)[CW], uint8_t* box,
+                                                      int lane) {
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  uint16_t out[CW];
+  if (row < p.M) {
+    epi_row_values<IN, SC, CW, ACT>(p, row, col0, vals, out);
+  } else {
+#pragma unroll
+    for (int j = 0; j < CW; ++j) out[j] = 0;
+  }
+  stage_row<CW>(box, lane, out);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmY, box, col0, row_base);
+    bulk_commit_group();
   }
 }
 
@@ -636,6 +713,23 @@ __device__ __forceinline__ void promoted_store(const KParams& p, int row, int co
 #pragma unroll
     for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
     epilogue_chunk_a<IN, SC, SWAP, CW, ACT>(p, row, col0 + c, r);
+  }
+}
+
+// The same through staging boxes and TMA stores (rows over M); `nbox`
+// counts the warp's boxes used so far (they alternate).
+template <int IN, int SC, int CW, int CPT, int ACT>
+__device__ __forceinline__ void promoted_store_staged(const KParams& p, const CUtensorMap* tmY, int row,
+                                                      int row_base, int col0, const uint32_t (&acc)[CPT],
+                                                      uint8_t* boxes, uint32_t& nbox, int lane) {
+#pragma unroll
+  for (int c = 0; c < CPT; c += CW) {
+    uint32_t r[CW];
+#pragma unroll
+    for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
+    epilogue_chunk_staged<IN, SC, CW, ACT>(p, tmY, row, row_base, col0 + c, r,
+                                           boxes + (nbox & 1u) * stage_box_bytes<CW>(), lane);
+    ++nbox;
   }
 }
 
@@ -727,16 +821,6 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, uint32_t (&r)[CW
   } else {
     tmem_ld16(taddr, r);
   }
-}
-
-// Promotion of one 32-column piece of a K block: acc[C0 + j] += s * r[j]
-// (float32 bits), with C0 known at compile time so the accumulator array
-// stays in registers.
-template <int C0, int N>
-__device__ __forceinline__ void fma_piece(uint32_t (&acc)[N], const uint32_t (&r)[32], float s) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    acc[C0 + j] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[j]), __uint_as_float(acc[C0 + j])));
 }
 
 // Split-K: store this split's partial for (tile, split); valid entries only.
@@ -1049,9 +1133,17 @@ __device__ __forceinline__ void stage_block_scales(const KParams& p, const Unit&
       cp_async_4(sc_a + t * ss + i, src, ok ? 4u : 0u);
     }
   }
+  // the tile's weight block rows: one, or (rows over M, tiles wider than
+  // 128) one per 128 columns, row h at sc_w + h ss; rows past N read zero
+  constexpr int WR = (!SWAP && BN > 128) ? BN / 128 : 1;
   const int wrow = SWAP ? w.tile_r : (w.col0 / 128);
-  for (int i = ept; i < w.nk; i += NT)
-    cp_async_4(sc_w + i, p.s_w + static_cast<int64_t>(wrow) * p.kb_count + w.kt0 + i, 4u);
+  const int wrows = (p.N + 127) / 128;
+  for (int idx = ept; idx < WR * w.nk; idx += NT) {
+    const int h = idx / w.nk, i = idx - h * w.nk;
+    const bool ok = SWAP || wrow + h < wrows;
+    const float* src = p.s_w + (ok ? static_cast<int64_t>(wrow + h) * p.kb_count + w.kt0 + i : 0);
+    cp_async_4(sc_w + h * ss + i, src, ok ? 4u : 0u);
+  }
 }
 
 // ------------------------------------------- split-K inside a cluster ----
@@ -1144,6 +1236,7 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
   const int S = p.split_k;
   const int R = 128 / S;
   if (!mbar_wait_cluster(red_full, 0, p.wait_limit_ns)) return false;
+  if (ept == 0) trace_point(p, TR_ARRIVED);
   const int rr = ept % R;
   const int row = w.row0 + static_cast<int>(cluster_ctarank()) * R + rr;
   if (row >= p.rows) return true;
@@ -1244,7 +1337,8 @@ template <int IN, int SC, bool SWAP, int BN, bool G = false, bool PR = false>
 __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     __maxnreg__((Cfg<IN, SC, SWAP, BN, G, PR>::kMaxRegs))
     fused_linear_kernel(const __grid_constant__ CUtensorMap tmP,
-                        const __grid_constant__ CUtensorMap tmQ, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmY, const KParams p) {
   using C = Cfg<IN, SC, SWAP, BN, G, PR>;
   constexpr int CW = C::kCW;
   extern __shared__ uint8_t smem_raw[];
@@ -1264,12 +1358,12 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     return C::kConvert ? op_area + (g % C::kOpSlots) * C::kQBytes : stage_base(s);
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(op_area + C::kOpBytes);
-  uint64_t* full = bars;              // TMA landed (expect_tx)
-  uint64_t* empty = bars + S;         // ring stage free (UMMA commit, or converter)
-  uint64_t* bfull = bars + 2 * S;     // [2] fp16 operands ready (INT8)
-  uint64_t* bempty = bars + 3 * S;    // [2] fp16 operands consumed (INT8)
+  uint64_t* full = bars;              // [S] TMA landed (expect_tx)
+  uint64_t* empty = bars + S;         // [S] ring stage free (UMMA commit, or converter)
+  uint64_t* bfull = bars + 2 * S;     // [kOpSlots] fp16 operands ready (INT8)
+  uint64_t* bempty = bfull + C::kOpSlots;  // [kOpSlots] fp16 operands consumed (INT8)
   constexpr int NB = C::kAccBufs;
-  uint64_t* tfull = bars + 4 * S;     // [NB] TMEM buffer holds a finished K block / tile
+  uint64_t* tfull = bempty + C::kOpSlots;  // [NB] TMEM buffer holds a finished K block / tile
   uint64_t* tempty = tfull + NB;      // [NB] TMEM buffer drained by the epilogue
   uint64_t* mma_done = tempty + NB;
   uint64_t* red_full = mma_done + 1;  // cluster split-K: this CTA's rows have all partials
@@ -1300,8 +1394,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::kConvert ? 128 : 1);
-      mbar_init(&bfull[s], 128);
-      mbar_init(&bempty[s], 1);
+    }
+    for (int o = 0; o < C::kOpSlots; ++o) {
+      mbar_init(&bfull[o], 128);
+      mbar_init(&bempty[o], 1);
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(&tfull[b], 1);
@@ -1420,7 +1516,20 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
               tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy);
               if constexpr (G) tma_prefetch_l2_2d(wmap, (w.kt0 + i) * C::kElemsPerStage, wy + p.N);
             }
+            // weights read once per call (decode, rows over N): this CTA's
+            // later units too, so the whole of its weight range streams
+            // into L2 while the previous kernel finishes
+            if (SWAP && p.evict_first_p) {
+              WorkIter it2 = it;
+              Unit w2;
+              while (work_next<PR>(p, BN, it2, w2))
+                for (int i = 0; i < w2.nk; ++i) {
+                  tma_prefetch_l2_2d(wmap, (w2.kt0 + i) * C::kElemsPerStage, w2.row0);
+                  if constexpr (G) tma_prefetch_l2_2d(wmap, (w2.kt0 + i) * C::kElemsPerStage, w2.row0 + p.N);
+                }
+            }
           }
+          trace_point(p, TR_PRE_ISSUED);
           griddep_wait();
           for (int i = 0; i < pre; ++i) load_op(false, w, i, i);
           trace_point(p, TR_FIRST_TMA);
@@ -1451,6 +1560,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           ++gp;
         }
       }
+      trace_point(p, TR_LAST_LOAD);
       // Wind-down: wait (bounded) until every stage this thread armed has
       // received all of its bytes, so that no bulk copy is still landing in
       // shared memory when the CTA leaves after some role gave up on a wait.
@@ -1656,6 +1766,11 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                             static_cast<uint32_t>(cbeg);
     const int ept = threadIdx.x - 32 * C::kEpiWarp0;  // 0 .. kEpiThreads-1
+    // staged TMA stores of Y (rows over M): two boxes per epilogue warp
+    const bool tstore = !SWAP && !G && p.tma_store != 0;
+    uint8_t* boxes = smem + p.out_stage_off +
+                     static_cast<uint32_t>(warp - C::kEpiWarp0) * 2u * stage_box_bytes<CW>();
+    uint32_t nbox = 0;
     griddep_wait();
     uint32_t blk = 0;
     bool ok = true;
@@ -1665,11 +1780,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     // staged one unit ahead, into the other of two buffers, so their global
     // latency overlaps the current unit; with swap-AB (decode, about one unit
     // per CTA) each unit stages its own, all copies in flight at once.
-    // Wide promotion tiles read their two scales per K block straight from
-    // global memory, one block ahead, into registers (no staging buffer).
     constexpr int kScaleRows = SWAP ? BN : 128;
-    constexpr bool kAhead = (SC == SC_BLOCK) && !SWAP && !C::kWidePromote;
-    const int scale_buf_floats = (kScaleRows + 1) * scale_row_stride(p.k_tiles);
+    constexpr int kWRows = (!SWAP && BN > 128) ? BN / 128 : 1;  // weight block rows per tile
+    constexpr bool kAhead = (SC == SC_BLOCK) && !SWAP;
+    const int scale_buf_floats = (kScaleRows + kWRows) * scale_row_stride(p.k_tiles);
     WorkIter it_pf = it;
     uint32_t su = 0;
     if constexpr (kAhead) {
@@ -1701,7 +1815,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           cp_async_commit();
           cp_async_wait<1>();            // this thread's copies for this unit landed
           epi_bar_sync(C::kEpiThreads);  // ... and every thread's
-        } else if constexpr (SC == SC_BLOCK && !C::kWidePromote) {
+        } else if constexpr (SC == SC_BLOCK) {
           epi_bar_sync(C::kEpiThreads);  // the previous unit's reads of this buffer are done
           stage_block_scales<SWAP, BN, C::kEpiThreads>(p, w, sc_a, ept);
           cp_async_commit();
@@ -1710,25 +1824,17 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
         }
         if constexpr (C::kWidePromote) {
           // 128 running sums per thread: one row (m) and the 128 columns of
-          // one weight block (n / 128), so one s_a and one s_w per K block,
-          // loaded a block ahead.  Per K block the buffer is read in four
-          // 32-column pieces, each piece's load in flight while the previous
-          // piece is added (two pieces in registers at a time).
-          const int nbw = (w.col0 + cbeg) >> 7;
-          const bool rv = row < p.M;
-          const bool wv = nbw < (p.N + 127) / 128;
-          const float* sa = p.s_a + (rv ? static_cast<int64_t>(row) * p.kb_count + w.kt0 : 0);
-          const float* sw = p.s_w + (wv ? static_cast<int64_t>(nbw) * p.kb_count + w.kt0 : 0);
-          float sa_n = (rv && w.nk > 0) ? __ldg(sa) : 0.0f;
-          float sw_n = (wv && w.nk > 0) ? __ldg(sw) : 0.0f;
+          // one weight block (n / 128), so one s_a and one s_w per K block
+          // (staged in shared memory one unit ahead).  Per K block the
+          // buffer is read in four 32-column pieces, each piece's load in
+          // flight while the previous piece is added (two pieces in
+          // registers at a time).
+          const float* sa_row = sc_a + lane_row * ss;
+          const float* sw_row = sc_w + (cbeg >> 7) * ss;
           for (int i = 0; i < w.nk; ++i, ++blk) {
             const int b = blk % NB;
             const uint32_t bph = (blk / NB) & 1u;
-            const float srow = sa_n * sw_n;
-            if (i + 1 < w.nk) {
-              sa_n = rv ? __ldg(sa + i + 1) : 0.0f;
-              sw_n = wv ? __ldg(sw + i + 1) : 0.0f;
-            }
+            const float srow = sa_row[i] * sw_row[i];
             if (!mbar_wait(&tfull[b], bph, lim)) {
               record_status(p.status, ST_TIMEOUT_EPILOGUE);
               ok = false;
@@ -1737,25 +1843,29 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             tc_fence_after();
             if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
             const uint32_t tb = t_lane + static_cast<uint32_t>(b * BN);
-            uint32_t ra[32], rb[32];
-            tmem_ld32(tb, ra);
+            // 16-column pieces, the next piece's load in flight while the
+            // current one is added
+            uint32_t rp[2][16];
+            tmem_ld16(tb, rp[0]);
             tmem_ld_wait();
-            reg_fence<32>(ra);
-            tmem_ld32(tb + 32u, rb);
-            fma_piece<0, CPT>(acc, ra, srow);
-            tmem_ld_wait();
-            reg_fence<32>(rb);
-            tmem_ld32(tb + 64u, ra);
-            fma_piece<32, CPT>(acc, rb, srow);
-            tmem_ld_wait();
-            reg_fence<32>(ra);
-            tmem_ld32(tb + 96u, rb);
-            fma_piece<64, CPT>(acc, ra, srow);
-            tmem_ld_wait();
-            reg_fence<32>(rb);
-            tc_fence_before();
-            mbar_arrive(&tempty[b]);  // the buffer is free once all of it is in registers
-            fma_piece<96, CPT>(acc, rb, srow);
+            reg_fence<16>(rp[0]);
+#pragma unroll
+            for (int q = 0; q < CPT / 16; ++q) {
+              if (q + 1 < CPT / 16) {
+                tmem_ld16(tb + static_cast<uint32_t>(16 * (q + 1)), rp[(q + 1) & 1]);
+              } else {
+                tc_fence_before();
+                mbar_arrive(&tempty[b]);  // the buffer is free once all of it is in registers
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                acc[16 * q + j] = __float_as_uint(__fmaf_rn(srow, __uint_as_float(rp[q & 1][j]),
+                                                            __uint_as_float(acc[16 * q + j])));
+              if (q + 1 < CPT / 16) {
+                tmem_ld_wait();
+                reg_fence<16>(rp[(q + 1) & 1]);
+              }
+            }
           }
         } else
         for (int i = 0; i < w.nk; ++i, ++blk) {
@@ -1793,6 +1903,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           }
         }
         if (!ok) break;
+        if (ept == 0) trace_point(p, TR_LAST_ACC);
         // (wide tiles take split-K through the workspace only)
         if constexpr (!C::kWidePromote) {
         if (p.cluster_reduce) {
@@ -1831,7 +1942,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             for (int c = 0; c < CPT; ++c)
               if (row < p.rows && w.col0 + cbeg + c < p.cols)
                 red_add_s32(reinterpret_cast<int*>(wsb + c * 128), static_cast<int32_t>(acc[c]));
+            if (ept == 0) trace_point(p, TR_PARTIAL_OUT);
             do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
+            if (ept == 0) trace_point(p, TR_ARRIVED);
             if (do_epi) {
 #pragma unroll
               for (int c = 0; c < CPT; ++c) {
@@ -1847,7 +1960,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
 #pragma unroll
             for (int c = 0; c < CPT; ++c)
               if (row < p.rows && w.col0 + cbeg + c < p.cols) __stcg(wsb + c * 128, acc[c]);
+            if (ept == 0) trace_point(p, TR_PARTIAL_OUT);
             do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
+            if (ept == 0) trace_point(p, TR_ARRIVED);
             if (do_epi) {
               if constexpr (CPT > 64) {
                 // 32 columns at a time, so the partials in flight stay small
@@ -1869,7 +1984,18 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           }
         }
         if (do_epi) {
-          EG_ACT_DISPATCH(p.act, (promoted_store<IN, SC, SWAP, CW, CPT, A_>(p, row, w.col0 + cbeg, acc)))
+          if (ept == 0) trace_point(p, TR_STORE_BEGIN);
+          if constexpr (!SWAP) {
+            if (tstore) {
+              EG_ACT_DISPATCH(p.act, (promoted_store_staged<IN, SC, CW, CPT, A_>(
+                                         p, &tmY, row, w.row0 + quarter * 32, w.col0 + cbeg, acc, boxes,
+                                         nbox, lane)))
+            } else {
+              EG_ACT_DISPATCH(p.act, (promoted_store<IN, SC, SWAP, CW, CPT, A_>(p, row, w.col0 + cbeg, acc)))
+            }
+          } else {
+            EG_ACT_DISPATCH(p.act, (promoted_store<IN, SC, SWAP, CW, CPT, A_>(p, row, w.col0 + cbeg, acc)))
+          }
         }
       } else {
         // ---- accumulator in TMEM buffer blk&1 until the unit is done ----
@@ -1891,6 +2017,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           tc_fence_after();
           if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
         }
+        if (ept == 0) trace_point(p, TR_LAST_ACC);
         if (p.cluster_reduce) {
           // the accumulator is final, so every UMMA has completed and this
           // CTA's operand ring is idle
@@ -1910,6 +2037,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             tmem_ld_wait();
             cluster_send<BN, CW>(p, smem_u32(red_buf), red_full, w, lane_row, cbeg + c, r);
           }
+          if (ept == 0) trace_point(p, TR_PARTIAL_OUT);
           tc_fence_before();
           mbar_arrive(&tempty[b]);
           ++blk;
@@ -1938,9 +2066,12 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             for (int j = 0; j < CW; ++j)
               if (row < p.rows && w.col0 + ct + j < p.cols) __stcg(wsb + j * 128, r[j]);
           }
+          if (ept == 0) trace_point(p, TR_PARTIAL_OUT);
           do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
+          if (ept == 0) trace_point(p, TR_ARRIVED);
         }
         if (do_epi) {
+          if (ept == 0) trace_point(p, TR_STORE_BEGIN);
 #pragma unroll 1
           for (int c = 0; c < CPT; c += CW) {
             // this thread's columns cbeg + c ... (tb already points at cbeg)
@@ -1959,6 +2090,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
               // are independent and overlap
               reduce_partials<IN, C::kAccN, CW>(p, w.tile, w.contrib, cc, lane_row, row < p.rows,
                                                 p.cols - (w.col0 + cc), r);
+              if (c == 0 && ept == 0) trace_point(p, TR_REDUCED);
             }
             if constexpr (G) {
               // the up half's columns of the same outputs
@@ -1982,6 +2114,15 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
                 continue;
               }
             }
+            if constexpr (!SWAP && !G) {
+              if (tstore) {
+                EG_ACT_DISPATCH(p.act, (epilogue_chunk_staged<IN, SC, CW, A_>(
+                                           p, &tmY, row, w.row0 + quarter * 32, w.col0 + cc, r,
+                                           boxes + (nbox & 1u) * stage_box_bytes<CW>(), lane)))
+                ++nbox;
+                continue;
+              }
+            }
             epilogue_chunk<IN, SC, SWAP, CW>(p, row, w.col0 + cc, r);
           }
         }
@@ -2001,6 +2142,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     // block scales: no copy of this thread may still be landing in shared
     // memory when the CTA leaves (the loop can end early on a timeout)
     if constexpr (SC == SC_BLOCK) cp_async_wait<0>();
+    // every staged store of Y has read its box and written Y (the grid's
+    // dependents read Y once it completes)
+    if (tstore && lane == 0) bulk_wait_group_all();
     if (ept == 0) trace_point(p, TR_EPI_DONE);
   }
 

@@ -14,6 +14,8 @@ struct KernelEntry {
   int tmem_cols = 0;             // TMEM columns one CTA allocates
   int acc_n = 0;                 // accumulator columns per unit (gated: 2 tile_n)
   int regsplit_need = 0;         // registers a setmaxnreg split needs (0: none)
+  int cw = 0;                    // epilogue chunk columns (staged store box width)
+  int epi_warps = 0;             // epilogue warps (one pair of staging boxes each)
 };
 
 // Each returns false when bn has no instantiation for that kind and swap.
@@ -51,5 +53,7 @@ bool lookup_e4m3_tc_pair(int bn, KernelEntry* out);
     out->tmem_cols = static_cast<int>(C_::kTmemCols);                                  \
     out->acc_n = C_::kAccN;                                                            \
     out->regsplit_need = C_::kRegSplitNeed;                                            \
+    out->cw = C_::kCW;                                                                 \
+    out->epi_warps = C_::kEpiWarps;                                                    \
     return true;                                                                       \
   } while (0)

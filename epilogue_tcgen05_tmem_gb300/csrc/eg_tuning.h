@@ -23,16 +23,16 @@ bool tuning_lookup(const eg_problem& p, int sms, eg_tuning* out);
 bool tuning_default(const eg_problem& p, int sms, eg_tuning* out);
 
 // Shared memory the kernel uses beyond its ring for block scaling: buffers
-// of (tile rows + 1) x (K tiles rounded up to 4, + 4) floats, two without
-// swap-AB (the current unit's block scales and the next unit's, in flight),
-// one with.  Tiles wider than 128 columns (rows over M) read their scales
-// into registers and stage none.
+// of (tile rows + weight block rows) x (K tiles rounded up to 4, + 4)
+// floats, two without swap-AB (the current unit's block scales and the next
+// unit's, in flight), one with.  A tile has one weight block row, or one
+// per 128 columns when it is wider (rows over M).
 inline uint64_t block_scale_smem_bytes(const eg_problem& p, int swap_ab, int tile_n,
                                        int elems_per_stage) {
   if (p.scale != EG_SCALE_BLOCK) return 0;
-  if (!swap_ab && tile_n > 128) return 0;
   const int64_t kt = (p.K + elems_per_stage - 1) / elems_per_stage;
-  return (swap_ab ? 1u : 2u) * static_cast<uint64_t>((swap_ab ? tile_n : 128) + 1) *
+  const int wrows = (!swap_ab && tile_n > 128) ? tile_n / 128 : 1;
+  return (swap_ab ? 1u : 2u) * static_cast<uint64_t>((swap_ab ? tile_n : 128) + wrows) *
          static_cast<uint64_t>((kt + 3) / 4 * 4 + 4) * 4u;
 }
 

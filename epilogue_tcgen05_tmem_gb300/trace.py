@@ -3,8 +3,11 @@
 Each CTA writes EG_TRACE_POINTS %globaltimer stamps (ns): start, setup done,
 first TMA issued (after any wait on the previous kernel), first UMMA
 operands ready, last UMMA committed, first accumulator ready in the
-epilogue, epilogue done, end.  Unwritten points stay at the buffer's fill
-value (0).
+epilogue, epilogue done, end; then the first weight loads issued (before
+the wait on the previous kernel), the last load issued, and for the CTA's
+last work unit the accumulator final, the split-K partial stored or sent,
+the arrival counted or partials received, and the start of the output
+stores.  Unwritten points stay at the buffer's fill value (0).
 """
 from __future__ import annotations
 

@@ -220,7 +220,9 @@ typedef struct eg_plan eg_plan;
  * divide the stages; default two for CTA pairs with 6+ even stages, else
  * one), EG_ACC_RELEASE=0 (promotion kernels release ring stages / INT8
  * operand slots with their own commit instead of the K block's accumulator
- * commit), EG_WAIT_CAP_MS (bound on any in-kernel wait). */
+ * commit), EG_STAGED_STORE=0 (rows-over-M epilogues store Y directly from
+ * registers instead of through shared-memory boxes and TMA stores),
+ * EG_WAIT_CAP_MS (bound on any in-kernel wait). */
 EG_API eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning,
                          eg_plan** out);
 
@@ -279,12 +281,20 @@ EG_API eg_status eg_plan_get_launch(const eg_plan* plan, eg_launch_info* out);
 
 /* Tracing: when `trace` is non-NULL, every later run of this plan records,
  * per CTA, EG_TRACE_POINTS device %globaltimer values (nanoseconds) into
- * trace[cta * EG_TRACE_POINTS + point] for ctas < trace_ctas: CTA start,
- * setup done, first TMA issued, first UMMA operands ready, last UMMA
- * committed, first accumulator ready in the epilogue, epilogue done, CTA
- * end.  The buffer is caller-owned device memory of trace_ctas *
- * EG_TRACE_POINTS * 8 bytes.  NULL turns tracing off. */
-#define EG_TRACE_POINTS 8
+ * trace[cta * EG_TRACE_POINTS + point] for ctas < trace_ctas:
+ *   0 CTA start, 1 setup done, 2 first TMA issued (after the wait on the
+ *   previous kernel), 3 first UMMA operands ready, 4 last UMMA committed,
+ *   5 first accumulator ready in the epilogue, 6 epilogue done, 7 CTA end,
+ *   8 first weight loads issued (before the wait on the previous kernel),
+ *   9 last load issued, and for the CTA's last work unit, seen by its first
+ *   epilogue thread: 10 accumulator final, 11 split-K partial stored or
+ *   sent, 12 arrival counted or partials received, 14 output stores (with
+ *   the last arriver's reduction) begin, 13 the last arriver's first chunk
+ *   reduced (tensor-memory accumulator path).  Point 15, and points a path
+ *   does not pass, keep the buffer's value.
+ * The buffer is caller-owned device memory of trace_ctas * EG_TRACE_POINTS
+ * * 8 bytes.  NULL turns tracing off. */
+#define EG_TRACE_POINTS 16
 EG_API eg_status eg_plan_set_trace(eg_plan* plan, uint64_t* trace, int32_t trace_ctas);
 
 /* One fused linear-layer call that allocates no device memory.  (The pages

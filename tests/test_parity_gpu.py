@@ -216,6 +216,59 @@ def test_block_fp8_wide_tiles(M, N, K, tuning):
     check_full(p, tuning)
 
 
+STAGED_CASES = [
+    # dtype, scale, M, N, K, tuning, epilogue
+    ("bf16", "none", 300, 520, 640, dict(tile_n=64, stages=4, split_k=1, swap_ab=0),
+     dict(act="gelu_tanh", bias=True, residual=True, residual_pre_act=True)),
+    ("bf16", "none", 520, 648, 512, dict(tile_n=256, stages=6, split_k=1, swap_ab=0, cta_pair=1),
+     dict(act="gelu_tanh", bias=True, residual=True, residual_pre_act=True)),
+    ("e4m3", "token_channel", 200, 456, 512, dict(tile_n=224, stages=4, split_k=1, swap_ab=0),
+     dict(act="silu", bias=True)),
+    ("e4m3", "token_channel", 150, 392, 1024, dict(tile_n=128, stages=4, split_k=2, swap_ab=0),
+     dict(act="silu", bias=True, residual=True)),
+    ("e4m3", "block", 300, 640, 1024, dict(tile_n=256, stages=3, split_k=1, swap_ab=0, stream_k=1),
+     dict(act="gelu_erf", bias=True, residual=True)),
+    ("int8", "token_channel", 130, 200, 640, dict(tile_n=64, stages=3, split_k=1, swap_ab=0),
+     dict(residual=True)),
+]
+
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype,scale,M,N,K,tuning,epi", STAGED_CASES)
+def test_staged_tma_stores_match_direct_stores(dtype, scale, M, N, K, tuning, epi, out, monkeypatch):
+    """Rows over M store Y through shared-memory boxes and TMA stores (the
+    boxes clip at M and N); the direct stores from registers
+    (EG_STAGED_STORE=0) give bit-identical outputs, and both meet the bound
+    against the oracle."""
+    p = inputs.make_problem(M, N, K, dtype, scale, seed=23, **epi)
+    p.out = out
+    y_staged, _ = run(p, tuning)
+    monkeypatch.setenv("EG_STAGED_STORE", "0")
+    y_direct, _ = run(p, tuning)
+    monkeypatch.delenv("EG_STAGED_STORE")
+    assert np.array_equal(bits(y_staged), bits(y_direct))
+    ref = oracle.linear(p)
+    if dtype == "int8" and out == "bf16":
+        assert ulp_dist(bits(y_staged), ref).max() <= 1
+    else:
+        assert_close_out(bits(y_staged), ref, out)
+
+
+def test_staged_stores_with_unaligned_output_rows_fall_back():
+    """Y rows that are not 16-byte aligned: the plan stores directly."""
+    p = inputs.make_problem(130, 203, 256, "bf16", act="relu", bias=False, seed=29)
+    plan = make_plan(p, dict(tile_n=64, stages=3, split_k=1, swap_ab=0))
+    d = to_device(p)
+    Yw = torch.full((p.M, 205), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    Y = Yw[:, :p.N]
+    plan.run(d["A"], d["W"], Y)
+    torch.cuda.synchronize()
+    assert plan.device_status() == eg.EG_OK
+    assert_close_rms(bits(Y.cpu()), oracle.linear(p))
+    assert (Yw[:, p.N:].view(torch.int16) == -1).all()
+    plan.close()
+
+
 def test_block_fp8_wide_tiles_debug_accumulators():
     p = inputs.make_problem(140, 384, 640, "e4m3", "block", seed=19)
     yacc, _ = run(p, dict(tile_n=256, stages=4, split_k=1, swap_ab=0), debug=True)

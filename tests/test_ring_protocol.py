@@ -145,12 +145,26 @@ def test_grouped_stage_release(S, CG):
         assert simulate(S, CG, T=61, seed=seed) is None
 
 
-@pytest.mark.parametrize("S", [2, 3, 4])
-def test_release_by_accumulator_commit(S):
-    """Promotion kernels: the stage of K block g is freed by block g's
-    accumulator commit (4 buffers, the epilogue draining them in order)."""
+@pytest.mark.parametrize("S,NB", [(2, 4), (3, 4), (4, 4), (2, 2)])
+def test_release_by_accumulator_commit(S, NB):
+    """Promotion kernels: the stage (or INT8 operand slot, three of them) of
+    K block g is freed by block g's accumulator commit (four buffers, or two
+    for 256-wide tiles, the epilogue draining them in order)."""
     for seed in range(40):
-        assert simulate(S, 1, T=53, acc_release=True, NB=4, seed=seed) is None
+        assert simulate(S, 1, T=53, acc_release=True, NB=NB, seed=seed) is None
+
+
+def test_release_by_accumulator_commit_needs_enough_buffers():
+    """A ring deeper than the accumulator buffers breaks the release by the
+    accumulator commit (the host allows it only up to the buffer count)."""
+    bad = 0
+    for seed in range(200):
+        try:
+            if simulate(4, 1, T=53, acc_release=True, NB=2, seed=seed) is not None:
+                bad += 1
+        except AssertionError:
+            bad += 1
+    assert bad > 0
 
 
 def test_per_stage_release_with_promotion():
