@@ -704,15 +704,30 @@ __device__ __forceinline__ void epilogue_chunk(const KParams& p, int row, int co
 // col0 + CPT - 1 of its row), CW columns at a time, with the activation a
 // compile-time choice made once for all of them (the chunk loop unrolls and
 // the accumulators stay in registers).
+// Chunk `idx` (CW values) of a thread's CPT accumulators, picked with
+// selects so that the accumulators stay in registers while the chunk loop
+// itself is not unrolled.
+template <int CW, int CPT>
+__device__ __forceinline__ void pick_chunk(const uint32_t (&acc)[CPT], int idx, uint32_t (&r)[CW]) {
+#pragma unroll
+  for (int j = 0; j < CW; ++j) r[j] = acc[j];
+#pragma unroll
+  for (int k = 1; k < CPT / CW; ++k)
+#pragma unroll
+    for (int j = 0; j < CW; ++j) r[j] = (idx == k) ? acc[k * CW + j] : r[j];
+}
+
+// The promoted store runs once per output tile, between two tiles' K loops,
+// so its code is usually not in the instruction cache when it starts: the
+// chunk loop is a runtime loop (one copy of the chunk code per activation).
 template <int IN, int SC, bool SWAP, int CW, int CPT, int ACT>
 __device__ __forceinline__ void promoted_store(const KParams& p, int row, int col0,
                                                const uint32_t (&acc)[CPT]) {
-#pragma unroll
-  for (int c = 0; c < CPT; c += CW) {
+#pragma unroll 1
+  for (int q = 0; q < CPT / CW; ++q) {
     uint32_t r[CW];
-#pragma unroll
-    for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
-    epilogue_chunk_a<IN, SC, SWAP, CW, ACT>(p, row, col0 + c, r);
+    pick_chunk<CW, CPT>(acc, q, r);
+    epilogue_chunk_a<IN, SC, SWAP, CW, ACT>(p, row, col0 + q * CW, r);
   }
 }
 
@@ -722,12 +737,11 @@ template <int IN, int SC, int CW, int CPT, int ACT>
 __device__ __forceinline__ void promoted_store_staged(const KParams& p, const CUtensorMap* tmY, int row,
                                                       int row_base, int col0, const uint32_t (&acc)[CPT],
                                                       uint8_t* boxes, uint32_t& nbox, int lane) {
-#pragma unroll
-  for (int c = 0; c < CPT; c += CW) {
+#pragma unroll 1
+  for (int q = 0; q < CPT / CW; ++q) {
     uint32_t r[CW];
-#pragma unroll
-    for (int j = 0; j < CW; ++j) r[j] = acc[c + j];
-    epilogue_chunk_staged<IN, SC, CW, ACT>(p, tmY, row, row_base, col0 + c, r,
+    pick_chunk<CW, CPT>(acc, q, r);
+    epilogue_chunk_staged<IN, SC, CW, ACT>(p, tmY, row, row_base, col0 + q * CW, r,
                                            boxes + (nbox & 1u) * stage_box_bytes<CW>(), lane);
     ++nbox;
   }
@@ -1066,11 +1080,12 @@ __device__ __forceinline__ bool split_arrive_last(const KParams& p, int tile, in
 // in contributor order 0..contrib-1, so the result is the same whichever CTA
 // arrives last.  G contributors' loads are issued per round, so the latency
 // is paid once per G contributors, not once per contributor.
-template <int IN, int BN, int NV>
+template <int IN, int BN, int NV, int GMAX = 8>
 __device__ __forceinline__ void reduce_partials(const KParams& p, int tile, int contrib,
                                                 int col_first, int lane_row, bool row_valid,
                                                 int cols_left, uint32_t (&acc)[NV]) {
-  constexpr int G = (32 / NV) < 1 ? 1 : ((32 / NV) > 8 ? 8 : (32 / NV));
+  constexpr int G0 = (32 / NV) < 1 ? 1 : ((32 / NV) > 8 ? 8 : (32 / NV));
+  constexpr int G = G0 > GMAX ? GMAX : G0;
   for (int s0 = 0; s0 < contrib; s0 += G) {
     uint32_t v[G][NV];
 #pragma unroll
@@ -1964,7 +1979,7 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             do_epi = split_arrive_last(p, w.tile, w.contrib, ept, C::kEpiThreads, last_flag);
             if (ept == 0) trace_point(p, TR_ARRIVED);
             if (do_epi) {
-              if constexpr (CPT > 64) {
+              if constexpr (C::kWidePromote) {
                 // 32 columns at a time, so the partials in flight stay small
 #pragma unroll
                 for (int c = 0; c < CPT; c += 32) {

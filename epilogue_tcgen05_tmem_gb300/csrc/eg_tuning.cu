@@ -17,7 +17,7 @@ namespace {
 // Rows written by the offline sweep (bench/sweep tool); empty until swept.
 const TuningRow kTable[] = {
 #include "eg_tuning_table.inc"
-    {-1, -1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
+    {-1, -1, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}};
 
 // decode buckets, then the mid-range (prefill ramp) buckets
 constexpr int kBuckets[] = {1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048};
@@ -89,17 +89,38 @@ bool tuning_default(const eg_problem& p, int sms, eg_tuning* out) {
   return true;
 }
 
-bool tuning_lookup(const eg_problem& p, int sms, eg_tuning* out) {
-  // the swept rows are for plain (ungated) layers
-  if (p.flags & EG_EPI_GATED) return tuning_default(p, sms, out);
-  const int b = bucket_of(p.M);
+int32_t epi_class_of(const eg_problem& p) {
+  if (p.flags & EG_EPI_GATED) return EPI_CLASS_GATED;
+  if (p.flags & EG_RUN_QUANT_A) return EPI_CLASS_QUANT;
+  return EPI_CLASS_PLAIN;
+}
+
+namespace {
+
+const TuningRow* find_row(const eg_problem& p, int bucket, int32_t epi) {
   for (const TuningRow& r : kTable) {
     if (r.dtype < 0) break;
-    if (r.dtype == p.dtype && r.scale == p.scale && r.N == p.N && r.K == p.K && r.m_max == b) {
-      *out = eg_tuning{r.tile_n, r.stages, r.split_k, r.swap_ab, r.stream_k, r.cluster_reduce,
-                       r.cta_pair};
-      return true;
-    }
+    if (r.dtype == p.dtype && r.scale == p.scale && r.N == p.N && r.K == p.K && r.m_max == bucket &&
+        r.epi == epi)
+      return &r;
+  }
+  return nullptr;
+}
+
+}  // namespace
+
+bool tuning_lookup(const eg_problem& p, int sms, eg_tuning* out) {
+  // rows of the problem's own epilogue class first; the quantisation
+  // prologue's GEMM is the plain layer's, so it falls back to the plain
+  // rows; a gated unit (twice the weights, two accumulators) to the rule
+  const int b = bucket_of(p.M);
+  const int32_t epi = epi_class_of(p);
+  const TuningRow* r = find_row(p, b, epi);
+  if (!r && epi == EPI_CLASS_QUANT) r = find_row(p, b, EPI_CLASS_PLAIN);
+  if (r) {
+    *out = eg_tuning{r->tile_n, r->stages, r->split_k, r->swap_ab, r->stream_k, r->cluster_reduce,
+                     r->cta_pair};
+    return true;
   }
   return tuning_default(p, sms, out);
 }

@@ -5,13 +5,22 @@
 
 namespace eg {
 
+// Epilogue classes the table keys its rows by: the plain fused layer (any
+// bias / residual / activation / output format), the gated unit (two weight
+// halves, two accumulators), and the layer behind the per-token
+// quantisation prologue (its GEMM runs as the prologue kernel's
+// programmatic dependent).
+enum : int32_t { EPI_CLASS_PLAIN = 0, EPI_CLASS_GATED = 1, EPI_CLASS_QUANT = 2 };
+
+int32_t epi_class_of(const eg_problem& p);
+
 // One row of the swept table.  m_max is the token bucket the row was tuned
 // at (1, 2, 4, 8, 16, 24, 32, 64, ..., 2048); rows with m_max == 0 cover
-// every M above the largest bucket.
+// every M above the largest bucket.  epi is the epilogue class.
 struct TuningRow {
   int32_t dtype, scale;
   int64_t N, K;
-  int32_t m_max;
+  int32_t m_max, epi;
   int32_t tile_n, stages, split_k, swap_ab, stream_k, cluster_reduce, cta_pair;
 };
 

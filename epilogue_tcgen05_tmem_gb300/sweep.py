@@ -1,12 +1,15 @@
 """Offline per-shape sweep of the fused kernel's tuning space.
 
 For one problem shape and each token bucket it times every valid
-(tile_n, stages, split_k, swap_ab) point under CUDA-graph replay, over
+(tile_n, stages, split_k, swap_ab, ...) point under CUDA-graph replay, over
 enough rotating weight copies that the weights stream from HBM, and keeps
 the fastest (ties within 1% go to the plain split over the balanced one, then the
 smaller split_k, then no swap, then fewer stages).  The rows it prints (or writes with --out) are the format of
 ``csrc/eg_tuning_table.inc``; the library consults that table before its
 default rule.
+
+Rows are keyed by the epilogue class too (plain, gated unit, behind the
+quantisation prologue: workloads fp8_swiglu, fp8_quant, int8_quant).
 
 This is the offline autotuning step of "Helion linear backend in vLLM"
 (sections "One kernel instead of three" and "How the autotuner searches":
@@ -105,11 +108,40 @@ def _midrange_candidates(p, swaps, max_bn, k_tiles):
                            cluster_reduce=0, cta_pair=1)
 
 
-def time_config(eg, torch, p, d, Ws, tuning, reps=3, calls=None):
+# Epilogue classes of the table rows (eg_tuning.h): plain, gated unit,
+# behind the per-token quantisation prologue.
+EPI_PLAIN, EPI_GATED, EPI_QUANT = 0, 1, 2
+
+# Sweepable workloads beyond inputs.workload(): the gated unit of the
+# FP8_Dynamic decode shape (W [2 x 12288, 4096]) and the FP8 / INT8 decode
+# layers behind the quantisation prologue (bf16 activations in).
+VARIANTS = {"fp8_swiglu": ("fp8_dynamic", EPI_GATED), "fp8_quant": ("fp8_dynamic", EPI_QUANT),
+            "int8_quant": ("w8a8_int8", EPI_QUANT)}
+
+GATED_TILES = {0: (64, 128), 1: (16, 32, 64)}  # gated kernels: tile_n per swap_ab
+
+
+def sweep_problem(workload, M):
+    """(problem, epilogue class) of a workload name at M tokens."""
+    from epilogue_tcgen05_tmem_gb300 import inputs
+    base, epi = VARIANTS.get(workload, (workload, EPI_PLAIN))
+    if epi == EPI_GATED:
+        p = inputs.make_gated_problem(M, 12288, 4096, "e4m3", "token_channel", act="silu",
+                                      outlier_frac=0.01)
+    else:
+        p = inputs.workload(base, M)
+    return p, epi
+
+
+def gated_ok(c):
+    return c["tile_n"] in GATED_TILES[c["swap_ab"]] and not c["cluster_reduce"] and not c["cta_pair"]
+
+
+def time_config(eg, torch, p, d, Ws, tuning, reps=3, calls=None, epi=EPI_PLAIN):
     try:
         plan = eg.Plan(p.M, p.N, p.K, p.dtype, p.scale, p.act, bias=p.bias is not None,
                        residual=p.residual is not None, residual_pre_act=p.residual_pre_act,
-                       pdl=True, tuning=tuning)
+                       pdl=True, tuning=tuning, gated=epi == EPI_GATED, quant_a=epi == EPI_QUANT)
     except eg.EgError:
         return None
     stream = torch.cuda.Stream()
@@ -160,11 +192,15 @@ def sweep(workload, tokens, swaps=(0, 1), verbose=True):
     eg.lib()
     rows = []
     for M in tokens:
-        p = inputs.workload(workload, M)
+        p, epi = sweep_problem(workload, M)
         A = torch.from_numpy(np.ascontiguousarray(p.A))
         W = torch.from_numpy(np.ascontiguousarray(p.W))
         if p.dtype == "bf16":
             A, W = A.view(torch.int16).view(torch.bfloat16), W.view(torch.int16).view(torch.bfloat16)
+        if epi == EPI_QUANT:
+            # the layer reads bf16 activations and quantises them itself
+            A = torch.from_numpy(inputs.activations_bf16(p.M, p.K, outlier_frac=0.01)).view(
+                torch.bfloat16)
         d = {"A": A.cuda(), "s_a": None, "s_w": None, "bias": None, "residual": None}
         if p.s_a is not None:
             d["s_a"] = torch.from_numpy(p.s_a).cuda()
@@ -179,12 +215,14 @@ def sweep(workload, tokens, swaps=(0, 1), verbose=True):
         Ws = [W0] + [W0.clone() for _ in range(nw - 1)]
         results = []
         for c in candidates(p, swaps):
-            t = time_config(eg, torch, p, d, Ws, c)
+            if epi == EPI_GATED and not gated_ok(c):
+                continue
+            t = time_config(eg, torch, p, d, Ws, c, epi=epi)
             if t is not None:
                 results.append((c, t))
         c, t = pick(results)
         bucket = M if M <= 2048 else 0
-        row = (eg.DTYPES[p.dtype], eg.SCALES[p.scale], p.N, p.K, bucket, c["tile_n"],
+        row = (eg.DTYPES[p.dtype], eg.SCALES[p.scale], p.N, p.K, bucket, epi, c["tile_n"],
                c["stages"], c["split_k"], c["swap_ab"], c["stream_k"], c["cluster_reduce"],
                c["cta_pair"])
         rows.append(row)
@@ -207,7 +245,7 @@ def format_rows(rows, comment=""):
     if comment:
         out.append(f"// {comment}")
     for r in rows:
-        out.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % r)
+        out.append("    {%d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d, %d}," % r)
     return "\n".join(out) + "\n"
 
 

@@ -106,9 +106,10 @@ def test_binding_structs_match_header(name, cls):
 
 
 def test_tuning_table_rows_are_valid():
-    """Every swept row has the 12 fields of the table, uses the cluster
-    reduction only with a split of 2, 4 or 8 and without balanced split-K,
-    and CTA pairs only unsplit, without swap-AB, with tiles of 128 or 256."""
+    """Every swept row has the 13 fields of the table, an epilogue class of
+    0, 1 or 2, uses the cluster reduction only with a split of 2, 4 or 8 and
+    without balanced split-K, CTA pairs only unsplit, without swap-AB, with
+    tiles of 128 or 256, and gated rows only the gated kernels' tiles."""
     import os
     import re
     path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
@@ -117,8 +118,11 @@ def test_tuning_table_rows_are_valid():
             for m in re.findall(r"^\s*\{([-\d, ]+)\},", open(path).read(), flags=re.M)]
     assert rows
     for r in rows:
-        assert len(r) == 12, r
-        dtype, scale, N, K, bucket, tn, stages, split, swap, sk, cl, pair = r
+        assert len(r) == 13, r
+        dtype, scale, N, K, bucket, epi, tn, stages, split, swap, sk, cl, pair = r
+        assert epi in (0, 1, 2), r
+        if epi == 1:
+            assert tn in ((16, 32, 64) if swap else (64, 128)) and cl == 0 and pair == 0, r
         assert bucket in (0, 1, 2, 4, 8, 16, 24, 32, 64, 128, 256, 512, 1024, 2048)
         assert tn in (16, 32, 64, 128, 192, 224, 256)
         if tn in (192, 224):
@@ -142,8 +146,18 @@ def test_sweep_candidates_and_rows():
     assert all(set(c) == keys for c in cands)
     cl = [c for c in cands if c["cluster_reduce"]]
     assert cl and all(c["split_k"] in (2, 4, 8) and c["stream_k"] == 0 for c in cl)
-    text = sweep.format_rows([(1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1, 0)])
-    assert text.strip() == "{1, 1, 1024, 4096, 16, 16, 4, 4, 1, 0, 1, 0},"
+    text = sweep.format_rows([(1, 1, 1024, 4096, 16, 0, 16, 4, 4, 1, 0, 1, 0)])
+    assert text.strip() == "{1, 1, 1024, 4096, 16, 0, 16, 4, 4, 1, 0, 1, 0},"
+
+
+def test_sweep_gated_candidates_use_gated_kernels():
+    from epilogue_tcgen05_tmem_gb300 import sweep
+    p, epi = sweep.sweep_problem("fp8_swiglu", 8)
+    assert epi == sweep.EPI_GATED and p.meta.get("gated") and p.W.shape[0] == 2 * p.N
+    cands = [c for c in sweep.candidates(p, swaps=(0, 1)) if sweep.gated_ok(c)]
+    assert cands and all(c["tile_n"] in sweep.GATED_TILES[c["swap_ab"]] for c in cands)
+    q, e = sweep.sweep_problem("int8_quant", 4)
+    assert e == sweep.EPI_QUANT and q.dtype == "int8"
 
 
 def test_sweep_pair_candidates():

@@ -312,6 +312,36 @@ def test_graph_mode_matches_direct_and_recaptures():
     plan.close()
 
 
+def _table_rows():
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "epilogue_tcgen05_tmem_gb300", "csrc", "eg_tuning_table.inc")
+    return [tuple(int(x) for x in m.split(","))
+            for m in re.findall(r"^\s*\{([-\d, ]+)\},", open(path).read(), flags=re.M)]
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_tuning_lookup_by_epilogue_class(M):
+    """Plans take the table row of their own epilogue class: the plain
+    FP8_Dynamic decode layer, its gated unit (W [2N, K]) and the layer behind
+    the quantisation prologue each get their own swept row."""
+    rows = _table_rows()
+    keys = ("tile_n", "stages", "split_k", "swap_ab", "stream_k", "cluster_reduce", "cta_pair")
+
+    def want(epi):
+        for r in rows:
+            if r[:6] == (1, 1, 12288, 4096, M, epi):
+                return dict(zip(keys, r[6:]))
+        return None
+    for epi, kw in ((0, {}), (1, dict(gated=True)), (2, dict(quant_a=True))):
+        w = want(epi)
+        assert w is not None, epi
+        plan = eg.Plan(M, 12288, 4096, "e4m3", "token_channel", "silu", **kw)
+        assert plan.tuning == w, (epi, plan.tuning, w)
+        plan.close()
+
+
 def test_graph_cache_evicts_and_recaptures():
     """More distinct argument sets than the plan keeps graphs for: every
     call is still right, also when an evicted set comes back."""
