@@ -1858,28 +1858,23 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             tc_fence_after();
             if (blk == 0 && ept == 0) trace_point(p, TR_FIRST_ACC);
             const uint32_t tb = t_lane + static_cast<uint32_t>(b * BN);
-            // 16-column pieces, the next piece's load in flight while the
-            // current one is added
-            uint32_t rp[2][16];
-            tmem_ld16(tb, rp[0]);
-            tmem_ld_wait();
-            reg_fence<16>(rp[0]);
+            // two halves of 64 columns: each half's four loads in flight
+            // together, one wait, then its 64 FMAs (two waits per K block)
+            uint32_t rh[64];
 #pragma unroll
-            for (int q = 0; q < CPT / 16; ++q) {
-              if (q + 1 < CPT / 16) {
-                tmem_ld16(tb + static_cast<uint32_t>(16 * (q + 1)), rp[(q + 1) & 1]);
-              } else {
+            for (int h = 0; h < CPT / 64; ++h) {
+              tmem_ld32p(tb + static_cast<uint32_t>(64 * h), rh);
+              tmem_ld32p(tb + static_cast<uint32_t>(64 * h + 32), rh + 32);
+              tmem_ld_wait();
+              reg_fence<64>(rh);
+              if (h + 1 == CPT / 64) {
                 tc_fence_before();
                 mbar_arrive(&tempty[b]);  // the buffer is free once all of it is in registers
               }
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                acc[16 * q + j] = __float_as_uint(__fmaf_rn(srow, __uint_as_float(rp[q & 1][j]),
-                                                            __uint_as_float(acc[16 * q + j])));
-              if (q + 1 < CPT / 16) {
-                tmem_ld_wait();
-                reg_fence<16>(rp[(q + 1) & 1]);
-              }
+              for (int j = 0; j < 64; ++j)
+                acc[64 * h + j] = __float_as_uint(__fmaf_rn(srow, __uint_as_float(rh[j]),
+                                                            __uint_as_float(acc[64 * h + j])));
             }
           }
         } else
