@@ -203,11 +203,13 @@ eg_status validate_problem(const eg_problem* p) {
 
 bool lookup_kernel(const eg_problem& p, int swap, int bn, int pair, eg::KernelEntry* ke) {
   if (pair) {
-    // CTA pairs: plain layers without swap-AB, bf16 or FP8 per-token/channel
+    // CTA pairs: plain layers without swap-AB, bf16, FP8 per-token/channel
+    // or FP8 block scales
     if (swap || (p.flags & EG_EPI_GATED)) return false;
     if (p.dtype == EG_IN_BF16) return eg::lookup_bf16_pair(bn, ke);
     if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_TOKEN_CHANNEL)
       return eg::lookup_e4m3_tc_pair(bn, ke);
+    if (p.dtype == EG_IN_E4M3 && p.scale == EG_SCALE_BLOCK) return eg::lookup_e4m3_block_pair(bn, ke);
     return false;
   }
   if (p.flags & EG_EPI_GATED) {

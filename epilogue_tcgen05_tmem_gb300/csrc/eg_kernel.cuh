@@ -215,7 +215,7 @@ struct Cfg {
       (IN == IN_BF16) ? idesc_f32acc(1, 1, kUmmaM, BN)
                       : idesc_f32acc(0, 0, kUmmaM, BN);  // e4m3 (f8f6f4) or f16 (converted int8)
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
-  static_assert(!kPromote || BN <= 128 || (kWidePromote && BN == 256 && !SWAP && !G && !PR),
+  static_assert(!kPromote || BN <= 128 || (kWidePromote && BN == 256 && !SWAP && !G),
                 "wide promotion: block scales, tile_n 256, rows over M");
   static_assert(!kWidePromote || kColsPerThread == 128, "128 running sums per epilogue thread");
   static_assert(!kWidePromote || 128 * kRegsLow + kEpiThreads * kRegsHigh <= kThreads * kMaxRegs,
@@ -224,8 +224,9 @@ struct Cfg {
   static_assert(!kConvert || kOpSlots <= kAccBufs,
                 "an operand slot is released by the accumulator commit of its K tile");
   static_assert(!G || !kPromote, "gated units use the tensor-memory accumulator path");
-  static_assert(!PR || (!SWAP && !kPromote && !G && (BN == 128 || BN == 256)),
-                "CTA pairs: tiles of 256 x 128 or 256 x 256, per-token/channel or bf16");
+  static_assert(!PR || (!SWAP && !G && (BN == 128 || BN == 256) && (!kPromote || kWidePromote)),
+                "CTA pairs: tiles of 256 x 128 or 256 x 256 (per-token/channel or bf16), or "
+                "256 x 256 with block-scale promotion");
 };
 
 template <int IN, int SC, bool SWAP, int BN, bool G = false, bool PR = false>
@@ -583,6 +584,77 @@ __device__ __forceinline__ void epi_row_values(const KParams& p, int m, int col0
   }
 }
 
+// The same for 16-bit outputs (bf16 or fp16), packed two per word: the float
+// path forms every value of the chunk first and then narrows pairs with one
+// conversion each (the format chosen once per chunk, not per element); the
+// rounding of each value is the same as the single-element narrowing.
+template <int IN, int SC, int CW, int ACT>
+__device__ __forceinline__ void epi_row_words(const KParams& p, int m, int col0,
+                                              const uint32_t (&vals)[CW], uint32_t (&wd)[CW / 2]) {
+  if constexpr (IN == IN_INT8) {
+    uint16_t o[CW];
+    epi_row_values<IN, SC, CW, ACT>(p, m, col0, vals, o);
+#pragma unroll
+    for (int j = 0; j < CW / 2; ++j)
+      wd[j] = static_cast<uint32_t>(o[2 * j]) | (static_cast<uint32_t>(o[2 * j + 1]) << 16);
+  } else {
+    const uint32_t flags = p.flags;
+    const bool has_bias = (flags & F_BIAS) != 0;
+    const bool has_res = (flags & (F_RES | F_RES_PRE)) != 0;
+    const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
+    const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
+    float v[CW];
+    if (p.vec_ok && col0 + CW <= p.N) {
+#pragma unroll
+      for (int g = 0; g < CW / 8; ++g) {
+        uint4 bv = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
+        if (has_bias) bv = __ldg(reinterpret_cast<const uint4*>(p.bias + col0) + g);
+        if (has_res) rv = __ldg(reinterpret_cast<const uint4*>(rrow + col0) + g);
+        float4 sw0 = make_float4(1, 1, 1, 1), sw1 = make_float4(1, 1, 1, 1);
+        if (SC == SC_TC) {
+          sw0 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g);
+          sw1 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g + 1);
+        }
+        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+        const float sws[8] = {sw0.x, sw0.y, sw0.z, sw0.w, sw1.x, sw1.y, sw1.z, sw1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float b = bf16_to_f(static_cast<uint16_t>(bw[e >> 1] >> (16 * (e & 1))));
+          const float r = bf16_to_f(static_cast<uint16_t>(rw[e >> 1] >> (16 * (e & 1))));
+          const float sc = (SC == SC_TC) ? sa * sws[e] : 1.0f;
+          v[g * 8 + e] = epi_value<ACT>(__uint_as_float(vals[g * 8 + e]), sc, b, r, flags);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < CW; ++j) {
+        const int n = col0 + j;
+        v[j] = 0.0f;
+        if (n < p.N) {
+          const float b = has_bias ? __bfloat162float(p.bias[n]) : 0.0f;
+          const float r = has_res ? __bfloat162float(rrow[n]) : 0.0f;
+          const float sw = (SC == SC_TC) ? __ldg(p.s_w + n) : 1.0f;
+          v[j] = epi_value<ACT>(__uint_as_float(vals[j]), (SC == SC_TC) ? sa * sw : 1.0f, b, r, flags);
+        }
+      }
+    }
+    if (p.out == OUT_F16) {
+#pragma unroll
+      for (int j = 0; j < CW / 2; ++j) {
+        const __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+        wd[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < CW / 2; ++j) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        wd[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+  }
+}
+
 // Apply the epilogue to CW consecutive accumulator columns of one TMEM lane
 // (= one UMMA row) and store them.  `vals` holds fp32 bits, or int32 for
 // INT8.  row = tile row index + lane row; c0 = first column of the chunk.
@@ -651,19 +723,16 @@ __device__ __forceinline__ void epilogue_chunk_a(const KParams& p, int row, int 
 template <int CW>
 __host__ __device__ constexpr uint32_t stage_box_bytes() { return 32u * CW * 2u; }
 
-// Write row r's CW output bits (2 bytes each) into the swizzled box.
+// Write row r's CW outputs (2 bytes each, packed two per word) into the
+// swizzled box.
 template <int CW>
-__device__ __forceinline__ void stage_row(uint8_t* box, int r, const uint16_t (&o)[CW]) {
+__device__ __forceinline__ void stage_row(uint8_t* box, int r, const uint32_t (&wd)[CW / 2]) {
   static_assert(CW == 32 || CW == 16, "64- or 32-byte box rows");
 #pragma unroll
   for (int c = 0; c < CW / 8; ++c) {
     const int pc = (CW == 32) ? (c ^ ((r >> 1) & 3)) : (c ^ ((r >> 2) & 1));
-    uint4 v;
-    v.x = static_cast<uint32_t>(o[8 * c + 0]) | (static_cast<uint32_t>(o[8 * c + 1]) << 16);
-    v.y = static_cast<uint32_t>(o[8 * c + 2]) | (static_cast<uint32_t>(o[8 * c + 3]) << 16);
-    v.z = static_cast<uint32_t>(o[8 * c + 4]) | (static_cast<uint32_t>(o[8 * c + 5]) << 16);
-    v.w = static_cast<uint32_t>(o[8 * c + 6]) | (static_cast<uint32_t>(o[8 * c + 7]) << 16);
-    *reinterpret_cast<uint4*>(box + r * (CW * 2) + pc * 16) = v;
+    *reinterpret_cast<uint4*>(box + r * (CW * 2) + pc * 16) =
+        make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]);
   }
 }
 
@@ -678,14 +747,14 @@ __device__ __forceinline__ void epilogue_chunk_staged(const KParams& p, const CU
                                                       int lane) {
   if (lane == 0) bulk_wait_group_read<1>();
   __syncwarp();
-  uint16_t out[CW];
+  uint32_t wd[CW / 2];
   if (row < p.M) {
-    epi_row_values<IN, SC, CW, ACT>(p, row, col0, vals, out);
+    epi_row_words<IN, SC, CW, ACT>(p, row, col0, vals, wd);
   } else {
 #pragma unroll
-    for (int j = 0; j < CW; ++j) out[j] = 0;
+    for (int j = 0; j < CW / 2; ++j) wd[j] = 0u;
   }
-  stage_row<CW>(box, lane, out);
+  stage_row<CW>(box, lane, wd);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
@@ -1416,8 +1485,9 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
     }
     for (int b = 0; b < NB; ++b) {
       mbar_init(&tfull[b], 1);
-      // per epilogue thread, or (PR) one arrival per CTA of the pair
-      mbar_init(&tempty[b], PR ? 2 : C::kEpiThreads);
+      // per epilogue thread; CTA pairs: one arrival per CTA of the pair per
+      // unit, or (promotion, per K block) one per epilogue warp of both CTAs
+      mbar_init(&tempty[b], PR ? (C::kPromote ? 2 * C::kEpiWarps : 2) : C::kEpiThreads);
     }
     mbar_init(mma_done, 1);
     mbar_init(red_full, 1);
@@ -1627,7 +1697,8 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           const uint32_t ph = rm.ph;
           const int b = blk % NB;
           if (C::kPromote) {
-            if (!mbar_wait(&tempty[b], ((blk / NB) & 1u) ^ 1u, lim)) {
+            const uint32_t tph = ((blk / NB) & 1u) ^ 1u;
+            if (!(PR ? mbar_wait_cluster(&tempty[b], tph, lim) : mbar_wait(&tempty[b], tph, lim))) {
               record_status(p.status, ST_TIMEOUT_MMA);
               ok = false;
               break;
@@ -1703,7 +1774,10 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
               umma_commit(eb);
           }
           if (C::kPromote) {
-            umma_commit(&tfull[b]);
+            if constexpr (PR)
+              umma_commit_pair(&tfull[b]);  // both CTAs' accumulators of the K block
+            else
+              umma_commit(&tfull[b]);
             ++blk;
           }
         }
@@ -1868,8 +1942,15 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
               tmem_ld_wait();
               reg_fence<64>(rh);
               if (h + 1 == CPT / 64) {
+                // the buffer is free once all of it is in registers (CTA
+                // pairs: each warp's arrival on the even CTA's barrier)
                 tc_fence_before();
-                mbar_arrive(&tempty[b]);  // the buffer is free once all of it is in registers
+                if constexpr (PR) {
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&tempty[b]), 0));
+                } else {
+                  mbar_arrive(&tempty[b]);
+                }
               }
 #pragma unroll
               for (int j = 0; j < 64; ++j)

@@ -32,9 +32,11 @@ EG_DECLARE_LOOKUP(lookup_int8_tc)
 EG_DECLARE_LOOKUP(lookup_bf16_gated)
 EG_DECLARE_LOOKUP(lookup_e4m3_tc_gated)
 #undef EG_DECLARE_LOOKUP
-// CTA-pair kernels (no swap-AB): bf16 and FP8 per-token/channel.
+// CTA-pair kernels (no swap-AB): bf16 and FP8 per-token/channel, and FP8
+// block scales (256-wide promotion tiles).
 bool lookup_bf16_pair(int bn, KernelEntry* out);
 bool lookup_e4m3_tc_pair(int bn, KernelEntry* out);
+bool lookup_e4m3_block_pair(int bn, KernelEntry* out);
 
 }  // namespace eg
 

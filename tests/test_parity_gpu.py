@@ -197,10 +197,21 @@ def test_block_fp8_full_size_sampled(M):
     _sampled(p, y, npts=1500 if M > 32 else 600)
 
 
+def test_block_fp8_m2048_cta_pairs_sampled():
+    """The Block_FP8 layer at 2048 tokens on 256 x 256 CTA-pair tiles,
+    sampled outputs against the oracle."""
+    p = inputs.workload("block_fp8", 2048)
+    y, _ = run(p, dict(tile_n=256, stages=3, split_k=1, swap_ab=0, cta_pair=1))
+    _sampled(p, y, npts=1500, seed=3)
+
+
 WIDE_BLOCK = [
     dict(tile_n=256, stages=4, split_k=1, swap_ab=0),
     dict(tile_n=256, stages=3, split_k=1, swap_ab=0, stream_k=1),
     dict(tile_n=256, stages=2, split_k=2, swap_ab=0),          # accumulator-commit release
+    # CTA pairs: 256 x 256 tiles, each CTA promoting its 128 rows
+    dict(tile_n=256, stages=4, split_k=1, swap_ab=0, cta_pair=1),
+    dict(tile_n=256, stages=2, split_k=1, swap_ab=0, cta_pair=1),  # accumulator-commit release
 ]
 
 
@@ -210,7 +221,8 @@ def test_block_fp8_wide_tiles(M, N, K, tuning):
     """256-wide promotion tiles (two weight blocks per tile, 128 running sums
     per epilogue thread, scales read per K block into registers): ragged M,
     N not a multiple of 256 (the second weight block of the last tile lies
-    past N), several K splits."""
+    past N), several K splits, and CTA pairs (M = 17: the odd CTA's rows all
+    lie past M; M = 130: two of them are valid)."""
     p = inputs.make_problem(M, N, K, "e4m3", "block", act="gelu_erf", bias=True,
                             residual=True, seed=17)
     check_full(p, tuning)
@@ -228,6 +240,8 @@ STAGED_CASES = [
      dict(act="silu", bias=True, residual=True)),
     ("e4m3", "block", 300, 640, 1024, dict(tile_n=256, stages=3, split_k=1, swap_ab=0, stream_k=1),
      dict(act="gelu_erf", bias=True, residual=True)),
+    ("e4m3", "block", 600, 896, 768, dict(tile_n=256, stages=3, split_k=1, swap_ab=0, cta_pair=1),
+     dict(act="silu", bias=True, residual=True)),
     ("int8", "token_channel", 130, 200, 640, dict(tile_n=64, stages=3, split_k=1, swap_ab=0),
      dict(residual=True)),
 ]
@@ -269,9 +283,10 @@ def test_staged_stores_with_unaligned_output_rows_fall_back():
     plan.close()
 
 
-def test_block_fp8_wide_tiles_debug_accumulators():
-    p = inputs.make_problem(140, 384, 640, "e4m3", "block", seed=19)
-    yacc, _ = run(p, dict(tile_n=256, stages=4, split_k=1, swap_ab=0), debug=True)
+@pytest.mark.parametrize("pair", [0, 1])
+def test_block_fp8_wide_tiles_debug_accumulators(pair):
+    p = inputs.make_problem(140 + 200 * pair, 384, 640, "e4m3", "block", seed=19)
+    yacc, _ = run(p, dict(tile_n=256, stages=4, split_k=1, swap_ab=0, cta_pair=pair), debug=True)
     _, acc, _ = oracle.linear(p, want_acc=True)
     rms = float(np.sqrt(np.mean(acc ** 2)))
     assert float(np.max(np.abs(yacc.numpy().astype(np.float64) - acc))) <= 1e-4 * rms
@@ -812,10 +827,13 @@ def test_cta_pair_unsupported_tunings(t):
         make_plan(p, t)
 
 
-def test_cta_pair_rejects_block_scales():
+def test_cta_pair_block_scales_need_wide_tiles():
+    """Block-scale pairs exist only for 256-wide promotion tiles."""
     p = inputs.make_problem(256, 512, 512, "e4m3", "block", seed=1)
     with pytest.raises(eg.EgError):
         make_plan(p, dict(tile_n=128, stages=3, split_k=1, swap_ab=0, cta_pair=1))
+    with pytest.raises(eg.EgError):
+        make_plan(p, dict(tile_n=256, stages=3, split_k=2, swap_ab=0, cta_pair=1))
 
 
 @pytest.mark.parametrize("dtype,scale", [("bf16", "none"), ("e4m3", "token_channel")])
