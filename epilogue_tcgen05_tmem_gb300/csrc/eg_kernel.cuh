@@ -149,8 +149,10 @@ struct Cfg {
   // transform of K tile g waits for the UMMAs of tile g - kOpSlots, so
   // three slots keep two tiles of slack between the transform warps and the
   // UMMA issuer (at most the accumulator buffers, for the release by the
-  // accumulator commit; 64 + 64 x 3 tensor-memory columns at tile_n 16)
-  static constexpr int kOpSlots = kConvert ? 3 : 2;
+  // accumulator commit; 64 + 64 x 3 tensor-memory columns at tile_n 16).
+  // Two at tile_n 32, so that 4 x 32 + 2 x 64 columns leave room for a
+  // second CTA on the SM.
+  static constexpr int kOpSlots = kConvert ? (BN == 32 ? 2 : 3) : 2;
   static constexpr uint32_t kOpBytes = kConvert ? kOpSlots * kQBytes : 0u;
   static constexpr uint32_t kTxBytes =  // bytes one stage's TMA delivers (PR: to both CTAs)
       PR ? 2u * (128u + BN / 2) * 128u
@@ -184,7 +186,7 @@ struct Cfg {
   // CTAs per SM for decode tiles.
   static constexpr int kMinBlocks =
       G ? (BN <= 32 ? 2 : 1)
-        : kConvert ? (BN <= 16 ? 2 : 1)
+        : kConvert ? (BN <= 32 ? 2 : 1)
                    : ((kPromote && BN >= 64) || BN >= 128) ? 1 : (BN <= 32 ? 3 : 2);
   // Register cap per thread for that residency.  The SM's 64K registers are
   // split over its 4 sub-partitions (16K each) and warps are spread over
