@@ -16,6 +16,7 @@
 #include "../../include/eg.h"
 #include "eg_kernel.cuh"
 #include "eg_registry.h"
+#include "eg_gated.h"
 #include "eg_quant.h"
 #include "eg_tuning.h"
 
@@ -137,6 +138,13 @@ struct eg_plan {
   std::vector<GraphEntry> graphs;
   cudaStream_t cap_stream = nullptr;
   int last_launches = 0;
+  // Gated units of INT8 and Block_FP8 inputs run in two kernels: the fused
+  // kernel's accumulator output over all 2N weight rows into gacc ([M][2N]
+  // words), then the combine kernel (act(gate) * up and the epilogue).  prob
+  // is then that accumulator GEMM and `user` the caller's problem.
+  bool two_pass_gated = false;
+  eg_problem user{};
+  uint32_t* gacc = nullptr;
 };
 
 namespace {
@@ -179,10 +187,10 @@ eg_status validate_problem(const eg_problem* p) {
   if (outs & (outs - 1))
     return fail(EG_ERR_INVALID_ARG, "EG_OUT_F16, EG_OUT_E4M3 and EG_OUT_DEBUG_ACCUM exclude each other");
   if (p->flags & EG_EPI_GATED) {
-    const bool ok_in = p->scale == EG_SCALE_NONE ||
-                       (p->dtype == EG_IN_E4M3 && p->scale == EG_SCALE_TOKEN_CHANNEL);
-    if (!ok_in)
-      return fail(EG_ERR_UNSUPPORTED, "gated units take bf16 or E4M3 per-token/per-channel inputs");
+    // block scales: the up half starts on a 128-row weight block
+    if (p->scale == EG_SCALE_BLOCK && p->N % 128)
+      return fail(EG_ERR_UNSUPPORTED, "gated units with block scales need N %% 128 == 0 (N=%lld)",
+                  (long long)p->N);
     if (p->flags & (EG_EPI_RESIDUAL_PRE_ACT | EG_OUT_DEBUG_ACCUM))
       return fail(EG_ERR_INVALID_ARG,
                   "EG_EPI_GATED excludes EG_EPI_RESIDUAL_PRE_ACT and EG_OUT_DEBUG_ACCUM");
@@ -457,9 +465,8 @@ bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
   return a0 < b0 + bn && b0 < a0 + an;
 }
 
-eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
+eg_status validate_args_for(const eg_problem& p, const eg_args* a, bool debug_out) {
   if (!a) return fail(EG_ERR_INVALID_ARG, "args is NULL");
-  const eg_problem& p = pl->prob;
   if (p.M == 0 || p.N == 0) return EG_OK;
   const int eb = elt_bytes(p.dtype);
   if (!a->Y) return fail(EG_ERR_INVALID_ARG, "Y is NULL");
@@ -508,6 +515,10 @@ eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
        overlaps(a->Y, ybytes, a->residual, size_t(p.M - 1) * a->ldr * 2 + size_t(p.N) * 2)))
     return fail(EG_ERR_INVALID_ARG, "Y must not alias A, W or the residual");
   return EG_OK;
+}
+
+eg_status validate_args(const eg_plan* pl, const eg_args* a, bool debug_out) {
+  return validate_args_for(pl->prob, a, debug_out);
 }
 
 eg_status ensure_maps(eg_plan* pl, const eg_args* a) {
@@ -794,7 +805,17 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
   *out = nullptr;
   eg_status s = validate_problem(problem);
   if (s != EG_OK) return s;
-  const eg_problem& p = *problem;
+  // INT8 and Block_FP8 gated units: the plan's GEMM is the accumulator
+  // output over all 2N weight rows; the combine kernel does the rest
+  const bool two_pass = (problem->flags & EG_EPI_GATED) &&
+                        (problem->dtype == EG_IN_INT8 || problem->scale == EG_SCALE_BLOCK);
+  eg_problem inner = *problem;
+  if (two_pass) {
+    inner.N = 2 * problem->N;
+    inner.act = EG_ACT_NONE;
+    inner.flags = (problem->flags & (EG_RUN_PDL | EG_RUN_QUANT_A)) | EG_OUT_DEBUG_ACCUM;
+  }
+  const eg_problem& p = inner;
 
   // device checks come after the argument checks, so invalid problems are
   // rejected without touching the GPU
@@ -808,9 +829,17 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
                 major, minor);
 
   eg_tuning t{};
+  // a two-kernel gated unit's GEMM takes the rows of the plain layer of the
+  // same K and per-half N (the weight stream per output is twice as long,
+  // the shape of the work per tile is the same)
+  eg_problem key = p;
+  if (two_pass) {
+    key = *problem;
+    key.flags &= ~static_cast<uint32_t>(EG_EPI_GATED);
+  }
   if (tuning) {
     t = *tuning;
-  } else if (!eg::tuning_lookup(p, sm_count_of(dev), &t)) {
+  } else if (!eg::tuning_lookup(key, sm_count_of(dev), &t)) {
     return fail(EG_ERR_NOT_TUNED, "no tuning entry or default for this problem");
   }
   eg::KernelEntry ke;
@@ -878,13 +907,18 @@ eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning, eg_
       (e = cudaMemset(pl->status, 0, sizeof(int))) != cudaSuccess ||
       (e = cudaDeviceSynchronize()) != cudaSuccess)
     return cleanup(cuda_fail(e, "zeroing plan counters"));
+  pl->two_pass_gated = two_pass;
+  pl->user = *problem;
+  if (two_pass && p.M > 0 && p.N > 0 &&
+      (e = cudaMalloc(reinterpret_cast<void**>(&pl->gacc), size_t(p.M) * size_t(p.N) * 4u)) != cudaSuccess)
+    return cleanup(cuda_fail(e, "allocating the gated unit's accumulators"));
   *out = pl;
   return EG_OK;
 }
 
 eg_status eg_plan_workspace_bytes(const eg_plan* plan, size_t* out) {
   if (!plan || !out) return fail(EG_ERR_INVALID_ARG, "NULL argument");
-  *out = plan->ws_bytes;
+  *out = plan->ws_bytes + (plan->gacc ? size_t(plan->prob.M) * size_t(plan->prob.N) * 4u : 0u);
   return EG_OK;
 }
 
@@ -928,7 +962,7 @@ eg_status eg_plan_set_test_stall(eg_plan* plan, uint64_t wait_limit_ns, int32_t 
   return EG_OK;
 }
 
-static eg_status run_direct(eg_plan* pl, const eg_args* a, cudaStream_t st) {
+static eg_status run_gemm(eg_plan* pl, const eg_args* a, cudaStream_t st) {
   const eg_problem& p = pl->prob;
   eg_args q;
   if (p.flags & EG_RUN_QUANT_A) {
@@ -953,15 +987,43 @@ static eg_status run_direct(eg_plan* pl, const eg_args* a, cudaStream_t st) {
   return launch_fused(pl, kp, st);
 }
 
+// INT8 / Block_FP8 gated unit: the accumulators of the 2N weight rows, then
+// the combine kernel (a programmatic dependent of the GEMM with EG_RUN_PDL).
+static eg_status run_two_pass_gated(eg_plan* pl, const eg_args* a, cudaStream_t st) {
+  const eg_problem& u = pl->user;
+  eg_args q = *a;
+  q.Y = pl->gacc;
+  q.ldy = 2 * u.N;
+  q.bias = nullptr;
+  q.residual = nullptr;
+  q.ldr = 0;
+  q.s_y = nullptr;
+  eg_status s = run_gemm(pl, &q, st);
+  if (s != EG_OK) return s;
+  const uint32_t fl = ((u.flags & EG_EPI_BIAS) ? uint32_t(eg::F_BIAS) : 0u) |
+                      ((u.flags & EG_EPI_RESIDUAL) ? uint32_t(eg::F_RES) : 0u);
+  const int out = (u.flags & EG_OUT_F16) ? eg::OUT_F16 : (u.flags & EG_OUT_E4M3) ? eg::OUT_E4M3 : eg::OUT_BF16;
+  const float* s_a = (u.flags & EG_RUN_QUANT_A) ? pl->qs : a->s_a;
+  EG_CUDA(eg::launch_gated_combine(pl->gacc, u.M, u.N, u.dtype == EG_IN_INT8, s_a, a->s_w, a->bias,
+                                   a->residual, a->ldr, a->Y, a->ldy, u.act, fl, out, a->s_y, st,
+                                   (u.flags & EG_RUN_PDL) != 0),
+          "launching the gated combine kernel");
+  return EG_OK;
+}
+
+static eg_status run_direct(eg_plan* pl, const eg_args* a, cudaStream_t st) {
+  return pl->two_pass_gated ? run_two_pass_gated(pl, a, st) : run_gemm(pl, a, st);
+}
+
 eg_status eg_plan_run(eg_plan* plan, const eg_args* args, void* stream) {
   if (!plan) return fail(EG_ERR_INVALID_ARG, "plan is NULL");
-  const eg_problem& p = plan->prob;
-  eg_status s = validate_args(plan, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0);
+  const eg_problem& p = plan->two_pass_gated ? plan->user : plan->prob;
+  eg_status s = validate_args_for(p, args, (p.flags & EG_OUT_DEBUG_ACCUM) != 0);
   if (s != EG_OK) return s;
   plan->last_launches = 0;
   if (p.M == 0 || p.N == 0) return EG_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int launches = (p.flags & EG_RUN_QUANT_A) ? 2 : 1;
+  const int launches = ((p.flags & EG_RUN_QUANT_A) ? 2 : 1) + (plan->two_pass_gated ? 1 : 0);
   if (!(p.flags & EG_RUN_GRAPH)) {
     if ((s = run_direct(plan, args, st)) != EG_OK) return s;
     plan->last_launches = launches;
@@ -1014,7 +1076,7 @@ eg_status eg_plan_run_unfused(eg_plan* plan, const eg_args* args, void* T1, void
     return fail(EG_ERR_UNSUPPORTED, "the unfused path takes quantised A (no EG_RUN_QUANT_A)");
   if (p.flags & (EG_OUT_F16 | EG_OUT_E4M3))
     return fail(EG_ERR_UNSUPPORTED, "the unfused path writes bf16 only");
-  if (p.flags & EG_EPI_GATED)
+  if ((p.flags & EG_EPI_GATED) || plan->two_pass_gated)
     return fail(EG_ERR_UNSUPPORTED, "the unfused path has no gated unit");
   eg_status s = validate_args(plan, args, false);
   if (s != EG_OK) return s;
@@ -1085,6 +1147,7 @@ eg_status eg_plan_destroy(eg_plan* plan) {
   if (plan->qs) cudaFree(plan->qs);
   if (plan->counters) cudaFree(plan->counters);
   if (plan->status) cudaFree(plan->status);
+  if (plan->gacc) cudaFree(plan->gacc);
   delete plan;
   return EG_OK;
 }
@@ -1142,6 +1205,8 @@ eg_status eg_linear_noalloc(const eg_problem* problem, const eg_tuning* tuning,
   const eg_problem& p = *problem;
   if (p.flags & EG_RUN_GRAPH)
     return fail(EG_ERR_INVALID_ARG, "eg_linear_noalloc keeps no captured graphs (drop EG_RUN_GRAPH)");
+  if ((p.flags & EG_EPI_GATED) && (p.dtype == EG_IN_INT8 || p.scale == EG_SCALE_BLOCK))
+    return fail(EG_ERR_UNSUPPORTED, "INT8 and Block_FP8 gated units need an accumulator buffer: use a plan");
   if (p.flags & EG_RUN_QUANT_A)
     return fail(EG_ERR_UNSUPPORTED, "eg_linear_noalloc has no buffers for quantised activations "
                                     "(quantise with eg_quantize_rows first)");

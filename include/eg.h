@@ -139,10 +139,16 @@ enum {
                                    bias cover the 2N rows; per output (m, n)
                                    gate = scale * acc[m][n] + bias[n],
                                    up = scale * acc[m][N + n] + bias[N + n],
-                                   y = act(gate) * up (+ R[m][n]).  bf16 or
-                                   E4M3 token/channel inputs; not with
-                                   EG_EPI_RESIDUAL_PRE_ACT, EG_OUT_DEBUG_ACCUM
-                                   or cluster_reduce. */
+                                   y = act(gate) * up (+ R[m][n]).  bf16 and
+                                   E4M3 token/channel inputs: one kernel (no
+                                   cluster_reduce).  INT8 token/channel and
+                                   E4M3 block scales (N % 128 == 0): two
+                                   kernels, the accumulators of all 2N rows
+                                   into a buffer the plan owns, then a
+                                   combine kernel (eg_plan_run_unfused and
+                                   eg_linear_noalloc reject these).  Not with
+                                   EG_EPI_RESIDUAL_PRE_ACT or
+                                   EG_OUT_DEBUG_ACCUM. */
   EG_OUT_F16 = 128,             /* Y is fp16 [M][ldy] (nearest even) */
   EG_OUT_E4M3 = 256             /* Y is E4M3 codes [M][ldy] (one byte each) of
                                    v / s_y with s_y = *eg_args.s_y (computed
@@ -226,7 +232,9 @@ typedef struct eg_plan eg_plan;
 EG_API eg_status eg_plan_create(const eg_problem* problem, const eg_tuning* tuning,
                          eg_plan** out);
 
-/* Bytes of split-K workspace the plan holds (0 when split_k == 1). */
+/* Bytes of device scratch the plan holds: the split-K workspace (0 when
+ * split_k == 1) and, for INT8 / Block_FP8 gated units, the M x 2N
+ * accumulator buffer. */
 EG_API eg_status eg_plan_workspace_bytes(const eg_plan* plan, size_t* out);
 
 /* The tuning the plan runs. */

@@ -742,12 +742,82 @@ def test_gated_unit_narrow_outputs(out):
     assert_close_out(bits(y), oracle.linear_gated(p), out)
 
 
+GATED_TWO_PASS_CASES = [
+    # dtype, scale, M, N, K, tuning of the accumulator GEMM over the 2N rows
+    ("int8", "token_channel", 1, 1024, 2048, None),
+    ("int8", "token_channel", 5, 1000, 1024, dict(tile_n=16, stages=3, split_k=4, swap_ab=1)),
+    ("int8", "token_channel", 24, 512, 1536, dict(tile_n=32, stages=3, split_k=2, swap_ab=1,
+                                                 cluster_reduce=1)),
+    ("int8", "token_channel", 150, 320, 640, dict(tile_n=64, stages=3, split_k=1, swap_ab=0)),
+    ("e4m3", "block", 1, 512, 1024, None),
+    ("e4m3", "block", 9, 384, 768, dict(tile_n=16, stages=3, split_k=2, swap_ab=1)),
+    ("e4m3", "block", 300, 640, 1024, dict(tile_n=256, stages=3, split_k=1, swap_ab=0, stream_k=1)),
+]
+
+
+@pytest.mark.parametrize("dtype,scale,M,N,K,tuning", GATED_TWO_PASS_CASES)
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+def test_gated_unit_int8_and_block(dtype, scale, M, N, K, tuning, act):
+    """INT8 and Block_FP8 gated units: the fused kernel's accumulators of the
+    2N weight rows, then the combine kernel (two launches), against the
+    oracle's gated unit; the accumulator GEMM runs swap-AB, split-K (through
+    the workspace or a cluster), rows over M and balanced split-K."""
+    p = inputs.make_gated_problem(M, N, K, dtype, scale, act=act, bias=True, residual=True, seed=27)
+    plan = make_plan(p, tuning)
+    y, _ = run(p, plan=plan)
+    assert plan.last_launch_count() == 2
+    plan.close()
+    assert_close_rms(bits(y), oracle.linear_gated(p))
+
+
+@pytest.mark.parametrize("out", ["f16", "e4m3"])
+@pytest.mark.parametrize("dtype,scale", [("int8", "token_channel"), ("e4m3", "block")])
+def test_gated_unit_int8_and_block_outputs(dtype, scale, out):
+    p = inputs.make_gated_problem(8, 512, 1024, dtype, scale, act="silu", seed=28)
+    if out == "e4m3":
+        v = (oracle.linear_gated(p).astype(np.uint32) << 16).view(np.float32)
+        p.s_y = float(np.abs(v).max()) / 200.0
+    p.out = out
+    y, _ = run(p)
+    assert_close_out(bits(y), oracle.linear_gated(p), out)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_gated_unit_int8_quant_prologue(graph):
+    """The INT8 gated unit behind the per-token quantisation prologue (bf16
+    activations in; quantisation, accumulator GEMM and combine: three
+    launches, programmatic dependents) gives the same bits as quantising
+    first and running the unit on the codes, in direct and graph mode."""
+    M, N, K = 4, 512, 1024
+    p = inputs.make_gated_problem(M, N, K, "int8", "token_channel", act="silu", bias=True, seed=29)
+    X = torch.from_numpy(inputs.activations_bf16(M, K, seed=29).view(np.int16)).cuda().view(torch.bfloat16)
+    d = to_device(p)
+    plan = eg.Plan(M, N, K, "int8", "token_channel", "silu", bias=True, gated=True, quant_a=True,
+                   pdl=True, graph=graph)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        plan.run(X, d["W"], Y, None, d["s_w"], d["bias"])
+    assert plan.last_launch_count() == 3
+    torch.cuda.synchronize()
+    assert plan.device_status() == eg.EG_OK
+    plan.close()
+    q, s = eg.quantize_rows(X, "int8")
+    ref = make_plan(p)
+    Y2 = torch.empty_like(Y)
+    ref.run(q, d["W"], Y2, s, d["s_w"], d["bias"])
+    torch.cuda.synchronize()
+    ref.close()
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
+
+
 def test_gated_unit_rejections():
-    for kw, status in [(dict(dtype="int8", scale="token_channel"), eg.EG_ERR_UNSUPPORTED),
-                       (dict(dtype="e4m3", scale="block"), eg.EG_ERR_UNSUPPORTED)]:
+    with pytest.raises(eg.EgError) as ei:
+        eg.Plan(4, 200, 512, "e4m3", "block", gated=True)   # up half off a weight block
+    assert ei.value.status == eg.EG_ERR_UNSUPPORTED
+    for kw in (dict(residual=True, residual_pre_act=True), dict(debug_accum=True)):
         with pytest.raises(eg.EgError) as ei:
-            eg.Plan(4, 256, 512, gated=True, **kw)
-        assert ei.value.status == status
+            eg.Plan(4, 256, 512, "int8", "token_channel", gated=True, **kw)
+        assert ei.value.status == eg.EG_ERR_INVALID_ARG
     with pytest.raises(eg.EgError) as ei:
         eg.Plan(4, 256, 512, "e4m3", "token_channel", gated=True,
                 tuning=dict(tile_n=16, stages=4, split_k=4, swap_ab=1, cluster_reduce=1))
