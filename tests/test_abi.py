@@ -42,6 +42,13 @@ BAD = [
     (dict(M=4, N=8, K=133152, dtype="int8", scale="token_channel"), eg.EG_ERR_UNSUPPORTED),
     (dict(M=4, N=8, K=64, flags=eg.EG_EPI_RESIDUAL | eg.EG_EPI_RESIDUAL_PRE_ACT), eg.EG_ERR_INVALID_ARG),
     (dict(M=4, N=8, K=64, flags=1 << 12), eg.EG_ERR_INVALID_ARG),
+    # gated units: block scales need the up half on a weight block; no
+    # pre-activation residual, no accumulator output
+    (dict(M=4, N=200, K=256, dtype="e4m3", scale="block", flags=eg.EG_EPI_GATED), eg.EG_ERR_UNSUPPORTED),
+    (dict(M=4, N=256, K=256, dtype="int8", scale="token_channel",
+          flags=eg.EG_EPI_GATED | eg.EG_EPI_RESIDUAL_PRE_ACT), eg.EG_ERR_INVALID_ARG),
+    (dict(M=4, N=256, K=256, dtype="e4m3", scale="block",
+          flags=eg.EG_EPI_GATED | eg.EG_OUT_DEBUG_ACCUM), eg.EG_ERR_INVALID_ARG),
 ]
 
 

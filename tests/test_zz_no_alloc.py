@@ -137,3 +137,17 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     s = eg.eg_linear_noalloc(prob, t, args, None)
     assert s == eg.EG_ERR_UNSUPPORTED
     assert "scratch" in eg.last_error_detail()
+
+
+@pytest.mark.parametrize("dtype,scale", [("int8", "token_channel"), ("e4m3", "block")])
+def test_noalloc_rejects_two_kernel_gated_units(dtype, scale):
+    """INT8 and Block_FP8 gated units need an [M][2N] accumulator buffer,
+    which only a plan holds."""
+    p = inputs.make_gated_problem(4, 256, 512, dtype, scale, act="silu", seed=2)
+    prob = eg.make_problem(p.M, p.N, p.K, dtype, scale, "silu", eg.EG_EPI_GATED)
+    d = to_device(p)
+    args = eg.eg_args(d["A"].data_ptr(), d["W"].data_ptr(), d["s_a"].data_ptr(),
+                      d["s_w"].data_ptr(), None, None, d["Y"].data_ptr(), p.K, p.K, 0, p.N)
+    s = eg.eg_linear_noalloc(prob, None, args, None)
+    assert s == eg.EG_ERR_UNSUPPORTED
+    assert "accumulator buffer" in eg.last_error_detail()
