@@ -606,7 +606,24 @@ __device__ __forceinline__ void epi_row_words(const KParams& p, int m, int col0,
     const float sa = (SC == SC_TC) ? __ldg(p.s_a + m) : 1.0f;
     const __nv_bfloat16* rrow = has_res ? p.R + static_cast<int64_t>(m) * p.ldr : nullptr;
     float v[CW];
-    if (p.vec_ok && col0 + CW <= p.N) {
+    if (p.vec_ok && col0 + CW <= p.N && !has_bias && !has_res) {
+      // no bias or residual: the scaled, activated accumulator (epi_value's
+      // arithmetic with no epilogue terms), the flag tests out of the loop
+#pragma unroll
+      for (int g = 0; g < CW / 8; ++g) {
+        float4 sw0 = make_float4(1, 1, 1, 1), sw1 = make_float4(1, 1, 1, 1);
+        if (SC == SC_TC) {
+          sw0 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g);
+          sw1 = __ldg(reinterpret_cast<const float4*>(p.s_w + col0) + 2 * g + 1);
+        }
+        const float sws[8] = {sw0.x, sw0.y, sw0.z, sw0.w, sw1.x, sw1.y, sw1.z, sw1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float sc = (SC == SC_TC) ? sa * sws[e] : 1.0f;
+          v[g * 8 + e] = act_c<ACT>(__uint_as_float(vals[g * 8 + e]) * sc);
+        }
+      }
+    } else if (p.vec_ok && col0 + CW <= p.N) {
 #pragma unroll
       for (int g = 0; g < CW / 8; ++g) {
         uint4 bv = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
