@@ -1210,10 +1210,12 @@ __device__ __forceinline__ void reduce_partials(const KParams& p, int tile, int 
 __host__ __device__ constexpr int scale_row_stride(int nk) { return (nk + 3) / 4 * 4 + 4; }
 
 // Block scales of one unit into a shared-memory buffer, with asynchronous
-// copies (the caller commits and waits): sc_a[t][i] = s_a of tile row (or,
-// with swap-AB, column) t at K block kt0 + i, row stride
-// scale_row_stride(nk), zero beyond M; then sc_w[i] of the tile's weight
-// block row.  16-byte copies when the rows' pieces are 16-byte aligned.
+// copies (the caller commits and waits): sc_a[t][i] = s_a of tile row t at
+// K block kt0 + i, row stride scale_row_stride(nk), zero beyond M; with
+// swap-AB (t a tile column, i.e. a token) K-block-major instead,
+// sc_a[i][t] (row length BN), so that a thread reads a K block's token
+// scales as 16-byte vectors; then sc_w[i] of the tile's weight block row.
+// 16-byte copies when the rows' pieces are 16-byte aligned.
 template <bool SWAP, int BN, int NT>
 __device__ __forceinline__ void stage_block_scales(const KParams& p, const Unit& w, float* buf,
                                                    int ept) {
@@ -1222,7 +1224,15 @@ __device__ __forceinline__ void stage_block_scales(const KParams& p, const Unit&
   const int ss = scale_row_stride(w.nk);
   float* sc_a = buf;
   float* sc_w = buf + T * ss;
-  if ((p.kb_count & 3) == 0 && (w.kt0 & 3) == 0 && (w.nk & 3) == 0) {
+  if constexpr (SWAP) {
+    for (int idx = ept; idx < T * w.nk; idx += NT) {
+      const int i = idx / T, t = idx - i * T;
+      const int m = base + t;
+      const bool ok = m < p.M;
+      const float* src = p.s_a + (ok ? static_cast<int64_t>(m) * p.kb_count + w.kt0 + i : 0);
+      cp_async_4(sc_a + i * T + t, src, ok ? 4u : 0u);
+    }
+  } else if ((p.kb_count & 3) == 0 && (w.kt0 & 3) == 0 && (w.nk & 3) == 0) {
     const int q = w.nk >> 2;
     for (int idx = ept; idx < T * q; idx += NT) {
       const int t = idx / q, c = idx - t * q;
@@ -1933,6 +1943,14 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           cp_async_commit();
           cp_async_wait<0>();
           epi_bar_sync(C::kEpiThreads);
+          if constexpr (SWAP) {
+            // the tile's weight block row is one scale per K block: fold it
+            // in, sc_a[i][t] = s_w[i] * s_a[t][i] (the product the promotion
+            // applies), so a K block's promotion reads one vector per 4 tokens
+            for (int idx = ept; idx < BN * w.nk; idx += C::kEpiThreads)
+              sc_a[idx] = sc_w[idx / BN] * sc_a[idx];
+            epi_bar_sync(C::kEpiThreads);
+          }
         }
         if constexpr (C::kWidePromote) {
           // 128 running sums per thread: one row (m) and the 128 columns of
@@ -2004,15 +2022,29 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&tempty[b]);  // the buffer is free once the values are in registers
+          if constexpr (SC == SC_BLOCK && SWAP) {
+            // s_w[i] * s_a[token][i] of this thread's tokens (0 beyond M),
+            // four per 16-byte read
+            const float4* sp = reinterpret_cast<const float4*>(sc_a + i * BN + cbeg);
 #pragma unroll
-          for (int c = 0; c < CPT; ++c) {
-            if constexpr (SC == SC_BLOCK) {
-              float s = srow;
-              if (SWAP) s = srow * sc_a[(cbeg + c) * ss + i];  // 0 beyond M
-              acc[c] = __float_as_uint(__fmaf_rn(s, __uint_as_float(r[c]), __uint_as_float(acc[c])));
-            } else {
-              acc[c] = static_cast<uint32_t>(static_cast<int32_t>(acc[c]) +
-                                             __float2int_rn(__uint_as_float(r[c])));
+            for (int c4 = 0; c4 < CPT / 4; ++c4) {
+              const float4 s = sp[c4];
+              const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * c4 + e;
+                acc[c] = __float_as_uint(__fmaf_rn(sv[e], __uint_as_float(r[c]), __uint_as_float(acc[c])));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+              if constexpr (SC == SC_BLOCK) {
+                acc[c] = __float_as_uint(__fmaf_rn(srow, __uint_as_float(r[c]), __uint_as_float(acc[c])));
+              } else {
+                acc[c] = static_cast<uint32_t>(static_cast<int32_t>(acc[c]) +
+                                               __float2int_rn(__uint_as_float(r[c])));
+              }
             }
           }
         }
