@@ -488,7 +488,7 @@ __device__ __forceinline__ uint32_t pick(const uint32_t (&v)[CW], int j) {
   return x;
 }
 
-template <int IN, int SC, int CW, int ACT>
+template <int IN, int SC, int CW, int ACT, int OF = -1>
 __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
                                            const uint32_t (&vals)[CW], const SwapIn<CW>& in) {
   if (n >= p.N) return;
@@ -511,13 +511,18 @@ __device__ __forceinline__ void store_swap(const KParams& p, int n, int col0,
     for (int q = 0; q < 4; ++q) {
       if (j0 + q < count) {
         uint16_t o;
-        if (IN == IN_INT8)
+        if (IN == IN_INT8) {
           o = epi_int8<ACT>(static_cast<int32_t>(v[q]), sa[q], in.sw, in.b, r[q], p.flags, p.out, sy);
+        } else {
+          const float y = epi_value<ACT>(__uint_as_float(v[q]), (SC == SC_TC) ? sa[q] * in.sw : 1.0f,
+                                         in.b, r[q], p.flags);
+          o = (OF == OUT_BF16) ? __bfloat16_as_ushort(__float2bfloat16_rn(y)) : out_bits(y, p.out, sy);
+        }
+        const int64_t at = static_cast<int64_t>(col0 + j0 + q) * p.ldy + n;
+        if (OF == OUT_BF16)
+          reinterpret_cast<uint16_t*>(p.Y)[at] = o;
         else
-          o = out_bits(epi_value<ACT>(__uint_as_float(v[q]), (SC == SC_TC) ? sa[q] * in.sw : 1.0f,
-                                      in.b, r[q], p.flags),
-                       p.out, sy);
-        store_out(p, static_cast<int64_t>(col0 + j0 + q) * p.ldy + n, o);
+          store_out(p, at, o);
       }
     }
   }
@@ -1346,7 +1351,7 @@ __device__ __forceinline__ RowIn cluster_row_inputs(const KParams& p, int row) {
 // 4-column groups e / R, + T / R, ... (T = epilogue threads, a multiple of
 // R): the group's global loads and S 16-byte partial reads first, then its
 // arithmetic and stores.  False on timeout.
-template <int IN, int SC, bool SWAP, int BN, int T, int ACT>
+template <int IN, int SC, bool SWAP, int BN, int T, int ACT, int OF = -1>
 __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uint32_t* red,
                                                      uint64_t* red_full, const Unit& w, int ept,
                                                      const RowIn& in) {
@@ -1405,13 +1410,17 @@ __device__ __forceinline__ bool cluster_reduce_store(const KParams& p, const uin
       const float sa = SWAP ? cs[g] : in.s, sw = SWAP ? in.s : cs[g];
       const float bias = SWAP ? in.b : cb[g];
       uint16_t o;
-      if (IN == IN_INT8)
+      if (IN == IN_INT8) {
         o = epi_int8<ACT>(static_cast<int32_t>(acc[g]), sa, sw, bias, rv[g], p.flags, p.out, sy);
+      } else {
+        const float y = epi_value<ACT>(__uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f,
+                                       bias, rv[g], p.flags);
+        o = (OF == OUT_BF16) ? __bfloat16_as_ushort(__float2bfloat16_rn(y)) : out_bits(y, p.out, sy);
+      }
+      if (OF == OUT_BF16)
+        reinterpret_cast<uint16_t*>(p.Y)[at] = o;
       else
-        o = out_bits(epi_value<ACT>(__uint_as_float(acc[g]), (SC == SC_TC) ? sa * sw : 1.0f,
-                                    bias, rv[g], p.flags),
-                     p.out, sy);
-      store_out(p, at, o);
+        store_out(p, at, o);
     }
   }
   return true;
@@ -2188,8 +2197,14 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
           mbar_arrive(&tempty[b]);
           ++blk;
           bool red_ok = false;
-          EG_ACT_DISPATCH(p.act, (red_ok = cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads, A_>(
-                                      p, red_buf, red_full, w, ept, rin)))
+          // decode's usual bf16 output: a narrowing chosen at compile time
+          if (SWAP && p.out == OUT_BF16) {
+            EG_ACT_DISPATCH(p.act, (red_ok = cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads, A_,
+                                                                  OUT_BF16>(p, red_buf, red_full, w, ept, rin)))
+          } else {
+            EG_ACT_DISPATCH(p.act, (red_ok = cluster_reduce_store<IN, SC, SWAP, BN, C::kEpiThreads, A_>(
+                                        p, red_buf, red_full, w, ept, rin)))
+          }
           if (!red_ok) {
             record_status(p.status, ST_TIMEOUT_EPILOGUE);
             ok = false;
@@ -2256,7 +2271,11 @@ __global__ void __launch_bounds__(Cfg<IN, SC, SWAP, BN, G, PR>::kThreads)
             }
             if constexpr (kPre) {
               if (!(p.flags & F_DEBUG)) {
-                EG_ACT_DISPATCH(p.act, (store_swap<IN, SC, CW, A_>(p, row, w.col0, r, pre)))
+                if (p.out == OUT_BF16) {
+                  EG_ACT_DISPATCH(p.act, (store_swap<IN, SC, CW, A_, OUT_BF16>(p, row, w.col0, r, pre)))
+                } else {
+                  EG_ACT_DISPATCH(p.act, (store_swap<IN, SC, CW, A_>(p, row, w.col0, r, pre)))
+                }
                 continue;
               }
             }
